@@ -1,0 +1,418 @@
+"""Throughput benchmark: causal RoPE GQA attention forward + backward on GB300.
+
+One step = attn_fwd + attn_bwd (every kernel of the hot path) over one batch
+of seeded synthetic bf16 inputs of the chosen workload (default: the
+Llama-3-8B attention layer, B=1, Hq=32, Hkv=8, S=4096, D=128). Prints one
+JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+value: causal-pair FLOPs (fwd 4*D, bwd 10*D per unmasked (query, key) pair)
+of all ranks / device time of K steps (CUDA events on the launching stream,
+L2 flushed between steps, inputs resident in HBM). e2e: the same metric with
+host buffers: each step copies the inputs from pinned host memory, runs the
+C-ABI calls and copies every output back. roofline: the dominant kernel's
+achieved TFLOP/s from library-recorded CUDA events over the timed region,
+against the measured dense bf16 peak. cpu_baseline: the fp64 oracle on a
+bounded sample, on this host's cores. --impl reference times that oracle as
+the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mqa_attention_gb300 import inputs as I  # noqa: E402
+from mqa_attention_gb300.workloads import WORKLOADS, by_name  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama3_8b_gqa_s4096"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in WORKLOADS])
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ inputs
+def host_inputs(wl, rank):
+    """Seeded bf16 bit patterns (uint16) per tensor; ranks draw distinct streams."""
+    return {n: I.normal_bf16_bits(I.seed_for(wl.index, n) + 100 * rank, s)
+            for n, s in wl.shapes().items()}
+
+
+def to_bf16_tensor(bits, device=None, pin=False):
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    if pin:
+        return t.pin_memory()
+    return t.to(device) if device is not None else t
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons (200 ms period)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.rows if t0 <= t <= t1 + 0.2]
+        used = inside if inside else [r for _, r in self.rows]
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in used:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample_heads(wl, host, budget_s=10.0):
+    """fp64 oracle forward + backward of whole query heads (each with its KV
+    head) until `budget_s` of CPU time is spent. Returns (TFLOP/s, heads, s)."""
+    import oracle as O
+
+    f = {n: torch.from_numpy(I.bf16_bits_to_f64(host[n])) for n in host}
+    G = wl.Hq // wl.Hkv
+    per_head = (4 + (10 if wl.backward else 0)) * wl.D * (wl.S * (wl.S + 1) // 2)
+    t0 = time.perf_counter()
+    done = 0
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            g = h // G
+            q = f["q"][b:b + 1, h:h + 1]
+            k, v = f["k"][b:b + 1, g:g + 1], f["v"][b:b + 1, g:g + 1]
+            O.attention_forward(q, k, v, wl.scale, wl.theta, wl.causal)
+            if wl.backward:
+                O.attention_backward(q, k, v, f["dout"][b:b + 1, h:h + 1], wl.scale, wl.theta,
+                                     wl.causal)
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done * per_head / dt / 1e12, done, dt
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    """The fp64 oracle timed as the reference arm (rank 0 only). Each step: the
+    out, lse and dq rows of 64 query rows of one head (rows spread over the
+    sequence), credited 10*D FLOPs per causal pair of those rows (Q.Kᵀ, P.V,
+    recomputed Q.Kᵀ, dO.Vᵀ, dS.K)."""
+    if rank != 0:
+        return
+    import oracle as O
+
+    wl = by_name(args.workload)
+    host = host_inputs(wl, 0)
+    f = {n: torch.from_numpy(I.bf16_bits_to_f64(host[n])) for n in host}
+    G = wl.Hq // wl.Hkv
+    R = 64
+    rng = np.random.default_rng(12345)
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        h = step % wl.Hq
+        b = (step // wl.Hq) % wl.B
+        rows = torch.from_numpy(np.sort(rng.choice(wl.S, size=R, replace=False)))
+        q = f["q"][b:b + 1, h:h + 1]
+        k, v = f["k"][b:b + 1, h // G:h // G + 1], f["v"][b:b + 1, h // G:h // G + 1]
+        t0 = time.perf_counter()
+        O.forward_rows(q, k, v, rows, wl.scale, wl.theta, wl.causal)
+        O.backward_dq_rows(q, k, v, f["dout"][b:b + 1, h:h + 1], rows, wl.scale, wl.theta,
+                           wl.causal)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            pairs = int((rows + 1).sum()) if wl.causal else R * wl.S
+            flops.append(10 * wl.D * pairs)
+    total = sum(times)
+    value = sum(flops) / total / 1e12
+    unit = "TFLOP/s"
+    line = {
+        "impl": "reference",
+        "metric": "causal GQA attn fwd+bwd TFLOP/s (fp64 CPU oracle)",
+        "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic N(0,1) bf16 inputs, seeded",
+        "config": config_of(wl, args.gpus, l2="n/a (host)"),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": torch.get_num_threads(),
+                         "kind": "oracle",
+                         "sample": f"per step {R} query rows of one head (out, lse, dq)"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, n, l2):
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
+            "rope_theta": wl.theta, "causal": wl.causal,
+            "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
+            "l2": l2}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local):
+    import mqa_attention_gb300 as M
+    from mqa_attention_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (GB300)")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    barrier(world)
+    M.lib()
+    wl = by_name(args.workload)
+    host = host_inputs(wl, rank)
+    dev = {n: to_bf16_tensor(h, "cuda") for n, h in host.items()}
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["dout"]
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, wl.S), dtype=torch.float32, device="cuda")
+    dq = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(k.shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    dims = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, wl.scale, wl.causal)
+
+    def step():
+        M.attn_fwd(q, k, v, out, lse, *dims, stream=stream)
+        if wl.backward:
+            M.attn_bwd(q, k, v, out, lse, do, dq, dk, dv, *dims, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if M.sync_status() != 0:
+        raise SystemExit("device status error during warm-up")
+
+    sampler = ClockSampler(local)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    M.profile_begin(max(4096, 2 * args.steps))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between steps (outside the events)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    M.profile_end()
+    status = M.sync_status()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world)
+    kern = {}
+    for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
+                       (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
+                       (M.KERNEL_DQ_FINAL, "dq_finalize")):
+        n, tot = M.profile_query(kind)
+        if n:
+            kern[name] = {"launches": n, "avg_ms": tot / n}
+    launches_per_step = 2 + 1 + ((2 + 1 + 1) if wl.backward else 0)
+
+    # ---- end to end through host buffers
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
+    hp = {n: to_bf16_tensor(h, pin=True) for n, h in host.items()}
+    ho = {"out": torch.empty(out.shape, dtype=torch.bfloat16).pin_memory(),
+          "lse": torch.empty(lse.shape, dtype=torch.float32).pin_memory()}
+    if wl.backward:
+        for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            ho[n] = torch.empty(t.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for n, t in hp.items()
+              if wl.backward or n != "dout")
+    d2h = sum(t.numel() * t.element_size() for t in ho.values())
+
+    def e2e_step():
+        q.copy_(hp["q"], non_blocking=True)
+        k.copy_(hp["k"], non_blocking=True)
+        v.copy_(hp["v"], non_blocking=True)
+        if wl.backward:
+            do.copy_(hp["dout"], non_blocking=True)
+        step()
+        ho["out"].copy_(out, non_blocking=True)
+        ho["lse"].copy_(lse, non_blocking=True)
+        if wl.backward:
+            ho["dq"].copy_(dq, non_blocking=True)
+            ho["dk"].copy_(dk, non_blocking=True)
+            ho["dv"].copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    if rank != 0:
+        return
+    peak_tf, peak_hbm, peak_src = peaks()
+    total_flops = wl.flops * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    # dominant kernel: the one with the largest share of the step
+    dom = max(kern.items(), key=lambda kv: kv[1]["avg_ms"])
+    algo_flops = {"attn_fwd": wl.fwd_flops, "attn_bwd_main": wl.bwd_flops}
+    roof = None
+    if dom[0] in algo_flops:
+        achieved = algo_flops[dom[0]] / (dom[1]["avg_ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "step_frac_of_peak": value / world / peak_tf}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tf, heads, secs = oracle_sample_heads(wl, host)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": f"{heads} of {wl.B * wl.Hq} query heads, full S={wl.S}, "
+                         f"fwd{'+bwd' if wl.backward else ''} in fp64 ({secs:.1f} s)"}
+    line = {
+        "metric": "causal GQA attn fwd+bwd TFLOP/s (Llama-3-8B S=4096 shape), % of GB300 bf16 "
+                  "peak in roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
+        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)"),
+        "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "kernels_ms": {n: round(d["avg_ms"], 5) for n, d in kern.items()},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,134 @@
+/*
+ * mqa_attention_gb300 — C ABI of a CUDA library for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes causal self-attention with rotary position embedding
+ * (RoPE) applied to Q and K, grouped-query / multi-query K/V sharing and a
+ * numerically stable (online) softmax, forward and backward:
+ *
+ *   q~_i = R_i q_i,  k~_j = R_j k_j                  (half-split RoPE)
+ *   s_ij = scale * q~_i . k~_j,  j <= i when causal
+ *   lse_i = ln sum_j exp(s_ij),  P_ij = exp(s_ij - lse_i)
+ *   out_i = sum_j P_ij v_j
+ *
+ * Sources (web pages, cited by title and section):
+ *   "Picotron模型实现解析Llama架构与Flash Attention集成", §1 嵌入层与位置编码
+ *     (apply_rotary_pos_emb: x*cos + rotate_half(x)*sin, rotate_half = cat(-x2, x1)),
+ *     §2 注意力机制实现 (flash_attn_func(q, k, v, causal)), §Flash Attention的优势
+ *     (IO-aware tiling that never stores the S x S score matrix);
+ *   "深度学习系统设计llama3-from-scratch：并行计算架构", §键值（Key-Value）共享机制
+ *     (32 query heads share 8 key/value heads), §RoPE位置编码的并行实现,
+ *     §注意力得分矩阵计算 (q.kᵀ / sqrt(head_dim)), §因果掩码的并行应用, §Softmax的并行计算;
+ *   "ColossalAI 中的 PaLM 教学实现不到 200 行核心代码与 Booster 分布式训练实战",
+ *     §2.3 RotaryEmbedding (inv_freq = 1/theta^(2i/dim), cat(freqs, freqs), both q and k
+ *     rotated), §2.5 Attention (multi-query: one K/V head for all query heads; upper
+ *     triangle masked; row maximum subtracted before the softmax).
+ *
+ * Conventions shared by every entry point
+ *   Layout   q, out, dq: [B, Hq, S, D]; k, v, dk, dv: [B, Hkv, S, D]; lse: [B, Hq, S];
+ *            all contiguous row-major, D innermost.
+ *   Heads    query head h reads K/V head h / (Hq / Hkv) (contiguous groups).
+ *   RoPE     half-split: for i < D/2, angle = p * theta^(-2i/D) at position p = 0..S-1;
+ *            y_i = x_i cos - x_{i+D/2} sin, y_{i+D/2} = x_{i+D/2} cos + x_i sin.
+ *            The rotated q and k are rounded to bf16 before the score product.
+ *   Sizes    D in {64, 128}; S a positive multiple of 128; Hq a multiple of Hkv;
+ *            B * Hq * S < 2^31.
+ *   Pointers device pointers, 16-byte aligned, not aliasing one another. The caller owns
+ *            every buffer; the library never frees or keeps them.
+ *   Stream   all work is enqueued on `stream` (a cudaStream_t, or 0); no call
+ *            synchronises with the host except where stated. Temporary workspace is
+ *            taken from a library-owned stream-ordered pool on the current device.
+ *   Device   the current CUDA device must be an sm_103 GPU (GB300).
+ *   Errors   every entry point returns ATTN_OK (0) or one of the codes below and writes
+ *            nothing when it rejects its arguments. Device-side failures of a launched
+ *            kernel (a wait that exceeded its time limit) are reported by
+ *            attn_sync_status().
+ */
+#ifndef MQA_ATTENTION_GB300_ATTN_H_
+#define MQA_ATTENTION_GB300_ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* same type as cudaStream_t */
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = 1,     /* null / misaligned pointer, non-positive size, Hq % Hkv != 0,
+                               non-finite or non-positive scale or theta, size overflow */
+  ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, S % 128 != 0, or device is not sm_103 */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (see attn_sync_status) */
+};
+
+/* Forward pass.
+ *   q    [B,Hq,S,D]  bf16, read
+ *   k, v [B,Hkv,S,D] bf16, read
+ *   out  [B,Hq,S,D]  bf16, written: softmax(scale * q~ k~ᵀ + mask) v
+ *   lse  [B,Hq,S]    fp32, written: natural-log log-sum-exp of each score row
+ *   rope_theta > 0 (RoPE base), scale > 0 (score multiplier, usually 1/sqrt(D)),
+ *   causal != 0 masks keys after the query (j > i); causal == 0 attends to all keys.
+ * Sources: Picotron §1, §2; llama3-from-scratch §注意力得分矩阵计算, §因果掩码的并行应用,
+ *   §Softmax的并行计算; PaLM §2.3, §2.5 (see the file header). */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float rope_theta, float scale, int causal,
+             attn_stream_t stream);
+
+/* Backward pass of attn_fwd with respect to q, k and v, for L = sum(dout * out).
+ *   q, k, v, out (bf16) and lse (fp32) as produced by / given to attn_fwd;
+ *   dout [B,Hq,S,D] bf16, read;
+ *   dq [B,Hq,S,D], dk, dv [B,Hkv,S,D]: fp32, written (fully overwritten).
+ *   dk and dv sum the contributions of all Hq/Hkv query heads of each group.
+ * With dP_ij = dout_i.v_j, delta_i = dout_i.out_i, dS_ij = P_ij (dP_ij - delta_i):
+ *   dq_i = scale R_iᵀ sum_j dS_ij k~_j,  dk_j = scale R_jᵀ sum_{h,i} dS_ij q~_i,
+ *   dv_j = sum_{h,i} P_ij dout_i.
+ * lse is treated as an input that is not differentiated. The gradient formulas are the
+ * chain rule through the forward definition above (no page writes them out). */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+             int D, float rope_theta, float scale, int causal, attn_stream_t stream);
+
+/* Waits for all work on `stream`, then reads and clears the device status word of the
+ * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait since the
+ * last call (its outputs are then undefined). Synchronises the host with `stream`. */
+int attn_sync_status(attn_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(int status);
+
+/* Kernel timing with CUDA events recorded on the launching stream around every kernel
+ * the library launches. attn_profile_begin clears previous records and enables
+ * recording (at most `max_launches` launches per kernel kind are kept);
+ * attn_profile_end disables it. attn_profile_query synchronises the recorded events and
+ * returns the number of recorded launches of `kernel` and their summed duration in ms.
+ * Kernel kinds: 0 rope (forward RoPE pre-pass), 1 forward attention, 2 backward
+ * pre-pass, 3 backward dK/dV/dQ main kernel, 4 dQ finalisation. */
+enum {
+  ATTN_KERNEL_ROPE = 0,
+  ATTN_KERNEL_FWD = 1,
+  ATTN_KERNEL_BWD_PREP = 2,
+  ATTN_KERNEL_BWD_MAIN = 3,
+  ATTN_KERNEL_DQ_FINAL = 4,
+  ATTN_NUM_KERNELS = 5
+};
+int attn_profile_begin(int max_launches);
+int attn_profile_end(void);
+int attn_profile_query(int kernel, int* launches, float* total_ms);
+
+/* Fault-path testing: while `enable` is non-zero, the main kernels of subsequent
+ * attn_fwd / attn_bwd calls wait on a barrier that nothing signals, so the wait expires
+ * after its time limit (about two seconds), the kernel unwinds, releases its tensor
+ * memory and reports ATTN_ERR_TIMEOUT through attn_sync_status(). Outputs of such a
+ * call are undefined. Not for production use. */
+int attn_debug_inject_timeout(int enable);
+
+/* Library version string. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_ATTENTION_GB300_ATTN_H_ */

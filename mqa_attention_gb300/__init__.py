@@ -1,0 +1,211 @@
+"""Python binding of the mqa_attention_gb300 C ABI (include/attn.h).
+
+Argument marshalling only: every step of the attention computation runs in
+the CUDA kernels of ``libmqa_attention_gb300.so``. There is no CPU fallback;
+calling into the library without the built shared library raises.
+
+Tensors are passed as ``torch.Tensor`` (their device pointer is used) or as
+raw integer device pointers. The stream defaults to torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "AttnError",
+    "lib",
+    "attn_fwd",
+    "attn_bwd",
+    "forward",
+    "backward",
+    "sync_status",
+    "status_string",
+    "profile_begin",
+    "profile_end",
+    "profile_query",
+    "debug_inject_timeout",
+    "version",
+    "EXPORTED_SYMBOLS",
+    "KERNEL_ROPE",
+    "KERNEL_FWD",
+    "KERNEL_BWD_PREP",
+    "KERNEL_BWD_MAIN",
+    "KERNEL_DQ_FINAL",
+]
+
+LIB_NAME = "libmqa_attention_gb300.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL = range(5)
+
+EXPORTED_SYMBOLS = (
+    "attn_fwd",
+    "attn_bwd",
+    "attn_sync_status",
+    "attn_status_string",
+    "attn_profile_begin",
+    "attn_profile_end",
+    "attn_profile_query",
+    "attn_debug_inject_timeout",
+    "attn_version",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (loaded on first use; raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_NAME} is not built; run `python -m mqa_attention_gb300.build` "
+                    "(or __graft_entry__.build())"
+                )
+            L = ctypes.CDLL(LIB_PATH)
+            L.attn_fwd.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P]
+            L.attn_fwd.restype = _I
+            L.attn_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _I, _I, _I, _I, _I, _F, _F, _I, _P]
+            L.attn_bwd.restype = _I
+            L.attn_sync_status.argtypes = [_P]
+            L.attn_sync_status.restype = _I
+            L.attn_status_string.argtypes = [_I]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_profile_begin.argtypes = [_I]
+            L.attn_profile_begin.restype = _I
+            L.attn_profile_end.argtypes = []
+            L.attn_profile_end.restype = _I
+            L.attn_profile_query.argtypes = [_I, ctypes.POINTER(_I), ctypes.POINTER(_F)]
+            L.attn_profile_query.restype = _I
+            L.attn_debug_inject_timeout.argtypes = [_I]
+            L.attn_debug_inject_timeout.restype = _I
+            L.attn_version.argtypes = []
+            L.attn_version.restype = ctypes.c_char_p
+            _lib = L
+        return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, what: str):
+    if code != ATTN_OK:
+        raise AttnError(code, what)
+
+
+def attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, stream=None):
+    """C ABI attn_fwd: out (bf16) and lse (fp32) from q, k, v (bf16)."""
+    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
+                          int(Hkv), int(S), int(D), float(rope_theta), float(scale),
+                          1 if causal else 0, _stream(stream)), "attn_fwd")
+
+
+def attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
+             stream=None):
+    """C ABI attn_bwd: dq, dk, dv (fp32) from q, k, v, out, dout (bf16) and lse (fp32)."""
+    _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                          _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S), int(D),
+                          float(rope_theta), float(scale), 1 if causal else 0,
+                          _stream(stream)), "attn_bwd")
+
+
+def _shapes(q, k):
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    return B, Hq, Hkv, S, D
+
+
+def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None):
+    """Allocates out / lse like q and runs attn_fwd. q: [B,Hq,S,D], k, v: [B,Hkv,S,D]."""
+    import torch
+
+    B, Hq, Hkv, S, D = _shapes(q, k)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, stream)
+    return out, lse
+
+
+def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None):
+    """Allocates fp32 dq, dk, dv and runs attn_bwd."""
+    import torch
+
+    B, Hq, Hkv, S, D = _shapes(q, k)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
+             stream)
+    return dq, dk, dv
+
+
+def sync_status(stream=None) -> int:
+    """Synchronises `stream` and returns (and clears) the device status code."""
+    return lib().attn_sync_status(_stream(stream))
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().attn_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def profile_begin(max_launches: int = 4096):
+    _check(lib().attn_profile_begin(int(max_launches)), "attn_profile_begin")
+
+
+def profile_end():
+    _check(lib().attn_profile_end(), "attn_profile_end")
+
+
+def profile_query(kernel: int):
+    """(launches, total_ms) recorded for one kernel kind since profile_begin."""
+    n = _I(0)
+    ms = _F(0.0)
+    _check(lib().attn_profile_query(int(kernel), ctypes.byref(n), ctypes.byref(ms)),
+           "attn_profile_query")
+    return n.value, ms.value
+
+
+def debug_inject_timeout(enable: bool):
+    _check(lib().attn_debug_inject_timeout(1 if enable else 0), "attn_debug_inject_timeout")
+
+
+def version() -> str:
+    return lib().attn_version().decode()

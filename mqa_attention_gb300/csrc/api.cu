@@ -1,0 +1,406 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// per-device state (status word, workspace pool, RoPE table cache), TMA tensor
+// maps, kernel launches and optional per-kernel event timing.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+using gbattn::kTile;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int* status = nullptr;            // device status word
+  cudaMemPool_t pool = nullptr;     // library-owned stream-ordered pool
+  std::map<std::tuple<int, int, uint64_t>, std::pair<float*, float*>> rope;  // (S, D, theta bits)
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+bool g_inject_timeout = false;
+
+// ------------------------------------------------------------------ profiling
+struct Profile {
+  bool on = false;
+  int cap = 0;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> rec[ATTN_NUM_KERNELS];
+  std::vector<cudaEvent_t> spare;
+};
+Profile g_prof;
+
+cudaEvent_t take_event() {
+  if (!g_prof.spare.empty()) {
+    cudaEvent_t e = g_prof.spare.back();
+    g_prof.spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Records events around one launch when profiling is on.
+struct LaunchTimer {
+  int kind;
+  cudaStream_t stream;
+  cudaEvent_t start = nullptr, stop = nullptr;
+  LaunchTimer(int k, cudaStream_t s) : kind(k), stream(s) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_prof.on || static_cast<int>(g_prof.rec[kind].size()) >= g_prof.cap) return;
+    start = take_event();
+    stop = take_event();
+    if (start && stop) cudaEventRecord(start, stream);
+  }
+  void done() {
+    if (!start || !stop) return;
+    cudaEventRecord(stop, stream);
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_prof.rec[kind].emplace_back(start, stop);
+  }
+};
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 matrix [rows][D], 128-byte swizzled boxes of {64 columns, box_rows rows}.
+bool make_map(CUtensorMap* m, const void* ptr, long long rows, int D, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const void* const* ptrs, int nptr, int B, int Hq, int Hkv, int S, int D, float theta,
+             float scale) {
+  for (int i = 0; i < nptr; ++i)
+    if (!aligned16(ptrs[i])) return ATTN_ERR_INVALID;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID;
+  if (!std::isfinite(theta) || theta <= 0.f || !std::isfinite(scale) || scale <= 0.f)
+    return ATTN_ERR_INVALID;
+  if (static_cast<long long>(B) * Hq * S >= (1LL << 31)) return ATTN_ERR_INVALID;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (S % kTile != 0) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// Current device's state, initialised on first use. Returns an ATTN_* code.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    d.supported = major == 10 && minor == 3;
+    if (d.supported) {
+      if (cudaMalloc(&d.status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (cudaMemset(d.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
+      uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse by later calls
+      cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    d.init = true;
+  }
+  if (!d.supported) return ATTN_ERR_UNSUPPORTED;
+  *out = &d;
+  return ATTN_OK;
+}
+
+// cos/sin table for (S, D, theta); built on first use (the stream is then
+// synchronised once so that the table is complete for every later stream).
+int rope_table(DeviceState* d, int S, int D, float theta, cudaStream_t stream, float** cs,
+               float** sn) {
+  uint32_t tb;
+  std::memcpy(&tb, &theta, 4);
+  const auto key = std::make_tuple(S, D, static_cast<uint64_t>(tb));
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = d->rope.find(key);
+    if (it != d->rope.end()) {
+      *cs = it->second.first;
+      *sn = it->second.second;
+      return ATTN_OK;
+    }
+  }
+  const size_t n = static_cast<size_t>(S) * (D / 2);
+  float* buf = nullptr;
+  if (cudaMalloc(&buf, 2 * n * sizeof(float)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (gbattn::launch_rope_table(buf, buf + n, S, D, static_cast<double>(theta), stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaFree(buf);
+    return ATTN_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto ins = d->rope.emplace(key, std::make_pair(buf, buf + n));
+  if (!ins.second) cudaFree(buf);  // another thread built it meanwhile
+  *cs = ins.first->second.first;
+  *sn = ins.first->second.second;
+  return ATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_version(void) { return "mqa_attention_gb300 0.1.0 (sm_103a)"; }
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported size or device";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float rope_theta, float scale, int causal,
+             attn_stream_t stream_) {
+  const void* ptrs[] = {q, k, v, out, lse};
+  int st = validate(ptrs, 5, B, Hq, Hkv, S, D, rope_theta, scale);
+  if (st != ATTN_OK) return st;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ATTN_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  float *cs = nullptr, *sn = nullptr;
+  if ((st = rope_table(d, S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+
+  const long long qrows = static_cast<long long>(B) * Hq * S;
+  const long long krows = static_cast<long long>(B) * Hkv * S;
+  const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
+  const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
+  uint8_t* ws = nullptr;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), qbytes + kbytes, d->pool, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  void* qr = ws;
+  void* kr = ws + qbytes;
+
+  bool ok = true;
+  {
+    gbattn::RowPrepParams rp{};
+    rp.S = S;
+    rp.D = D;
+    rp.cos_tab = cs;
+    rp.sin_tab = sn;
+    LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
+    rp.x = q; rp.y = qr; rp.rows = qrows;
+    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
+    rp.x = k; rp.y = kr; rp.rows = krows;
+    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
+    tm.done();
+  }
+  gbattn::FwdParams fp{};
+  ok = ok && make_map(&fp.map_q, qr, qrows, D, kTile) && make_map(&fp.map_k, kr, krows, D, kTile) &&
+       make_map(&fp.map_v, v, krows, D, kTile) && make_map(&fp.map_out, out, qrows, D, kTile);
+  if (ok) {
+    fp.lse = lse;
+    fp.status = d->status;
+    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.S = S; fp.D = D;
+    fp.scale_log2 = scale * 1.4426950408889634f;
+    fp.causal = causal ? 1 : 0;
+    fp.inject_timeout = g_inject_timeout ? 1 : 0;
+    LaunchTimer tm(ATTN_KERNEL_FWD, stream);
+    ok = gbattn::launch_fwd(fp, stream) == cudaSuccess;
+    tm.done();
+  }
+  cudaFreeAsync(ws, stream);
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+             int D, float rope_theta, float scale, int causal, attn_stream_t stream_) {
+  const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv};
+  int st = validate(ptrs, 9, B, Hq, Hkv, S, D, rope_theta, scale);
+  if (st != ATTN_OK) return st;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ATTN_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  float *cs = nullptr, *sn = nullptr;
+  if ((st = rope_table(d, S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+
+  const long long qrows = static_cast<long long>(B) * Hq * S;
+  const long long krows = static_cast<long long>(B) * Hkv * S;
+  const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
+  const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
+  const size_t accbytes = round256(static_cast<size_t>(qrows) * D * 4);
+  const size_t rowbytes = round256(static_cast<size_t>(qrows) * 4);
+  uint8_t* ws = nullptr;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
+                              qbytes + kbytes + accbytes + 2 * rowbytes, d->pool,
+                              stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  void* qr = ws;
+  void* kr = ws + qbytes;
+  float* dqacc = reinterpret_cast<float*>(ws + qbytes + kbytes);
+  float* delta = reinterpret_cast<float*>(ws + qbytes + kbytes + accbytes);
+  float* lse2 = reinterpret_cast<float*>(ws + qbytes + kbytes + accbytes + rowbytes);
+
+  bool ok = true;
+  {
+    gbattn::RowPrepParams rp{};
+    rp.S = S;
+    rp.D = D;
+    rp.cos_tab = cs;
+    rp.sin_tab = sn;
+    LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
+    rp.x = q; rp.y = qr; rp.rows = qrows;
+    rp.a = out; rp.b = dout; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
+    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
+    rp.x = k; rp.y = kr; rp.rows = krows;
+    rp.a = nullptr; rp.b = nullptr; rp.delta = nullptr; rp.lse = nullptr; rp.lse2 = nullptr;
+    rp.dqacc = nullptr;
+    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
+    tm.done();
+  }
+  gbattn::BwdParams bp{};
+  const int bq = gbattn::bwd_query_tile(D);
+  ok = ok && make_map(&bp.map_q, qr, qrows, D, bq) && make_map(&bp.map_do, dout, qrows, D, bq) &&
+       make_map(&bp.map_k, kr, krows, D, kTile) && make_map(&bp.map_v, v, krows, D, kTile);
+  if (ok) {
+    bp.lse2 = lse2;
+    bp.delta = delta;
+    bp.dqacc = dqacc;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.cos_tab = cs;
+    bp.sin_tab = sn;
+    bp.status = d->status;
+    bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.S = S; bp.D = D;
+    bp.scale = scale;
+    bp.scale_log2 = scale * 1.4426950408889634f;
+    bp.causal = causal ? 1 : 0;
+    bp.inject_timeout = g_inject_timeout ? 1 : 0;
+    LaunchTimer tm(ATTN_KERNEL_BWD_MAIN, stream);
+    ok = gbattn::launch_bwd_main(bp, stream) == cudaSuccess;
+    tm.done();
+  }
+  if (ok) {
+    LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
+    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, cs, sn, stream) == cudaSuccess;
+    tm.done();
+  }
+  cudaFreeAsync(ws, stream);
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_sync_status(attn_stream_t stream_) {
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+int attn_profile_begin(int max_launches) {
+  if (max_launches <= 0) return ATTN_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_prof.rec) {
+    for (auto& pr : r) {
+      g_prof.spare.push_back(pr.first);
+      g_prof.spare.push_back(pr.second);
+    }
+    r.clear();
+  }
+  g_prof.cap = max_launches;
+  g_prof.on = true;
+  return ATTN_OK;
+}
+
+int attn_profile_end(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof.on = false;
+  return ATTN_OK;
+}
+
+int attn_profile_query(int kernel, int* launches, float* total_ms) {
+  if (kernel < 0 || kernel >= ATTN_NUM_KERNELS || !launches || !total_ms) return ATTN_ERR_INVALID;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> rec;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    rec = g_prof.rec[kernel];
+  }
+  float sum = 0.f;
+  for (auto& pr : rec) {
+    if (cudaEventSynchronize(pr.second) != cudaSuccess) return ATTN_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, pr.first, pr.second) != cudaSuccess) return ATTN_ERR_CUDA;
+    sum += ms;
+  }
+  *launches = static_cast<int>(rec.size());
+  *total_ms = sum;
+  return ATTN_OK;
+}
+
+int attn_debug_inject_timeout(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_inject_timeout = enable != 0;
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,444 @@
+// Backward attention main kernel for sm_103a: dK, dV and the dQ partial sums.
+//
+// The gradients are the chain rule through the forward definition (scores
+// q~.k~ scale with keys after the query masked, softmax, P v; see attn_fwd.cu for
+// the pages it follows). With P recomputed from the saved lse:
+//   dP_ij = dout_i . v_j,  dS_ij = P_ij (dP_ij - delta_i),  delta_i = dout_i . out_i
+//   dv_j  = sum_{h in group} sum_i P_ij dout_i
+//   dk~_j = scale sum_{h in group} sum_i dS_ij q~_i      (rotated back here: dk = R_jᵀ dk~)
+//   dq~_i = scale sum_j dS_ij k~_j                      (summed into an fp32 buffer)
+// Query heads sharing one K/V head ("深度学习系统设计llama3-from-scratch：并行计算架构",
+// §键值（Key-Value）共享机制; "ColossalAI 中的 PaLM 教学实现…", §2.5 multi-query) are
+// reduced inside the CTA: dK and dV accumulate in tensor memory across every
+// query head of the group.
+//
+// GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
+// shared memory and walks the (query head, query tile) steps that see its keys
+// (only tiles on or below the diagonal when causal). Per step, in TMEM:
+//   Sᵀ  = K~ Q~ᵀ      [128 keys x BQ]    (SS MMA)
+//   dPᵀ = V dOᵀ       [128 keys x BQ]    (SS MMA)
+//   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta);
+//                  Pᵀ goes back to TMEM as bf16 (over Sᵀ), dSᵀ to shared memory
+//   dV += Pᵀ dO       (TS MMA, A from TMEM)
+//   dK += dSᵀ Q~      (SS MMA)
+//   dQ partial = dS K~ (D = 64: [BQ x D]) or its transpose K~ᵀ dSᵀ (D = 128:
+//                [D x BQ]), double-buffered, drained by its own warps with
+//                fp32 global reductions.
+// Warp roles: 0-7 softmax (two column halves), 8-11 dQ drain, 12 TMA producer,
+// 13 MMA issuer and TMEM owner.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+using namespace gb;
+
+constexpr int kThreads = 448;
+constexpr int kWarpLoad = 12;
+constexpr int kWarpMma = 13;
+
+enum : int {
+  kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
+  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
+  static constexpr bool kDqT = D == 128;          // dQ computed transposed ([D x BQ])
+  static constexpr int kRegions = D / 64;
+  static constexpr int kKRegionBytes = 128 * 128;  // 128 key rows x 128 B
+  static constexpr int kQRegionBytes = BQ * 128;   // BQ query rows x 128 B
+  static constexpr int kKTileBytes = kRegions * kKRegionBytes;
+  static constexpr int kQTileBytes = kRegions * kQRegionBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
+  static constexpr int kDsRegions = BQ / 64;
+  static constexpr int kDsBytes = kDsRegions * 16384;  // dSᵀ: 128 key rows x BQ bf16
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKTileBytes;
+  static constexpr int kStageOff = 2 * kKTileBytes;
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kDsOff + kDsBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColST = 0;
+  static constexpr uint32_t kColDPT = BQ;
+  __device__ static constexpr uint32_t col_dq(int buf) { return 2 * BQ + (buf ? 64u : 0u); }
+  static constexpr uint32_t kColDV = 2 * BQ + 128;
+  static constexpr uint32_t kColDK = 2 * BQ + 128 + D;
+  static_assert(kColDK + D == 512, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs / 4) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_kv, bar_s_full, bar_ds_full, bar_done, bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_dq_full[2], bar_dq_free[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
+
+  // ---- work item: key tile kt of KV head (b, hkv); heaviest (kt = 0) first
+  const int BHk = p.B * p.Hkv;
+  const int kt = static_cast<int>(blockIdx.x) / BHk;
+  const int bhk = static_cast<int>(blockIdx.x) % BHk;
+  const int b = bhk / p.Hkv;
+  const int hkv = bhk % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int k0 = kt * kTile;
+  const int kv_row = bhk * p.S + k0;
+  const int nqt = p.S / BQ;
+  const int qt_begin = p.causal ? k0 / BQ : 0;
+  const int per_head = nqt - qt_begin;
+  const int n = G * per_head;
+  // step s -> (query head, query tile)
+  auto step_qt = [&](int s) { return qt_begin + s % per_head; };
+  auto step_row = [&](int s) {
+    const int h = hkv * G + s / per_head;
+    return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
+  };
+
+  // ---- setup
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_kv), 1);
+    mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_ds_full), 256);
+    mbar_init(smem_u32(&bar_done), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_never), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bar_stage_full[s]), 1);
+      mbar_init(smem_u32(&bar_stage_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_dq_full[i]), 1);
+      mbar_init(smem_u32(&bar_dq_free[i]), 128);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+  auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
+
+  if (warp == kWarpLoad) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.map_q);
+      tma_prefetch_desc(&p.map_do);
+      const uint32_t kvb = smem_u32(&bar_kv);
+      mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
+      for (int r = 0; r < C::kRegions; ++r) {
+        tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
+        tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
+      }
+      int issued = 0;
+      for (int s = 0; s < n; ++s) {
+        const int st = s % C::kStages;
+        if (!bounded_wait(smem_u32(&bar_stage_empty[st]), ((s / C::kStages) & 1) ^ 1, abort_ptr,
+                          p.status, kSiteStageEmpty))
+          break;
+        const uint32_t full = smem_u32(&bar_stage_full[st]);
+        const uint32_t dst = stage_addr(s);
+        const int row = step_row(s);
+        mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
+        for (int r = 0; r < C::kRegions; ++r) {
+          tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
+          tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
+        }
+        bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
+        bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
+        ++issued;
+      }
+      // Copies already issued land before the CTA releases its shared memory.
+      drain_wait(kvb, 0);
+      for (int i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i)
+        drain_wait(smem_u32(&bar_stage_full[i % C::kStages]), (i / C::kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_st = idesc_bf16(128, BQ, 0, 0);
+      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idesc_dq = C::kDqT ? idesc_bf16(128, BQ, 1, 1) : idesc_bf16(128, D, 1, 1);
+      const uint32_t kaddr = sbase + C::kKOff;
+      const uint32_t vaddr = sbase + C::kVOff;
+      const uint32_t dsaddr = sbase + C::kDsOff;
+
+      auto issue_st = [&](int s) {
+        const uint32_t qaddr = stage_addr(s);
+        const uint32_t doaddr = qaddr + C::kQTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
+          const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColST, sdesc_sw128(kaddr + ok_, 16, 1024),
+                 sdesc_sw128(qaddr + oq, 16, 1024), idesc_st, kk > 0);
+          mma_ss(tmem + C::kColDPT, sdesc_sw128(vaddr + ok_, 16, 1024),
+                 sdesc_sw128(doaddr + oq, 16, 1024), idesc_st, kk > 0);
+        }
+      };
+      auto issue_dvdk = [&](int s, bool first) {
+        const uint32_t qaddr = stage_addr(s);
+        const uint32_t doaddr = qaddr + C::kQTileBytes;
+        constexpr int HC = BQ / 2;  // query columns per softmax half
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const int half = (16 * kk) / HC;
+          const uint32_t pcol = half * HC + 8 * (kk - half * (HC / 16));
+          mma_ts(tmem + C::kColDV, tmem + C::kColST + pcol,
+                 sdesc_sw128(doaddr + kk * 2048, C::kQRegionBytes, 1024), idesc_acc,
+                 (!first || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDK, sdesc_sw128(dsaddr + oa, 16, 1024),
+                 sdesc_sw128(qaddr + kk * 2048, C::kQRegionBytes, 1024), idesc_acc,
+                 (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_dq = [&](int buf) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if constexpr (C::kDqT) {
+            // dQᵀ [D x BQ] = K~ᵀ (MN-major A) x dSᵀ (MN-major B), K = keys
+            mma_ss(tmem + C::col_dq(buf), sdesc_sw128(kaddr + kk * 2048, C::kKRegionBytes, 1024),
+                   sdesc_sw128(dsaddr + kk * 2048, 16384, 1024), idesc_dq, kk > 0);
+          } else {
+            // dQ [BQ x D] = dS (MN-major A, from dSᵀ) x K~ (MN-major B), K = keys
+            mma_ss(tmem + C::col_dq(buf), sdesc_sw128(dsaddr + kk * 2048, 16384, 1024),
+                   sdesc_sw128(kaddr + kk * 2048, C::kKRegionBytes, 1024), idesc_dq, kk > 0);
+          }
+        }
+      };
+
+      bool ok = true;
+      if (p.inject_timeout)  // nothing ever arrives on bar_never
+        ok = bounded_wait(smem_u32(&bar_never), 0, abort_ptr, p.status, kSiteInject);
+      ok = ok && bounded_wait(smem_u32(&bar_kv), 0, abort_ptr, p.status, kSiteKv);
+      ok = ok && bounded_wait(smem_u32(&bar_stage_full[0]), 0, abort_ptr, p.status, kSiteStageFull);
+      if (ok) {
+        tc_fence_after();
+        issue_st(0);
+        mma_commit(smem_u32(&bar_s_full));
+      }
+      for (int s = 0; s < n && ok; ++s) {
+        ok = bounded_wait(smem_u32(&bar_ds_full), s & 1, abort_ptr, p.status, kSiteDsFull);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dvdk(s, s == 0);
+        mma_commit(smem_u32(&bar_stage_empty[s % C::kStages]));
+        const int buf = s & 1;
+        ok = bounded_wait(smem_u32(&bar_dq_free[buf]), ((s >> 1) & 1) ^ 1, abort_ptr, p.status,
+                          kSiteDqFree);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dq(buf);
+        mma_commit(smem_u32(&bar_dq_full[buf]));
+        if (s + 1 < n) {
+          ok = bounded_wait(smem_u32(&bar_stage_full[(s + 1) % C::kStages]),
+                            ((s + 1) / C::kStages) & 1, abort_ptr, p.status, kSiteStageFull);
+          if (!ok) break;
+          issue_st(s + 1);
+          mma_commit(smem_u32(&bar_s_full));
+        }
+      }
+      if (ok) mma_commit(smem_u32(&bar_done));
+      // Every MMA issued above completes before the tensor memory is released.
+      mma_commit(smem_u32(&bar_drain));
+      drain_wait(smem_u32(&bar_drain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 8) {
+    // ================================================================ dQ drain
+    const int r = tid & 127;  // TMEM lane: d (D = 128) or query row (D = 64)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int s = 0; s < n; ++s) {
+      const int buf = s & 1;
+      const bool got =
+          bounded_wait(smem_u32(&bar_dq_full[buf]), (s >> 1) & 1, abort_ptr, p.status, kSiteDqFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint32_t u0[32], u1[32];
+      tmem_ld32(tmem + lane_base + C::col_dq(buf), u0);
+      tmem_ld32(tmem + lane_base + C::col_dq(buf) + 32, u1);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_dq_free[buf]));
+      const long long row0 = step_row(s);
+      if constexpr (C::kDqT) {
+        // lane r = d; columns = the BQ = 64 query rows of the step
+        float* base = p.dqacc + row0 * D + r;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+      } else {
+        // lane r = query row; columns = d
+        float* base = p.dqacc + (row0 + r) * D;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          red_add_v4_f32(base + 4 * i, __uint_as_float(u0[4 * i]), __uint_as_float(u0[4 * i + 1]),
+                         __uint_as_float(u0[4 * i + 2]), __uint_as_float(u0[4 * i + 3]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          red_add_v4_f32(base + 32 + 4 * i, __uint_as_float(u1[4 * i]),
+                         __uint_as_float(u1[4 * i + 1]), __uint_as_float(u1[4 * i + 2]),
+                         __uint_as_float(u1[4 * i + 3]));
+      }
+    }
+  } else {
+    // ================================================================ softmax
+    constexpr int HC = BQ / 2;  // query columns of this half
+    const int half = warp >> 2;
+    const int r = tid & 127;  // key row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const int key = k0 + r;
+    for (int s = 0; s < n; ++s) {
+      const bool got = bounded_wait(smem_u32(&bar_s_full), s & 1, abort_ptr, p.status, kSiteSFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t st = stage_addr(s);
+      const float* lse2 = reinterpret_cast<const float*>(sgen + (st - sbase) + 2 * C::kQTileBytes);
+      const float* delta = lse2 + BQ;
+      const int q0 = step_qt(s) * BQ;
+      const bool mask = p.causal && q0 < k0 + kTile;
+#pragma unroll
+      for (int ch = 0; ch < HC / 32; ++ch) {
+        const int qb = half * HC + ch * 32;  // first query column of this chunk
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tmem + lane_base + C::kColST + qb, sv);
+        tmem_ld32(tmem + lane_base + C::kColDPT + qb, dpv);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pr[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = qb + 2 * i + e;
+            float pv = ex2(fmaf(__uint_as_float(sv[2 * i + e]), sl2, -lse2[q]));
+            if (mask && key > q0 + q) pv = 0.f;
+            pr[e] = pv;
+            dsv[e] = pv * (__uint_as_float(dpv[2 * i + e]) - delta[q]);
+          }
+          pk[i] = pack_bf16(pr[0], pr[1]);
+          dk[i] = pack_bf16(dsv[0], dsv[1]);
+        }
+        // Pᵀ back into this half's own Sᵀ columns (already read)
+        tmem_st16(tmem + lane_base + C::kColST + half * HC + ch * 16, pk);
+        // dSᵀ row r, query columns qb..qb+31, 128-byte-swizzled K-major layout
+        const uint32_t region = sbase + C::kDsOff + (qb / 64) * 16384;
+        const uint32_t c0 = (qb % 64) / 8;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(region + sw128_offset(r, c0 + q4), dk[4 * q4], dk[4 * q4 + 1],
+                       dk[4 * q4 + 2], dk[4 * q4 + 3]);
+      }
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_ds_full));
+    }
+    // ------------------------------------------------------------ dK / dV epilogue
+    const bool got = bounded_wait(smem_u32(&bar_done), 0, abort_ptr, p.status, kSiteDone);
+    (void)got;
+    __syncwarp();
+    tc_fence_after();
+    const long long grow = kv_row + r;
+    if (half == 0) {
+      float* dst = p.dv + grow * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(dst + cc * 32)[i] =
+              make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                          __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+      }
+    } else {
+      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2)
+      float* dst = p.dk + grow * D;
+      const float* cs = p.cos_tab + (long long)key * (D / 2);
+      const float* sn = p.sin_tab + (long long)key * (D / 2);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t x1[32], x2[32];
+        tmem_ld32(tmem + lane_base + C::kColDK + ch * 32, x1);
+        tmem_ld32(tmem + lane_base + C::kColDK + D / 2 + ch * 32, x2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
+          const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
+          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+          const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+          float y1[4], y2[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = __uint_as_float(x1[4 * i + e]);
+            const float bb = __uint_as_float(x2[4 * i + e]);
+            y1[e] = p.scale * (a * cc[e] + bb * ss[e]);
+            y2[e] = p.scale * (bb * cc[e] - a * ss[e]);
+          }
+          reinterpret_cast<float4*>(dst + ch * 32)[i] = make_float4(y1[0], y1[1], y1[2], y1[3]);
+          reinterpret_cast<float4*>(dst + D / 2 + ch * 32)[i] =
+              make_float4(y2[0], y2[1], y2[2], y2[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv);
+  attn_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
+  return p.D == 128 ? launch_bwd_d<128>(p, stream) : launch_bwd_d<64>(p, stream);
+}
+
+}  // namespace gbattn

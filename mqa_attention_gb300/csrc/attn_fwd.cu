@@ -1,0 +1,367 @@
+// Forward attention kernel for sm_103a: out = softmax(scale q~ k~ᵀ + mask) v and lse.
+//
+// The method (pages cited by title and section):
+//   scores q~_i . k~_j / sqrt(D) with keys after the query masked
+//     ("深度学习系统设计llama3-from-scratch：并行计算架构", §注意力得分矩阵计算, §因果掩码的并行应用);
+//   row maximum subtracted before the softmax, then P v
+//     ("ColossalAI 中的 PaLM 教学实现…", §2.5 Attention);
+//   IO-aware tiling that never writes the S x S score matrix to memory
+//     ("Picotron模型实现解析Llama架构与Flash Attention集成", §Flash Attention的优势).
+// The tiled softmax keeps, per query row, a running maximum m and sum l and
+// rescales the partial output when m grows; the final out = O / l and
+// lse = m + ln l equal the plain definition up to rounding.
+//
+// GB300 design: one CTA owns two 128-row query tiles (2c, 2c+1) of one head and
+// streams the 128-key K/V tiles of its KV head through a TMA ring. Warp roles:
+//   warps 0-3 / 4-7  softmax for query tile 0 / 1 (one thread per row),
+//   warp 8           TMA producer (Q once, then K_j, V_j into the ring),
+//   warp 9           tcgen05 MMA issuer (one thread) and TMEM owner.
+// TMEM (512 columns): S_0, S_1 (128 fp32 columns each), O_0, O_1 (D columns
+// each). P_t is written back as packed bf16 into the first 64 columns of S_t
+// and consumed from TMEM by the P.V MMA. While one tile's softmax runs, the
+// tensor core works on the other tile's MMAs. KV tiles above the diagonal are
+// never loaded; only the diagonal tile is masked.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+using namespace gb;
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+
+// Wait-site codes reported in the status word.
+enum : int {
+  kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5,
+  kSiteODone = 6, kSiteInject = 7
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 B (64 bf16)
+  static constexpr int kRegions = D / 64;
+  static constexpr int kTileBytes = kRegions * kRegionBytes;
+  static constexpr int kSlots = D == 128 ? 4 : 6;      // K/V ring depth (tiles)
+  static constexpr int kKvOff = 2 * kTileBytes;        // after Q_0, Q_1
+  static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
+  __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+  __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? D : 0); }
+};
+
+// Waits for a phase without looking at the abort flag (used to drain copies
+// and MMAs that were already issued before the CTA releases its resources).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs / 4) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kSlots], bar_kv_empty[C::kSlots];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  // ---- work item: heaviest query-tile pairs first
+  const int nq = p.S / kTile;
+  const int npairs = (nq + 1) / 2;
+  const int BH = p.B * p.Hq;
+  const int c = npairs - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int b = bh / p.Hq;
+  const int h = bh % p.Hq;
+  const int hkv = h / (p.Hq / p.Hkv);
+  // KV tiles seen by query tile 2c + t (0 when that tile is past the end)
+  auto tiles_of = [&](int t) {
+    const int qt = 2 * c + t;
+    return qt < nq ? (p.causal ? qt + 1 : nq) : 0;
+  };
+  const int n_0 = tiles_of(0);
+  const int n_1 = tiles_of(1);
+  const int n = n_0 > n_1 ? n_0 : n_1;
+  const int q_row0 = bh * p.S;
+  const int kv_row0 = (b * p.Hkv + hkv) * p.S;
+
+  // ---- setup
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_never), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_s_full[t]), 1);
+      mbar_init(smem_u32(&bar_p_full[t]), 128);
+      mbar_init(smem_u32(&bar_o_done[t]), 1);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == kWarpLoad) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.map_q);
+      tma_prefetch_desc(&p.map_k);
+      tma_prefetch_desc(&p.map_v);
+      const int nvalid = (n_0 > 0) + (n_1 > 0);
+      mbar_arrive_expect_tx(smem_u32(&bar_q), nvalid * C::kTileBytes);
+      for (int t = 0; t < 2; ++t) {
+        if ((t ? n_1 : n_0) == 0) continue;
+        for (int r = 0; r < C::kRegions; ++r)
+          tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
+                      q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        for (int w = 0; w < 2; ++w) {
+          const int slot = issued % C::kSlots;
+          const uint32_t ph = ((issued / C::kSlots) & 1) ^ 1;
+          if (!bounded_wait(smem_u32(&bar_kv_empty[slot]), ph, abort_ptr, p.status, kSiteKvEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bar_kv_full[slot]);
+          mbar_arrive_expect_tx(full, C::kTileBytes);
+          const CUtensorMap* map = w == 0 ? &p.map_k : &p.map_v;
+          const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + j * kTile, full);
+          ++issued;
+        }
+      }
+      // Loads already issued land before the CTA releases its shared memory (a
+      // no-op in a healthy run). Each slot has at most one load in flight: a load
+      // is issued only after the previous one in its slot was consumed.
+      drain_wait(smem_u32(&bar_q), 0);
+      for (int i = issued - C::kSlots > 0 ? issued - C::kSlots : 0; i < issued; ++i)
+        drain_wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+      auto slot_addr = [&](int i) { return sbase + C::kKvOff + (i % C::kSlots) * C::kTileBytes; };
+      auto wait_kv = [&](int i) {
+        return bounded_wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1, abort_ptr,
+                            p.status, kSiteKvFull);
+      };
+      auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = sbase + t * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::col_s(t), sdesc_sw128(qaddr + off, 16, 1024),
+                 sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                 sdesc_sw128(vaddr + kk * 16 * 128, C::kRegionBytes, 1024), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+
+      bool ok = true;
+      if (p.inject_timeout)  // nothing ever arrives on bar_never
+        ok = bounded_wait(smem_u32(&bar_never), 0, abort_ptr, p.status, kSiteInject);
+      ok = ok && bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ);
+      ok = ok && wait_kv(0);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          if ((t ? n_1 : n_0) == 0) continue;
+          issue_qk(t, slot_addr(0));
+          mma_commit(smem_u32(&bar_s_full[t]));
+        }
+        mma_commit(smem_u32(&bar_kv_empty[0]));
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int iv = 2 * j + 1;  // ring index of V_j
+        const int ik = 2 * j + 2;  // ring index of K_{j+1}
+        const bool next = j + 1 < n;
+        ok = wait_kv(iv) && (!next || wait_kv(ik));
+        if (!ok) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int nt = t ? n_1 : n_0;
+          if (j >= nt) continue;
+          ok = bounded_wait(smem_u32(&bar_p_full[t]), j & 1, abort_ptr, p.status, kSitePFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, slot_addr(iv), j > 0);
+          if (j == nt - 1) mma_commit(smem_u32(&bar_o_done[t]));
+          if (next && j + 1 < nt) {
+            issue_qk(t, slot_addr(ik));
+            mma_commit(smem_u32(&bar_s_full[t]));
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bar_kv_empty[iv % C::kSlots]));
+        if (next) mma_commit(smem_u32(&bar_kv_empty[ik % C::kSlots]));
+      }
+      // Every MMA issued above completes before the tensor memory is released.
+      mma_commit(smem_u32(&bar_drain));
+      drain_wait(smem_u32(&bar_drain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax
+    const int t = warp >> 2;
+    const int r = tid & 127;  // row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::col_s(t);
+    const uint32_t tO = tmem + lane_base + C::col_o(t);
+    const int nt = t ? n_1 : n_0;
+    const int qt = 2 * c + t;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running maximum, base-2 units (scores * scale * log2 e)
+    float l = 0.f;        // running sum of 2^(score2 - m)
+    for (int j = 0; j < nt; ++j) {
+      const bool got = bounded_wait(smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.status, kSiteSFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tS + cc * 32, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
+      }
+      const bool diag = p.causal && j == qt;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        if (diag && i > r) s[i] = -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      const float mx2 = mx * sl2;
+      float alpha = 1.f;
+      bool grew = false;
+      // Lazy rescaling: keep the old maximum unless the row maximum grew by more
+      // than 2^8; probabilities then stay below 256, well inside fp32 / bf16.
+      if (mx2 > m + 8.f) {
+        alpha = ex2(m - mx2);  // 0 on the first tile (m = -inf)
+        grew = true;
+        m = mx2;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a0 = ex2(fmaf(s[hh * 64 + 2 * i], sl2, -m));
+          const float a1 = ex2(fmaf(s[hh * 64 + 2 * i + 1], sl2, -m));
+          rs += a0 + a1;
+          pk[i] = pack_bf16(a0, a1);
+        }
+        tmem_st32(tS + hh * 32, pk);
+      }
+      l = l * alpha + rs;
+      if (j > 0 && __any_sync(0xffffffffu, grew)) {
+        const float f = grew ? alpha : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tO + cc * 32, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+          tmem_st32(tO + cc * 32, u);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p_full[t]));
+    }
+    if (nt > 0) {
+      // ------------------------------------------------------------ epilogue
+      bounded_wait(smem_u32(&bar_o_done[t]), 0, abort_ptr, p.status, kSiteODone);
+      __syncwarp();
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const uint32_t obuf = sbase + t * C::kTileBytes;  // Q_t is no longer read
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tO + cc * 32, u);
+        const uint32_t region = obuf + ((cc * 32) / 64) * C::kRegionBytes;
+        const uint32_t chunk0 = ((cc * 32) % 64) / 8;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(u[8 * q4 + 2 * e]) * inv_l,
+                             __uint_as_float(u[8 * q4 + 2 * e + 1]) * inv_l);
+          st_shared_v4(region + sw128_offset(r, chunk0 + q4), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (r == 0) {
+        for (int rg = 0; rg < C::kRegions; ++rg)
+          tma_store_2d(&p.map_out, rg * 64, q_row0 + qt * kTile, obuf + rg * C::kRegionBytes);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+      p.lse[static_cast<long long>(q_row0) + qt * kTile + r] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int nq = p.S / kTile;
+  const unsigned grid = static_cast<unsigned>(((nq + 1) / 2) * p.B * p.Hq);
+  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
+  return p.D == 128 ? launch_fwd_d<128>(p, stream) : launch_fwd_d<64>(p, stream);
+}
+
+}  // namespace gbattn

@@ -1,0 +1,182 @@
+// HBM-bound row kernels around the attention main kernels:
+//   * the RoPE cos/sin table (built once per (S, D, theta) in fp64, stored fp32),
+//   * the RoPE pre-pass that rotates q and k rows into bf16 (forward and backward),
+//     fused, for the backward, with delta_i = dout_i . out_i, lse in base 2 and the
+//     zeroing of the fp32 dq accumulator,
+//   * the dq finalisation dq_i = scale * R_iᵀ dq~_i.
+// RoPE is the half-split rotation x*cos + rotate_half(x)*sin with
+// rotate_half(x) = cat(-x2, x1) and inverse frequencies theta^(-2i/D)
+// ("Picotron模型实现解析Llama架构与Flash Attention集成", §1 嵌入层与位置编码;
+//  "ColossalAI 中的 PaLM 教学实现…", §2.3 RotaryEmbedding).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace gbattn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict__ sin_tab, int S,
+                                  int D, double theta) {
+  const int half = D / 2;
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= (long long)S * half) return;
+  const int p = static_cast<int>(idx / half);
+  const int i = static_cast<int>(idx % half);
+  const double inv_freq = pow(theta, -2.0 * i / static_cast<double>(D));
+  double s, c;
+  sincos(static_cast<double>(p) * inv_freq, &s, &c);
+  cos_tab[idx] = static_cast<float>(c);
+  sin_tab[idx] = static_cast<float>(s);
+}
+
+struct alignas(16) Bf16x8 {
+  __nv_bfloat162 v[4];
+};
+
+__device__ __forceinline__ void load8(const float* p, float (&o)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float (&o)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ void load8_bf16(const void* p, float (&o)[8]) {
+  const Bf16x8 x = *reinterpret_cast<const Bf16x8*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(x.v[i]);
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void store8_bf16(void* p, const float (&o)[8]) {
+  Bf16x8 x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x.v[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+  *reinterpret_cast<Bf16x8*>(p) = x;
+}
+
+// One thread per (row, c) with c < D/16: elements [8c, 8c+8) and [D/2+8c, D/2+8c+8).
+template <int D, bool kBwd>
+__global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
+  constexpr int T = D / 16;  // threads per row
+  constexpr int H = D / 2;
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = t / T;
+  const int c = static_cast<int>(t % T);
+  // Threads past the last row read row 0 (a valid address), take part in the
+  // shuffles below and write nothing.
+  const bool live = row < p.rows;
+  const long long r = live ? row : 0;
+  const int pos = static_cast<int>(r % p.S);
+  const long long e1 = r * D + 8 * c;
+  const long long e2 = e1 + H;
+  float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
+  load8_bf16(static_cast<const __nv_bfloat16*>(p.x) + e1, x1);
+  load8_bf16(static_cast<const __nv_bfloat16*>(p.x) + e2, x2);
+  load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
+  load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y1[i] = x1[i] * cs[i] - x2[i] * sn[i];
+    y2[i] = x2[i] * cs[i] + x1[i] * sn[i];
+  }
+  if (live) {
+    store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e1, y1);
+    store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e2, y2);
+  }
+  if constexpr (kBwd) {
+    float a1[8], a2[8], b1[8], b2[8];
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.a) + e1, a1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.a) + e2, a2);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.b) + e1, b1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.b) + e2, b2);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dot += a1[i] * b1[i] + a2[i] * b2[i];
+#pragma unroll
+    for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (live) {
+      if (c == 0) {
+        p.delta[r] = dot;
+        p.lse2[r] = p.lse[r] * kLog2e;
+      }
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      store8(p.dqacc + e1, z);
+      store8(p.dqacc + e2, z);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    dq_finalize_kernel(const float* __restrict__ dqacc, float* __restrict__ dq, long long rows,
+                       int S, float scale, const float* __restrict__ cos_tab,
+                       const float* __restrict__ sin_tab) {
+  constexpr int T = D / 16;
+  constexpr int H = D / 2;
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = t / T;
+  if (row >= rows) return;
+  const int c = static_cast<int>(t % T);
+  const int pos = static_cast<int>(row % S);
+  const long long e1 = row * D + 8 * c;
+  const long long e2 = e1 + H;
+  float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
+  load8(dqacc + e1, x1);
+  load8(dqacc + e2, x2);
+  load8(cos_tab + (long long)pos * H + 8 * c, cs);
+  load8(sin_tab + (long long)pos * H + 8 * c, sn);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // transpose of the rotation: rotation by -angle
+    y1[i] = scale * (x1[i] * cs[i] + x2[i] * sn[i]);
+    y2[i] = scale * (x2[i] * cs[i] - x1[i] * sn[i]);
+  }
+  store8(dq + e1, y1);
+  store8(dq + e2, y2);
+}
+
+long long blocks_for(long long threads) { return (threads + 255) / 256; }
+
+}  // namespace
+
+cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
+                              cudaStream_t stream) {
+  const long long n = (long long)S * (D / 2);
+  rope_table_kernel<<<(unsigned)blocks_for(n), 256, 0, stream>>>(cos_tab, sin_tab, S, D, theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
+  const long long threads = p.rows * (p.D / 16);
+  const unsigned grid = (unsigned)blocks_for(threads);
+  const bool bwd = p.delta != nullptr;
+  if (p.D == 128) {
+    if (bwd) row_prep_kernel<128, true><<<grid, 256, 0, stream>>>(p);
+    else row_prep_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (bwd) row_prep_kernel<64, true><<<grid, 256, 0, stream>>>(p);
+    else row_prep_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
+                               float scale, const float* cos_tab, const float* sin_tab,
+                               cudaStream_t stream) {
+  const long long threads = rows * (D / 16);
+  const unsigned grid = (unsigned)blocks_for(threads);
+  if (D == 128)
+    dq_finalize_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, cos_tab, sin_tab);
+  else
+    dq_finalize_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, cos_tab, sin_tab);
+  return cudaGetLastError();
+}
+
+}  // namespace gbattn

@@ -281,13 +281,19 @@ def backward_dkdv_keys(q, k, v, dout, keys, scale, theta, causal=True, round_rot
             kr = _maybe_round(rope_half_split(k[b, g], ang), round_rotated)
             for h in range(g * G, (g + 1) * G):
                 for r0 in range(0, S, row_block):
-                    rows = torch.arange(r0, min(S, r0 + row_block))
+                    r1 = min(S, r0 + row_block)
+                    rows = torch.arange(r0, r1)
+                    # With the causal mask, keys after the block's last row are
+                    # excluded for every row of the block: only keys < r1 enter.
+                    ncol = r1 if causal else S
                     qr = _maybe_round(rope_half_split(q[b, h, rows], ang[rows]), round_rotated)
-                    p, _ = _softmax_rows(_scores(qr, kr, scale, rows, causal))
-                    dp = dout[b, h, rows] @ v[b, g].T
+                    p, _ = _softmax_rows(_scores(qr, kr[:ncol], scale, rows, causal))
+                    dp = dout[b, h, rows] @ v[b, g, :ncol].T
                     delta = (p * dp).sum(dim=1)
                     ds = p * (dp - delta[:, None])
-                    dkr[bi, gi] += scale * (ds[:, keys].T @ qr)
-                    dv[bi, gi] += p[:, keys].T @ dout[b, h, rows]
+                    sel = keys < ncol
+                    ks = keys[sel]
+                    dkr[bi, gi, sel] += scale * (ds[:, ks].T @ qr)
+                    dv[bi, gi, sel] += p[:, ks].T @ dout[b, h, rows]
     dk = rope_half_split(dkr, ang[keys], inverse=True)
     return dk, dv

@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol include/attn.h declares, and
+rejects bad arguments before touching the GPU (so these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mqa_attention_gb300 as M
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "attn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", src)))
+
+
+def test_header_matches_binding_list():
+    assert declared_functions() == sorted(M.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    for name in declared_functions():
+        assert hasattr(built_lib, name), name
+
+
+def test_version_and_status_strings(built_lib):
+    assert "sm_103a" in M.version()
+    assert M.status_string(0) == "ok"
+    assert M.status_string(M.ATTN_ERR_TIMEOUT) == "device wait timed out"
+    assert M.status_string(99) == "unknown status"
+
+
+FAKE = 0x10000  # aligned, never dereferenced: validation rejects first
+
+
+def fwd_code(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=FAKE, B=1, Hq=4, Hkv=1, S=128, D=64,
+             theta=10000.0, scale=0.125):
+    return lib.attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, theta, scale, 1, None)
+
+
+def bwd_code(lib, ptr=FAKE, B=1, Hq=4, Hkv=1, S=128, D=64, theta=10000.0, scale=0.125, **over):
+    p = dict(q=ptr, k=ptr, v=ptr, out=ptr, lse=ptr, dout=ptr, dq=ptr, dk=ptr, dv=ptr)
+    p.update(over)
+    return lib.attn_bwd(p["q"], p["k"], p["v"], p["out"], p["lse"], p["dout"], p["dq"], p["dk"],
+                        p["dv"], B, Hq, Hkv, S, D, theta, scale, 1, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), M.ATTN_ERR_INVALID),
+    (dict(lse=FAKE + 4), M.ATTN_ERR_INVALID),
+    (dict(B=0), M.ATTN_ERR_INVALID),
+    (dict(Hq=6, Hkv=4), M.ATTN_ERR_INVALID),
+    (dict(scale=float("nan")), M.ATTN_ERR_INVALID),
+    (dict(scale=-1.0), M.ATTN_ERR_INVALID),
+    (dict(theta=0.0), M.ATTN_ERR_INVALID),
+    (dict(theta=float("inf")), M.ATTN_ERR_INVALID),
+    (dict(B=1 << 12, Hq=1 << 12, S=1 << 8), M.ATTN_ERR_INVALID),
+    (dict(D=96), M.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), M.ATTN_ERR_UNSUPPORTED),
+    (dict(S=100), M.ATTN_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_arguments(built_lib, kw, code):
+    assert fwd_code(built_lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=None), M.ATTN_ERR_INVALID),
+    (dict(dq=FAKE + 8), M.ATTN_ERR_INVALID),
+    (dict(Hq=3, Hkv=2), M.ATTN_ERR_INVALID),
+    (dict(S=-128), M.ATTN_ERR_INVALID),
+    (dict(D=32), M.ATTN_ERR_UNSUPPORTED),
+    (dict(S=192), M.ATTN_ERR_UNSUPPORTED),
+])
+def test_bwd_rejects_bad_arguments(built_lib, kw, code):
+    assert bwd_code(built_lib, **kw) == code
+
+
+def test_profile_arguments(built_lib):
+    assert built_lib.attn_profile_begin(0) == M.ATTN_ERR_INVALID
+    n, ms = ctypes.c_int(), ctypes.c_float()
+    assert built_lib.attn_profile_query(7, ctypes.byref(n), ctypes.byref(ms)) == M.ATTN_ERR_INVALID
+    assert built_lib.attn_profile_query(0, None, None) == M.ATTN_ERR_INVALID
+    assert built_lib.attn_profile_begin(16) == 0
+    assert built_lib.attn_profile_query(1, ctypes.byref(n), ctypes.byref(ms)) == 0
+    assert n.value == 0 and ms.value == 0.0
+    assert built_lib.attn_profile_end() == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without the shared library the binding raises; there is no fallback."""
+    monkeypatch.setattr(M, "_lib", None)
+    monkeypatch.setattr(M, "LIB_PATH", "/nonexistent/libmqa_attention_gb300.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        M.lib()

@@ -1,0 +1,192 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded bf16 inputs.
+
+Tolerances: out, dq, dk, dv max-abs 2e-2 and mean-abs 2e-3; lse abs 1e-3
+against the oracle with bf16-rounded RoPE(q), RoPE(k) (the precision in which
+the rotated operands reach the score product); out and the gradients are also
+held to the same bounds against the oracle with exact fp64 RoPE."""
+import numpy as np
+import pytest
+import torch
+
+import mqa_attention_gb300 as M
+import oracle as O
+from mqa_attention_gb300 import inputs as I
+from mqa_attention_gb300.workloads import Workload, by_index
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    return built_lib
+
+
+def gen(wl: Workload):
+    host = {n: I.normal_bf16_bits(I.seed_for(wl.index, n), s) for n, s in wl.shapes().items()}
+    dev = {n: torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).cuda()
+           for n, h in host.items()}
+    f64 = {n: torch.from_numpy(I.bf16_bits_to_f64(h)) for n, h in host.items()}
+    return dev, f64
+
+
+def run_gpu(wl: Workload, dev, backward=True):
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+    res = {"out": out, "lse": lse}
+    if backward:
+        res["dq"], res["dk"], res["dv"] = M.backward(dev["q"], dev["k"], dev["v"], out, lse,
+                                                     dev["dout"], wl.theta, wl.scale, wl.causal)
+    torch.cuda.synchronize()
+    assert M.sync_status() == 0
+    return {k: v.double().cpu() for k, v in res.items()}
+
+
+def err(got, want):
+    e = (got - want).abs()
+    return e.max().item(), e.mean().item()
+
+
+def assert_close(name, got, want, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    assert got.shape == want.shape, (name, got.shape, want.shape)
+    assert torch.isfinite(got).all(), name
+    mx, mn = err(got, want)
+    assert mx <= max_abs and mn <= mean_abs, f"{name}: max-abs {mx:.3e} mean-abs {mn:.3e}"
+
+
+def check_all(wl, g, f, backward=True):
+    """Full oracle comparison (both RoPE precisions)."""
+    for rr in (True, False):
+        out, lse = O.attention_forward(f["q"], f["k"], f["v"], wl.scale, wl.theta, wl.causal,
+                                       round_rotated=rr)
+        assert_close(f"out(rr={rr})", g["out"], out)
+        if rr:
+            assert_close("lse", g["lse"], lse, LSE_ABS, LSE_ABS)
+        if backward:
+            dq, dk, dv = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta,
+                                              wl.causal, round_rotated=rr)
+            assert_close(f"dq(rr={rr})", g["dq"], dq)
+            assert_close(f"dk(rr={rr})", g["dk"], dk)
+            assert_close(f"dv(rr={rr})", g["dv"], dv)
+
+
+SMALL = [
+    # (B, Hq, Hkv, S, D, causal): single tile, odd tile counts, G in {1,2,3,4,8,32}
+    (1, 4, 1, 128, 64, True),
+    (1, 2, 1, 256, 128, True),
+    (2, 4, 2, 384, 64, True),
+    (1, 6, 2, 640, 128, True),
+    (1, 8, 1, 256, 64, True),
+    (1, 4, 4, 256, 128, True),
+    (1, 32, 1, 128, 64, True),
+    (2, 2, 1, 256, 64, False),
+    (1, 4, 2, 384, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", SMALL)
+def test_small_shapes(B, Hq, Hkv, S, D, causal):
+    wl = Workload(100 + S // 128 + D, "small", B, Hq, Hkv, S, D,
+                  10000.0 if D == 64 else 500000.0, True, causal)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev)
+    check_all(wl, g, f)
+
+
+def test_tiny_mqa_forward_workload():
+    wl = by_index(1)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev, backward=False)
+    check_all(wl, g, f, backward=False)
+
+
+def test_forward_is_deterministic():
+    wl = Workload(150, "det", 1, 8, 2, 512, 128, 500000.0, True)
+    dev, _ = gen(wl)
+    a = M.forward(dev["q"], dev["k"], dev["v"], wl.theta)
+    b = M.forward(dev["q"], dev["k"], dev["v"], wl.theta)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def _subset(f, b, groups, G):
+    """Inputs of batch b restricted to the given KV heads and their query heads."""
+    qh = [h for g in groups for h in range(g * G, (g + 1) * G)]
+    return ({"q": f["q"][b:b + 1, qh], "dout": f["dout"][b:b + 1, qh],
+             "k": f["k"][b:b + 1, groups], "v": f["v"][b:b + 1, groups]}, qh)
+
+
+@pytest.mark.parametrize("index,picks", [
+    (2, [(0, [0, 7])]),
+    (3, [(0, [0]), (7, [0])]),
+    (4, [(0, [0, 31]), (3, [17])]),
+])
+def test_full_size_workloads(index, picks):
+    """Full-size run on the GPU; every output of the picked (batch, KV heads)
+    slices compared with the oracle, which computes that slice exactly."""
+    wl = by_index(index)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev)
+    G = wl.Hq // wl.Hkv
+    for b, groups in picks:
+        sub, qh = _subset(f, b, groups, G)
+        out, lse = O.attention_forward(sub["q"], sub["k"], sub["v"], wl.scale, wl.theta,
+                                       round_rotated=True)
+        dq, dk, dv = O.attention_backward(sub["q"], sub["k"], sub["v"], sub["dout"], wl.scale,
+                                          wl.theta, round_rotated=True)
+        assert_close("out", g["out"][b:b + 1, qh], out)
+        assert_close("lse", g["lse"][b:b + 1, qh], lse, LSE_ABS, LSE_ABS)
+        assert_close("dq", g["dq"][b:b + 1, qh], dq)
+        assert_close("dk", g["dk"][b:b + 1, groups], dk)
+        assert_close("dv", g["dv"][b:b + 1, groups], dv)
+
+
+def _sample(S, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(np.arange(1, S - 1), size=n - 2, replace=False)
+    return torch.from_numpy(np.sort(np.concatenate([[0, S - 1], rows])))
+
+
+def test_long_context_sampled():
+    """S = 32768: out, lse, dq on 256 seeded query rows of every head; dk, dv on
+    256 seeded key rows of KV head 0; exact sums over the full tensors."""
+    wl = by_index(5)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev)
+    rows = _sample(wl.S, 256, 5001)
+    out, lse = O.forward_rows(f["q"], f["k"], f["v"], rows, wl.scale, wl.theta, round_rotated=True)
+    assert_close("out", g["out"][:, :, rows], out)
+    assert_close("lse", g["lse"][:, :, rows], lse, LSE_ABS, LSE_ABS)
+    dq = O.backward_dq_rows(f["q"], f["k"], f["v"], f["dout"], rows, wl.scale, wl.theta,
+                            round_rotated=True)
+    assert_close("dq", g["dq"][:, :, rows], dq)
+    keys = _sample(wl.S, 256, 5002)
+    dk, dv = O.backward_dkdv_keys(f["q"], f["k"], f["v"], f["dout"], keys, wl.scale, wl.theta,
+                                  round_rotated=True, batches=[0], kv_heads=[0], row_block=2048)
+    assert_close("dk", g["dk"][0:1, 0:1, keys], dk)
+    assert_close("dv", g["dv"][0:1, 0:1, keys], dv)
+    _full_tensor_invariants(wl, g, f)
+
+
+def _full_tensor_invariants(wl, g, f):
+    """Properties that hold at any size: sum_j dv_j = sum over the group's query
+    heads and rows of dO; sum_j R_j dk_j = 0."""
+    G = wl.Hq // wl.Hkv
+    want = f["dout"].reshape(wl.B, wl.Hkv, G, wl.S, wl.D).sum((2, 3))
+    got = g["dv"].sum(2)
+    assert (got - want).abs().max().item() <= 1e-3 * want.abs().max().item() + 0.05
+    dkr = O.rope_half_split(g["dk"], O.rope_angles(wl.S, wl.D, wl.theta))
+    scale_ref = g["dk"].abs().sum(2).max().item()
+    assert dkr.sum(2).abs().max().item() <= 1e-3 * scale_ref
+
+
+def test_gpu_rejects_unsupported():
+    wl = Workload(160, "bad", 1, 2, 1, 128, 64, 10000.0, False)
+    dev, _ = gen(wl)
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(M.AttnError) as e:
+        M.attn_fwd(dev["q"], dev["k"], dev["v"], out, lse, 1, 2, 1, 128, 96, 1e4, 0.125, True)
+    assert e.value.code == M.ATTN_ERR_UNSUPPORTED
