@@ -93,15 +93,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows][D], 128-byte swizzled boxes of {64 columns, box_rows rows}.
-bool make_map(CUtensorMap* m, const void* ptr, long long rows, int D, int box_rows) {
+// 16-bit (bf16 or fp16) matrix [rows][D], 128-byte swizzled boxes of
+// {64 columns, box_rows rows}.
+bool make_map(CUtensorMap* m, const void* ptr, long long rows, int D, int box_rows,
+              bool fp16 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+  const CUtensorMapDataType dt =
+      fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -234,6 +238,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   bool ok = true;
   {
     gbattn::RowPrepParams rp{};
+    rp.mode = gbattn::kPrepFwd;
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
@@ -281,41 +286,59 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
   const size_t accbytes = round256(static_cast<size_t>(qrows) * D * 4);
   const size_t rowbytes = round256(static_cast<size_t>(qrows) * 4);
+  const size_t maxbytes = 256;
   uint8_t* ws = nullptr;
   if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
-                              qbytes + kbytes + accbytes + 2 * rowbytes, d->pool,
+                              2 * qbytes + 2 * kbytes + accbytes + 2 * rowbytes + maxbytes, d->pool,
                               stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  void* qr = ws;
-  void* kr = ws + qbytes;
-  float* dqacc = reinterpret_cast<float*>(ws + qbytes + kbytes);
-  float* delta = reinterpret_cast<float*>(ws + qbytes + kbytes + accbytes);
-  float* lse2 = reinterpret_cast<float*>(ws + qbytes + kbytes + accbytes + rowbytes);
+  uint8_t* w = ws;
+  void* qr = w; w += qbytes;        // fp16, scaled rotated q
+  void* dos = w; w += qbytes;       // fp16, scaled dout
+  void* kr = w; w += kbytes;        // fp16, scaled rotated k
+  void* vs = w; w += kbytes;        // fp16, scaled v
+  float* dqacc = reinterpret_cast<float*>(w); w += accbytes;
+  float* delta = reinterpret_cast<float*>(w); w += rowbytes;
+  float* lse2 = reinterpret_cast<float*>(w); w += rowbytes;
+  float* maxes = reinterpret_cast<float*>(w);
 
   bool ok = true;
   {
+    LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
+    gbattn::AbsMaxParams ap{};
+    ap.x[gbattn::kMaxQ] = q; ap.n[gbattn::kMaxQ] = qrows * D;
+    ap.x[gbattn::kMaxK] = k; ap.n[gbattn::kMaxK] = krows * D;
+    ap.x[gbattn::kMaxV] = v; ap.n[gbattn::kMaxV] = krows * D;
+    ap.x[gbattn::kMaxDO] = dout; ap.n[gbattn::kMaxDO] = qrows * D;
+    ap.maxes = maxes;
+    ok = cudaMemsetAsync(maxes, 0, 4 * sizeof(float), stream) == cudaSuccess &&
+         gbattn::launch_absmax(ap, stream) == cudaSuccess;
     gbattn::RowPrepParams rp{};
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
-    LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
-    rp.x = q; rp.y = qr; rp.rows = qrows;
-    rp.a = out; rp.b = dout; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
+    rp.maxes = maxes;
+    rp.mode = gbattn::kPrepBwdQ;
+    rp.x = q; rp.y = qr; rp.rows = qrows; rp.x2 = dout; rp.y2 = dos;
+    rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
-    rp.x = k; rp.y = kr; rp.rows = krows;
-    rp.a = nullptr; rp.b = nullptr; rp.delta = nullptr; rp.lse = nullptr; rp.lse2 = nullptr;
-    rp.dqacc = nullptr;
+    rp.mode = gbattn::kPrepBwdK;
+    rp.x = k; rp.y = kr; rp.rows = krows; rp.x2 = v; rp.y2 = vs;
+    rp.out = nullptr; rp.delta = nullptr; rp.lse = nullptr; rp.lse2 = nullptr; rp.dqacc = nullptr;
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
   }
   gbattn::BwdParams bp{};
   const int bq = gbattn::bwd_query_tile(D);
-  ok = ok && make_map(&bp.map_q, qr, qrows, D, bq) && make_map(&bp.map_do, dout, qrows, D, bq) &&
-       make_map(&bp.map_k, kr, krows, D, kTile) && make_map(&bp.map_v, v, krows, D, kTile);
+  ok = ok && make_map(&bp.map_q, qr, qrows, D, bq, true) &&
+       make_map(&bp.map_do, dos, qrows, D, bq, true) &&
+       make_map(&bp.map_k, kr, krows, D, kTile, true) &&
+       make_map(&bp.map_v, vs, krows, D, kTile, true);
   if (ok) {
     bp.lse2 = lse2;
     bp.delta = delta;
+    bp.maxes = maxes;
     bp.dqacc = dqacc;
     bp.dk = dk;
     bp.dv = dv;
@@ -333,7 +356,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   }
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
-    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, cs, sn, stream) == cudaSuccess;
+    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, maxes, cs, sn, stream) ==
+         cudaSuccess;
     tm.done();
   }
   cudaFreeAsync(ws, stream);

@@ -14,16 +14,24 @@
 //
 // GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
 // shared memory and walks the (query head, query tile) steps that see its keys
-// (only tiles on or below the diagonal when causal). Per step, in TMEM:
+// (only tiles on or below the diagonal when causal). Per step s, in TMEM:
 //   Sᵀ  = K~ Q~ᵀ      [128 keys x BQ]    (SS MMA)
 //   dPᵀ = V dOᵀ       [128 keys x BQ]    (SS MMA)
 //   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta);
-//                  Pᵀ goes back to TMEM as bf16 (over Sᵀ), dSᵀ to shared memory
+//                  Pᵀ to its own TMEM buffer, dSᵀ to a shared-memory buffer
 //   dV += Pᵀ dO       (TS MMA, A from TMEM)
 //   dK += dSᵀ Q~      (SS MMA)
 //   dQ partial = dS K~ (D = 64: [BQ x D]) or its transpose K~ᵀ dSᵀ (D = 128:
-//                [D x BQ]), double-buffered, drained by its own warps with
-//                fp32 global reductions.
+//                [D x BQ]), drained by its own warps with fp32 global reductions.
+// The MMA warp issues Sᵀ/dPᵀ of step s+1 before dV/dK/dQ of step s, so the
+// softmax of step s+1 overlaps three MMAs of step s. Pᵀ and dSᵀ buffers are
+// double-buffered where TMEM allows (D = 128); with D = 64 one Pᵀ buffer fits
+// and the softmax holds its results in registers until step s-1 is consumed.
+// All products run in fp16 (kind::f16 with fp16 A and B): the operands q~, k~,
+// v, dO arrive from the pre-pass multiplied by exact powers of two (q~ and k~
+// hold their bf16-rounded values, so the recomputed scores equal the
+// forward's), and Pᵀ, dSᵀ are rounded to fp16 (2^-11) instead of bf16 (2^-9);
+// the scales are undone in the epilogues.
 // Warp roles: 0-7 softmax (two column halves), 8-11 dQ drain, 12 TMA producer,
 // 13 MMA issuer and TMEM owner.
 #include "kernels.h"
@@ -40,33 +48,36 @@ constexpr int kWarpMma = 13;
 
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
-  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25
+  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteConsumed = 26
 };
 
 template <int D>
 struct BwdCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
   static constexpr bool kDqT = D == 128;          // dQ computed transposed ([D x BQ])
+  static constexpr int kNPT = D == 128 ? 2 : 1;   // Pᵀ TMEM buffers
   static constexpr int kRegions = D / 64;
   static constexpr int kKRegionBytes = 128 * 128;  // 128 key rows x 128 B
   static constexpr int kQRegionBytes = BQ * 128;   // BQ query rows x 128 B
   static constexpr int kKTileBytes = kRegions * kKRegionBytes;
   static constexpr int kQTileBytes = kRegions * kQRegionBytes;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;
   static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int kDsRegions = BQ / 64;
-  static constexpr int kDsBytes = kDsRegions * 16384;  // dSᵀ: 128 key rows x BQ bf16
+  static constexpr int kDsBytes = kDsRegions * 16384;  // dSᵀ: 128 key rows x BQ fp16
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKTileBytes;
   static constexpr int kStageOff = 2 * kKTileBytes;
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kSmemBytes = kDsOff + kDsBytes + 1024;
+  static constexpr int kSmemBytes = kDsOff + 2 * kDsBytes + 1024;
   // TMEM columns
   static constexpr uint32_t kColST = 0;
   static constexpr uint32_t kColDPT = BQ;
-  __device__ static constexpr uint32_t col_dq(int buf) { return 2 * BQ + (buf ? 64u : 0u); }
-  static constexpr uint32_t kColDV = 2 * BQ + 128;
-  static constexpr uint32_t kColDK = 2 * BQ + 128 + D;
+  static constexpr uint32_t kColPT = 2 * BQ;  // kNPT buffers of BQ/2 packed columns
+  __device__ static constexpr uint32_t col_pt(int buf) { return kColPT + buf * (BQ / 2); }
+  static constexpr uint32_t kColDQ = kColPT + kNPT * (BQ / 2);
+  static constexpr uint32_t kColDV = kColDQ + 64;
+  static constexpr uint32_t kColDK = kColDV + D;
   static_assert(kColDK + D == 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -85,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_kv, bar_s_full, bar_ds_full, bar_done, bar_drain, bar_never;
   __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_dq_full[2], bar_dq_free[2];
+  __shared__ __align__(8) uint64_t bar_consumed[2], bar_dq_full, bar_dq_free;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -108,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const int qt_begin = p.causal ? k0 / BQ : 0;
   const int per_head = nqt - qt_begin;
   const int n = G * per_head;
+  const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   // step s -> (query head, query tile)
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
@@ -128,14 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(smem_u32(&bar_done), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     mbar_init(smem_u32(&bar_never), 1);
+    mbar_init(smem_u32(&bar_dq_full), 1);
+    mbar_init(smem_u32(&bar_dq_free), 128);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_stage_full[s]), 1);
       mbar_init(smem_u32(&bar_stage_empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_dq_full[i]), 1);
-      mbar_init(smem_u32(&bar_dq_free[i]), 128);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bar_consumed[i]), 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -144,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
   auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
+  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s & 1) * C::kDsBytes; };
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
@@ -174,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
         ++issued;
       }
-      // Copies already issued land before the CTA releases its shared memory.
+      // Copies already issued land before the CTA releases its shared memory
+      // (at most one in flight per stage: a stage is refilled only once consumed).
       drain_wait(kvb, 0);
       for (int i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i)
         drain_wait(smem_u32(&bar_stage_full[i % C::kStages]), (i / C::kStages) & 1);
@@ -182,114 +195,118 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_st = idesc_bf16(128, BQ, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16(128, D, 0, 1);
-      constexpr uint32_t idesc_dq = C::kDqT ? idesc_bf16(128, BQ, 1, 1) : idesc_bf16(128, D, 1, 1);
-      const uint32_t kaddr = sbase + C::kKOff;
-      const uint32_t vaddr = sbase + C::kVOff;
-      const uint32_t dsaddr = sbase + C::kDsOff;
+    // The whole warp runs this loop with warp-uniform operands; elect.sync inside
+    // the MMA / commit wrappers lets one lane issue.
+    constexpr uint32_t idesc_st = idesc_fp16(128, BQ, 0, 0);
+    constexpr uint32_t idesc_acc = idesc_fp16(128, D, 0, 1);
+    constexpr uint32_t idesc_dq = C::kDqT ? idesc_fp16(128, BQ, 1, 1) : idesc_fp16(128, D, 1, 1);
+    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);                   // K-major operand
+    constexpr uint64_t kMnQ = sdesc_hi(C::kQRegionBytes, 1024);      // MN-major, BQ-row tiles
+    constexpr uint64_t kMnK = sdesc_hi(C::kKRegionBytes, 1024);      // MN-major, 128-row tiles
+    constexpr uint64_t kMnDs = sdesc_hi(16384, 1024);                // MN-major dSᵀ
+    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
+    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
+    };
+    const uint32_t kaddr = sbase + C::kKOff;
+    const uint32_t vaddr = sbase + C::kVOff;
 
-      auto issue_st = [&](int s) {
-        const uint32_t qaddr = stage_addr(s);
-        const uint32_t doaddr = qaddr + C::kQTileBytes;
+    auto issue_st = [&](int s) {
+      const uint32_t qaddr = stage_addr(s);
+      const uint32_t doaddr = qaddr + C::kQTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
-          const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColST, sdesc_sw128(kaddr + ok_, 16, 1024),
-                 sdesc_sw128(qaddr + oq, 16, 1024), idesc_st, kk > 0);
-          mma_ss(tmem + C::kColDPT, sdesc_sw128(vaddr + ok_, 16, 1024),
-                 sdesc_sw128(doaddr + oq, 16, 1024), idesc_st, kk > 0);
-        }
-      };
-      auto issue_dvdk = [&](int s, bool first) {
-        const uint32_t qaddr = stage_addr(s);
-        const uint32_t doaddr = qaddr + C::kQTileBytes;
-        constexpr int HC = BQ / 2;  // query columns per softmax half
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const int half = (16 * kk) / HC;
-          const uint32_t pcol = half * HC + 8 * (kk - half * (HC / 16));
-          mma_ts(tmem + C::kColDV, tmem + C::kColST + pcol,
-                 sdesc_sw128(doaddr + kk * 2048, C::kQRegionBytes, 1024), idesc_acc,
-                 (!first || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDK, sdesc_sw128(dsaddr + oa, 16, 1024),
-                 sdesc_sw128(qaddr + kk * 2048, C::kQRegionBytes, 1024), idesc_acc,
-                 (!first || kk > 0) ? 1u : 0u);
-        }
-      };
-      auto issue_dq = [&](int buf) {
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          if constexpr (C::kDqT) {
-            // dQᵀ [D x BQ] = K~ᵀ (MN-major A) x dSᵀ (MN-major B), K = keys
-            mma_ss(tmem + C::col_dq(buf), sdesc_sw128(kaddr + kk * 2048, C::kKRegionBytes, 1024),
-                   sdesc_sw128(dsaddr + kk * 2048, 16384, 1024), idesc_dq, kk > 0);
-          } else {
-            // dQ [BQ x D] = dS (MN-major A, from dSᵀ) x K~ (MN-major B), K = keys
-            mma_ss(tmem + C::col_dq(buf), sdesc_sw128(dsaddr + kk * 2048, 16384, 1024),
-                   sdesc_sw128(kaddr + kk * 2048, C::kKRegionBytes, 1024), idesc_dq, kk > 0);
-          }
-        }
-      };
-
-      bool ok = true;
-      if (p.inject_timeout)  // nothing ever arrives on bar_never
-        ok = bounded_wait(smem_u32(&bar_never), 0, abort_ptr, p.status, kSiteInject);
-      ok = ok && bounded_wait(smem_u32(&bar_kv), 0, abort_ptr, p.status, kSiteKv);
-      ok = ok && bounded_wait(smem_u32(&bar_stage_full[0]), 0, abort_ptr, p.status, kSiteStageFull);
-      if (ok) {
-        tc_fence_after();
-        issue_st(0);
-        mma_commit(smem_u32(&bar_s_full));
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
+        const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
+        mma_ss_w(tmem + C::kColST, desc(kKmaj, kaddr + ok_), desc(kKmaj, qaddr + oq), idesc_st,
+                 kk > 0);
+        mma_ss_w(tmem + C::kColDPT, desc(kKmaj, vaddr + ok_), desc(kKmaj, doaddr + oq), idesc_st,
+                 kk > 0);
       }
-      for (int s = 0; s < n && ok; ++s) {
-        ok = bounded_wait(smem_u32(&bar_ds_full), s & 1, abort_ptr, p.status, kSiteDsFull);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dvdk(s, s == 0);
-        mma_commit(smem_u32(&bar_stage_empty[s % C::kStages]));
-        const int buf = s & 1;
-        ok = bounded_wait(smem_u32(&bar_dq_free[buf]), ((s >> 1) & 1) ^ 1, abort_ptr, p.status,
-                          kSiteDqFree);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dq(buf);
-        mma_commit(smem_u32(&bar_dq_full[buf]));
-        if (s + 1 < n) {
-          ok = bounded_wait(smem_u32(&bar_stage_full[(s + 1) % C::kStages]),
-                            ((s + 1) / C::kStages) & 1, abort_ptr, p.status, kSiteStageFull);
-          if (!ok) break;
-          issue_st(s + 1);
-          mma_commit(smem_u32(&bar_s_full));
+    };
+    auto issue_dvdk = [&](int s, bool first) {
+      const uint32_t qaddr = stage_addr(s);
+      const uint32_t doaddr = qaddr + C::kQTileBytes;
+      const uint32_t pt = tmem + C::col_pt(s % C::kNPT);
+      const uint32_t dsaddr = ds_addr(s);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk)
+        mma_ts_w(tmem + C::kColDV, pt + kk * 8, desc(kMnQ, doaddr + kk * 2048), idesc_acc,
+                 (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk) {
+        const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_ss_w(tmem + C::kColDK, desc(kKmaj, dsaddr + oa), desc(kMnQ, qaddr + kk * 2048),
+                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto issue_dq = [&](int s) {
+      const uint32_t dsaddr = ds_addr(s);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        if constexpr (C::kDqT) {
+          // dQᵀ [D x BQ] = K~ᵀ (MN-major A) x dSᵀ (MN-major B), K = keys
+          mma_ss_w(tmem + C::kColDQ, desc(kMnK, kaddr + kk * 2048), desc(kMnDs, dsaddr + kk * 2048),
+                   idesc_dq, kk > 0);
+        } else {
+          // dQ [BQ x D] = dS (MN-major A, from dSᵀ) x K~ (MN-major B), K = keys
+          mma_ss_w(tmem + C::kColDQ, desc(kMnDs, dsaddr + kk * 2048), desc(kMnK, kaddr + kk * 2048),
+                   idesc_dq, kk > 0);
         }
       }
-      if (ok) mma_commit(smem_u32(&bar_done));
-      // Every MMA issued above completes before the tensor memory is released.
-      mma_commit(smem_u32(&bar_drain));
-      drain_wait(smem_u32(&bar_drain), 0);
+    };
+
+    bool ok = true;
+    if (p.inject_timeout)  // nothing ever arrives on bar_never
+      ok = wait(smem_u32(&bar_never), 0, kSiteInject);
+    ok = ok && wait(smem_u32(&bar_kv), 0, kSiteKv);
+    ok = ok && wait(smem_u32(&bar_stage_full[0]), 0, kSiteStageFull);
+    if (ok) {
+      tc_fence_after();
+      issue_st(0);
+      mma_commit_w(smem_u32(&bar_s_full));
     }
+    for (int s = 0; s < n && ok; ++s) {
+      ok = wait(smem_u32(&bar_ds_full), s & 1, kSiteDsFull);
+      if (!ok) break;
+      tc_fence_after();
+      if (s + 1 < n) {
+        // Sᵀ/dPᵀ of the next step first: the softmax warps have already read
+        // this step's, and the next softmax then overlaps dV/dK/dQ below.
+        ok = wait(smem_u32(&bar_stage_full[(s + 1) % C::kStages]), ((s + 1) / C::kStages) & 1,
+                  kSiteStageFull);
+        if (!ok) break;
+        issue_st(s + 1);
+        mma_commit_w(smem_u32(&bar_s_full));
+      }
+      issue_dvdk(s, s == 0);
+      mma_commit_w(smem_u32(&bar_stage_empty[s % C::kStages]));
+      ok = wait(smem_u32(&bar_dq_free), (s & 1) ^ 1, kSiteDqFree);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dq(s);
+      mma_commit_w(smem_u32(&bar_dq_full));
+      mma_commit_w(smem_u32(&bar_consumed[s & 1]));
+    }
+    if (ok) mma_commit_w(smem_u32(&bar_done));
+    // Every MMA issued above completes before the tensor memory is released.
+    mma_commit_w(smem_u32(&bar_drain));
+    drain_wait(smem_u32(&bar_drain), 0);
     __syncwarp();
   } else if (warp >= 8) {
     // ================================================================ dQ drain
     const int r = tid & 127;  // TMEM lane: d (D = 128) or query row (D = 64)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int s = 0; s < n; ++s) {
-      const int buf = s & 1;
       const bool got =
-          bounded_wait(smem_u32(&bar_dq_full[buf]), (s >> 1) & 1, abort_ptr, p.status, kSiteDqFull);
+          bounded_wait(smem_u32(&bar_dq_full), s & 1, abort_ptr, p.status, kSiteDqFull);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       uint32_t u0[32], u1[32];
-      tmem_ld32(tmem + lane_base + C::col_dq(buf), u0);
-      tmem_ld32(tmem + lane_base + C::col_dq(buf) + 32, u1);
+      tmem_ld32(tmem + lane_base + C::kColDQ, u0);
+      tmem_ld32(tmem + lane_base + C::kColDQ + 32, u1);
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dq_free[buf]));
+      mbar_arrive(smem_u32(&bar_dq_free));
       const long long row0 = step_row(s);
       if constexpr (C::kDqT) {
         // lane r = d; columns = the BQ = 64 query rows of the step
@@ -316,10 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   } else {
     // ================================================================ softmax
     constexpr int HC = BQ / 2;  // query columns of this half
+    constexpr int NCH = HC / 32;
     const int half = warp >> 2;
     const int r = tid & 127;  // key row in the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float sl2 = p.scale_log2;
+    // Sᵀ arrives multiplied by 2^(eq+ek), dPᵀ and delta by 2^(edo+ev)
+    const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
     const int key = k0 + r;
     for (int s = 0; s < n; ++s) {
       const bool got = bounded_wait(smem_u32(&bar_s_full), s & 1, abort_ptr, p.status, kSiteSFull);
@@ -330,13 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const float* delta = lse2 + BQ;
       const int q0 = step_qt(s) * BQ;
       const bool mask = p.causal && q0 < k0 + kTile;
+      uint32_t pk[NCH][16], dk[NCH][16];
 #pragma unroll
-      for (int ch = 0; ch < HC / 32; ++ch) {
+      for (int ch = 0; ch < NCH; ++ch) {
         const int qb = half * HC + ch * 32;  // first query column of this chunk
         uint32_t sv[32], dpv[32];
         tmem_ld32(tmem + lane_base + C::kColST + qb, sv);
         tmem_ld32(tmem + lane_base + C::kColDPT + qb, dpv);
-        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float pr[2], dsv[2];
@@ -348,18 +367,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             pr[e] = pv;
             dsv[e] = pv * (__uint_as_float(dpv[2 * i + e]) - delta[q]);
           }
-          pk[i] = pack_bf16(pr[0], pr[1]);
-          dk[i] = pack_bf16(dsv[0], dsv[1]);
+          pk[ch][i] = pack_fp16(pr[0], pr[1]);
+          dk[ch][i] = pack_fp16(dsv[0], dsv[1]);
         }
-        // Pᵀ back into this half's own Sᵀ columns (already read)
-        tmem_st16(tmem + lane_base + C::kColST + half * HC + ch * 16, pk);
+      }
+      // The Pᵀ / dSᵀ buffers of this step were last read by step s - kNPT
+      // (dSᵀ: s - 2); wait until that step's MMAs are done.
+      if (s >= C::kNPT) {
+        const int prev = s - C::kNPT;
+        const bool free_ok = bounded_wait(smem_u32(&bar_consumed[prev & 1]), (prev >> 1) & 1,
+                                          abort_ptr, p.status, kSiteConsumed);
+        if (!__all_sync(0xffffffffu, free_ok)) break;
+        tc_fence_after();
+      }
+      const uint32_t pt = tmem + lane_base + C::col_pt(s % C::kNPT);
+      const uint32_t dsb = ds_addr(s);
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int qb = half * HC + ch * 32;
+        // Pᵀ row r, queries qb..qb+31 -> packed columns qb/2 ..
+        tmem_st16(pt + qb / 2, pk[ch]);
         // dSᵀ row r, query columns qb..qb+31, 128-byte-swizzled K-major layout
-        const uint32_t region = sbase + C::kDsOff + (qb / 64) * 16384;
+        const uint32_t region = dsb + (qb / 64) * 16384;
         const uint32_t c0 = (qb % 64) / 8;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(region + sw128_offset(r, c0 + q4), dk[4 * q4], dk[4 * q4 + 1],
-                       dk[4 * q4 + 2], dk[4 * q4 + 3]);
+          st_shared_v4(region + sw128_offset(r, c0 + q4), dk[ch][4 * q4], dk[ch][4 * q4 + 1],
+                       dk[ch][4 * q4 + 2], dk[ch][4 * q4 + 3]);
       }
       tmem_st_wait();
       fence_async_smem();
@@ -367,12 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_arrive(smem_u32(&bar_ds_full));
     }
     // ------------------------------------------------------------ dK / dV epilogue
-    const bool got = bounded_wait(smem_u32(&bar_done), 0, abort_ptr, p.status, kSiteDone);
-    (void)got;
+    bounded_wait(smem_u32(&bar_done), 0, abort_ptr, p.status, kSiteDone);
     __syncwarp();
     tc_fence_after();
     const long long grow = kv_row + r;
     if (half == 0) {
+      // dV accumulated Pᵀ (dO 2^edo)
+      const float f = exp2i(-ex.dout);
       float* dst = p.dv + grow * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -381,11 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           reinterpret_cast<float4*>(dst + cc * 32)[i] =
-              make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                          __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+              make_float4(f * __uint_as_float(u[4 * i]), f * __uint_as_float(u[4 * i + 1]),
+                          f * __uint_as_float(u[4 * i + 2]), f * __uint_as_float(u[4 * i + 3]));
       }
     } else {
-      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2)
+      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2); dK
+      // accumulated (dS 2^(edo+ev)) (q~ 2^eq)
+      const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
       float* dst = p.dk + grow * D;
       const float* cs = p.cos_tab + (long long)key * (D / 2);
       const float* sn = p.sin_tab + (long long)key * (D / 2);
@@ -405,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           for (int e = 0; e < 4; ++e) {
             const float a = __uint_as_float(x1[4 * i + e]);
             const float bb = __uint_as_float(x2[4 * i + e]);
-            y1[e] = p.scale * (a * cc[e] + bb * ss[e]);
-            y2[e] = p.scale * (bb * cc[e] - a * ss[e]);
+            y1[e] = f * (a * cc[e] + bb * ss[e]);
+            y2[e] = f * (bb * cc[e] - a * ss[e]);
           }
           reinterpret_cast<float4*>(dst + ch * 32)[i] = make_float4(y1[0], y1[1], y1[2], y1[3]);
           reinterpret_cast<float4*>(dst + D / 2 + ch * 32)[i] =

@@ -166,72 +166,76 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
-      auto slot_addr = [&](int i) { return sbase + C::kKvOff + (i % C::kSlots) * C::kTileBytes; };
-      auto wait_kv = [&](int i) {
-        return bounded_wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1, abort_ptr,
-                            p.status, kSiteKvFull);
-      };
-      auto issue_qk = [&](int t, uint32_t kaddr) {
-        const uint32_t qaddr = sbase + t * C::kTileBytes;
+    // The whole warp runs this loop with warp-uniform operands; elect.sync inside
+    // the MMA / commit wrappers lets one lane issue.
+    constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);                 // K-major operand
+    constexpr uint64_t kMnV = sdesc_hi(C::kRegionBytes, 1024);     // MN-major V
+    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
+    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
+    };
+    auto slot_addr = [&](int i) { return sbase + C::kKvOff + (i % C::kSlots) * C::kTileBytes; };
+    auto wait_kv = [&](int i) {
+      return wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1, kSiteKvFull);
+    };
+    auto issue_qk = [&](int t, uint32_t kaddr) {
+      const uint32_t qaddr = sbase + t * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::col_s(t), sdesc_sw128(qaddr + off, 16, 1024),
-                 sdesc_sw128(kaddr + off, 16, 1024), idesc_qk, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+        mma_ss_w(tmem + C::col_s(t), desc(kKmaj, qaddr + off), desc(kKmaj, kaddr + off), idesc_qk,
+                 kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                 sdesc_sw128(vaddr + kk * 16 * 128, C::kRegionBytes, 1024), idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
-      };
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts_w(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, desc(kMnV, vaddr + kk * 16 * 128),
+                 idesc_pv, (acc || kk > 0) ? 1u : 0u);
+    };
 
-      bool ok = true;
-      if (p.inject_timeout)  // nothing ever arrives on bar_never
-        ok = bounded_wait(smem_u32(&bar_never), 0, abort_ptr, p.status, kSiteInject);
-      ok = ok && bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ);
-      ok = ok && wait_kv(0);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          if ((t ? n_1 : n_0) == 0) continue;
-          issue_qk(t, slot_addr(0));
-          mma_commit(smem_u32(&bar_s_full[t]));
-        }
-        mma_commit(smem_u32(&bar_kv_empty[0]));
+    bool ok = true;
+    if (p.inject_timeout)  // nothing ever arrives on bar_never
+      ok = wait(smem_u32(&bar_never), 0, kSiteInject);
+    ok = ok && wait(smem_u32(&bar_q), 0, kSiteQ);
+    ok = ok && wait_kv(0);
+    if (ok) {
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        if ((t ? n_1 : n_0) == 0) continue;
+        issue_qk(t, slot_addr(0));
+        mma_commit_w(smem_u32(&bar_s_full[t]));
       }
-      for (int j = 0; j < n && ok; ++j) {
-        const int iv = 2 * j + 1;  // ring index of V_j
-        const int ik = 2 * j + 2;  // ring index of K_{j+1}
-        const bool next = j + 1 < n;
-        ok = wait_kv(iv) && (!next || wait_kv(ik));
-        if (!ok) break;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nt = t ? n_1 : n_0;
-          if (j >= nt) continue;
-          ok = bounded_wait(smem_u32(&bar_p_full[t]), j & 1, abort_ptr, p.status, kSitePFull);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, slot_addr(iv), j > 0);
-          if (j == nt - 1) mma_commit(smem_u32(&bar_o_done[t]));
-          if (next && j + 1 < nt) {
-            issue_qk(t, slot_addr(ik));
-            mma_commit(smem_u32(&bar_s_full[t]));
-          }
-        }
-        if (!ok) break;
-        mma_commit(smem_u32(&bar_kv_empty[iv % C::kSlots]));
-        if (next) mma_commit(smem_u32(&bar_kv_empty[ik % C::kSlots]));
-      }
-      // Every MMA issued above completes before the tensor memory is released.
-      mma_commit(smem_u32(&bar_drain));
-      drain_wait(smem_u32(&bar_drain), 0);
+      mma_commit_w(smem_u32(&bar_kv_empty[0]));
     }
+    for (int j = 0; j < n && ok; ++j) {
+      const int iv = 2 * j + 1;  // ring index of V_j
+      const int ik = 2 * j + 2;  // ring index of K_{j+1}
+      const bool next = j + 1 < n;
+      ok = wait_kv(iv) && (!next || wait_kv(ik));
+      if (!ok) break;
+      for (int t = 0; t < 2 && ok; ++t) {
+        const int nt = t ? n_1 : n_0;
+        if (j >= nt) continue;
+        ok = wait(smem_u32(&bar_p_full[t]), j & 1, kSitePFull);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(t, slot_addr(iv), j > 0);
+        if (j == nt - 1) mma_commit_w(smem_u32(&bar_o_done[t]));
+        if (next && j + 1 < nt) {
+          issue_qk(t, slot_addr(ik));
+          mma_commit_w(smem_u32(&bar_s_full[t]));
+        }
+      }
+      if (!ok) break;
+      mma_commit_w(smem_u32(&bar_kv_empty[iv % C::kSlots]));
+      if (next) mma_commit_w(smem_u32(&bar_kv_empty[ik % C::kSlots]));
+    }
+    // Every MMA issued above completes before the tensor memory is released.
+    mma_commit_w(smem_u32(&bar_drain));
+    drain_wait(smem_u32(&bar_drain), 0);
     __syncwarp();
   } else {
     // ================================================================ softmax

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -9,23 +10,81 @@ namespace gbattn {
 
 constexpr int kTile = 128;  // query / key tile rows of the main kernels
 
+// ---------------------------------------------------------------- fp16 scaling
+// The backward runs its tensor-core products in fp16 (2^-11 relative
+// rounding of P and dS instead of bf16's 2^-9). Each fp16 operand tensor is
+// multiplied by an exact power of two chosen from the tensor's largest
+// magnitude, so that nothing overflows and the scaling adds no rounding:
+//   q~, k~ : largest |value| below 2^14   (|R x| <= sqrt(2) max|x|)
+//   v, dO  : largest |value| below 2^3, so |dP| <= 64 D and |dS| <= 128 D < 2^15.
+// Index of each tensor's maximum in the 4-float array written by the
+// abs-max pass.
+enum { kMaxQ = 0, kMaxK = 1, kMaxV = 2, kMaxDO = 3 };
+constexpr int kTargetQK = 14;
+constexpr int kTargetVDO = 3;
+constexpr int kMaxScaleExp = 40;
+
+// Exponent e (|e| <= kMaxScaleExp) with m * 2^e < 2^target for a finite m >= 0.
+__host__ __device__ inline int pow2_exponent(float m, int target) {
+  uint32_t bits;
+  memcpy(&bits, &m, 4);
+  const int ex = static_cast<int>((bits >> 23) & 0xffu);
+  int e;
+  if (ex == 255) e = 0;                       // inf / nan: outputs are non-finite anyway
+  else if (ex == 0) e = kMaxScaleExp;         // zero or subnormal maximum
+  else e = target - (ex - 126);               // m < 2^(ex - 126)
+  return e < -kMaxScaleExp ? -kMaxScaleExp : (e > kMaxScaleExp ? kMaxScaleExp : e);
+}
+// 2^e as a float, |e| <= 126.
+__host__ __device__ inline float exp2i(int e) {
+  const uint32_t bits = static_cast<uint32_t>(127 + e) << 23;
+  float f;
+  memcpy(&f, &bits, 4);
+  return f;
+}
+struct BwdExponents {
+  int q, k, v, dout;
+};
+__host__ __device__ inline BwdExponents bwd_exponents(const float* maxes) {
+  BwdExponents x;
+  x.q = pow2_exponent(maxes[kMaxQ] * 1.4142136f, kTargetQK);
+  x.k = pow2_exponent(maxes[kMaxK] * 1.4142136f, kTargetQK);
+  x.v = pow2_exponent(maxes[kMaxV], kTargetVDO);
+  x.dout = pow2_exponent(maxes[kMaxDO], kTargetVDO);
+  return x;
+}
+
+// ---------------------------------------------------------------- row kernels
 // RoPE cos/sin table, [S][D/2] fp32 each, built in fp64.
 cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
                               cudaStream_t stream);
 
-// Rotates rows of x (bf16 [rows][D], position = row % S) into y (bf16).
-// When `delta` is non-null it also writes delta[row] = sum_d a[row][d] * b[row][d]
-// (bf16 a, b), lse2[row] = lse[row] * log2(e), and zeroes dqacc[row][:] (fp32).
+// Largest |value| of up to four bf16 tensors, atomically max-ed into maxes[i]
+// (which the caller zeroes first).
+struct AbsMaxParams {
+  const void* x[4];
+  long long n[4];  // element counts, multiples of 8
+  float* maxes;
+};
+cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream);
+
+enum RowPrepMode { kPrepFwd = 0, kPrepBwdQ = 1, kPrepBwdK = 2 };
+// kPrepFwd : y = bf16(R x)                       (forward RoPE pre-pass)
+// kPrepBwdQ: y = fp16(bf16(R q) 2^eq), y2 = fp16(dout 2^edo),
+//            delta = (dout . out) 2^(edo+ev), lse2 = lse log2(e), dqacc row = 0
+// kPrepBwdK: y = fp16(bf16(R k) 2^ek),  y2 = fp16(v 2^ev)
 struct RowPrepParams {
+  int mode;
   const void* x;
   void* y;
   long long rows;
   int S, D;
   const float* cos_tab;
   const float* sin_tab;
-  // optional backward extras (query rows only)
-  const void* a;  // out
-  const void* b;  // dout
+  const float* maxes;  // backward modes
+  const void* x2;      // dout (BwdQ) or v (BwdK)
+  void* y2;
+  const void* out;     // BwdQ
   float* delta;
   const float* lse;
   float* lse2;
@@ -33,16 +92,17 @@ struct RowPrepParams {
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
-// dq = scale * R_iᵀ dqacc (fp32 in, fp32 out).
+// dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in, fp32 out).
 cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
-                               float scale, const float* cos_tab, const float* sin_tab,
-                               cudaStream_t stream);
+                               float scale, const float* maxes, const float* cos_tab,
+                               const float* sin_tab, cudaStream_t stream);
 
+// ---------------------------------------------------------------- main kernels
 struct FwdParams {
-  CUtensorMap map_q;    // rotated q, box {64, 128}
-  CUtensorMap map_k;    // rotated k, box {64, 128}
-  CUtensorMap map_v;    // v, box {64, 128}
-  CUtensorMap map_out;  // out, box {64, 128}
+  CUtensorMap map_q;    // rotated q (bf16), box {64, 128}
+  CUtensorMap map_k;    // rotated k (bf16), box {64, 128}
+  CUtensorMap map_v;    // v (bf16), box {64, 128}
+  CUtensorMap map_out;  // out (bf16), box {64, 128}
   float* lse;
   int* status;
   int B, Hq, Hkv, S, D;
@@ -53,13 +113,14 @@ struct FwdParams {
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 
 struct BwdParams {
-  CUtensorMap map_q;   // rotated q, box {64, BQ}
-  CUtensorMap map_do;  // dout, box {64, BQ}
-  CUtensorMap map_k;   // rotated k, box {64, 128}
-  CUtensorMap map_v;   // v, box {64, 128}
+  CUtensorMap map_q;   // scaled rotated q (fp16), box {64, BQ}
+  CUtensorMap map_do;  // scaled dout (fp16), box {64, BQ}
+  CUtensorMap map_k;   // scaled rotated k (fp16), box {64, 128}
+  CUtensorMap map_v;   // scaled v (fp16), box {64, 128}
   const float* lse2;   // lse * log2(e), [B*Hq*S]
-  const float* delta;  // [B*Hq*S]
-  float* dqacc;        // [B*Hq*S][D] fp32, accumulated with atomics
+  const float* delta;  // scaled delta, [B*Hq*S]
+  const float* maxes;  // the abs-max pass's four maxima
+  float* dqacc;        // [B*Hq*S][D] fp32, accumulated with atomics (scaled)
   float* dk;           // [B*Hkv*S][D] fp32
   float* dv;           // [B*Hkv*S][D] fp32
   const float* cos_tab;

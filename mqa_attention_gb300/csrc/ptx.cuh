@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #define GB_DEV __device__ __forceinline__
 
@@ -141,7 +142,7 @@ GB_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 GB_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 GB_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc), bf16 inputs, fp32 accumulate.
+// D(tmem) (+)= A(smem desc) * B(smem desc), 16-bit inputs, fp32 accumulate.
 GB_DEV void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                    uint32_t accumulate) {
   asm volatile(
@@ -166,6 +167,38 @@ GB_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
+}
+
+// Warp-wide forms: the whole (converged) warp executes them with identical,
+// warp-uniform operands and elect.sync picks one lane to issue (always the
+// same lane, so its commits track its own MMAs).
+GB_DEV void mma_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 x;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync x|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+GB_DEV void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 x;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync x|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+GB_DEV void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 x;\n\t"
+      "elect.sync x|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // Loads 32 consecutive 32-bit TMEM columns of this thread's lane (32x32b
@@ -241,6 +274,14 @@ GB_DEV void red_add_v4_f32(float* addr, float a, float b, float c, float d) {
 //   MN-major operand: 64-element MN chunks `lbo` bytes apart, 8-row K groups
 //                    `sbo` bytes apart.
 // Tiles start on 1024-byte boundaries, so the base-offset field stays 0.
+// Upper descriptor bits (everything but the start address) for given LBO/SBO;
+// a descriptor is then sdesc_hi(...) | (saddr >> 4) for 16-byte aligned shared
+// addresses below 256 KB.
+__host__ __device__ constexpr uint64_t sdesc_hi(uint32_t lbo, uint32_t sbo) {
+  return (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
 GB_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
@@ -251,16 +292,23 @@ GB_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+// Instruction descriptor, kind::f16 with fp32 D.
 // a_mn / b_mn: 0 = K-major operand, 1 = MN-major operand.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+// fmt: 0 = fp16 A and B, 1 = bf16 A and B (one MMA never mixes the two).
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, int a_mn, int b_mn, int fmt) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | (static_cast<uint32_t>(fmt) << 7)         // A format
+         | (static_cast<uint32_t>(fmt) << 10)        // B format
          | (static_cast<uint32_t>(a_mn) << 15)       // A major
          | (static_cast<uint32_t>(b_mn) << 16)       // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, 1);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, int a_mn, int b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, 0);
 }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
@@ -273,6 +321,10 @@ GB_DEV uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
 
 GB_DEV uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+GB_DEV uint32_t pack_fp16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

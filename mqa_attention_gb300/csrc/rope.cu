@@ -1,14 +1,17 @@
 // HBM-bound row kernels around the attention main kernels:
 //   * the RoPE cos/sin table (built once per (S, D, theta) in fp64, stored fp32),
-//   * the RoPE pre-pass that rotates q and k rows into bf16 (forward and backward),
-//     fused, for the backward, with delta_i = dout_i . out_i, lse in base 2 and the
-//     zeroing of the fp32 dq accumulator,
+//   * the abs-max pass that fixes the backward's power-of-two fp16 scales,
+//   * the RoPE pre-pass that rotates q and k rows (bf16 for the forward; for the
+//     backward bf16-rounded, scaled and stored fp16, fused with the fp16 copies of
+//     dout and v, delta_i = dout_i . out_i, lse in base 2 and the zeroing of the
+//     fp32 dq accumulator),
 //   * the dq finalisation dq_i = scale * R_iᵀ dq~_i.
 // RoPE is the half-split rotation x*cos + rotate_half(x)*sin with
 // rotate_half(x) = cat(-x2, x1) and inverse frequencies theta^(-2i/D)
 // ("Picotron模型实现解析Llama架构与Flash Attention集成", §1 嵌入层与位置编码;
 //  "ColossalAI 中的 PaLM 教学实现…", §2.3 RotaryEmbedding).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.h"
 
@@ -31,8 +34,8 @@ __global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict
   sin_tab[idx] = static_cast<float>(s);
 }
 
-struct alignas(16) Bf16x8 {
-  __nv_bfloat162 v[4];
+struct alignas(16) Vec8x16 {
+  uint32_t w[4];
 };
 
 __device__ __forceinline__ void load8(const float* p, float (&o)[8]) {
@@ -46,23 +49,67 @@ __device__ __forceinline__ void store8(float* p, const float (&o)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
 __device__ __forceinline__ void load8_bf16(const void* p, float (&o)[8]) {
-  const Bf16x8 x = *reinterpret_cast<const Bf16x8*>(p);
+  const Vec8x16 x = *reinterpret_cast<const Vec8x16*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(x.v[i]);
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.w[i]));
     o[2 * i] = f.x;
     o[2 * i + 1] = f.y;
   }
 }
 __device__ __forceinline__ void store8_bf16(void* p, const float (&o)[8]) {
-  Bf16x8 x;
+  Vec8x16 x;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) x.v[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-  *reinterpret_cast<Bf16x8*>(p) = x;
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+    x.w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<Vec8x16*>(p) = x;
+}
+// Rounds to bf16 (nearest even), multiplies by the power of two s (exact) and
+// stores as fp16 (exact while the result is a normal fp16 number).
+__device__ __forceinline__ void store8_bf16_scaled_f16(void* p, const float (&o)[8], float s) {
+  Vec8x16 x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = __bfloat162float(__float2bfloat16_rn(o[2 * i])) * s;
+    const float b = __bfloat162float(__float2bfloat16_rn(o[2 * i + 1])) * s;
+    __half2 h = __floats2half2_rn(a, b);
+    x.w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<Vec8x16*>(p) = x;
+}
+
+__global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
+  __shared__ float red[8];
+#pragma unroll 1
+  for (int t = 0; t < 4; ++t) {
+    if (p.x[t] == nullptr) continue;
+    const long long chunks = p.n[t] / 8;
+    float m = 0.f;
+    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
+         c += (long long)gridDim.x * blockDim.x) {
+      float v[8];
+      load8_bf16(static_cast<const __nv_bfloat16*>(p.x[t]) + c * 8, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = 0.f;
+      for (int w = 0; w < 8; ++w) b = fmaxf(b, red[w]);
+      // non-negative floats order like their bit patterns
+      atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), __float_as_uint(b));
+    }
+    __syncthreads();
+  }
 }
 
 // One thread per (row, c) with c < D/16: elements [8c, 8c+8) and [D/2+8c, D/2+8c+8).
-template <int D, bool kBwd>
+template <int D, int kMode>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
@@ -86,29 +133,43 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
     y1[i] = x1[i] * cs[i] - x2[i] * sn[i];
     y2[i] = x2[i] * cs[i] + x1[i] * sn[i];
   }
-  if (live) {
-    store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e1, y1);
-    store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e2, y2);
-  }
-  if constexpr (kBwd) {
-    float a1[8], a2[8], b1[8], b2[8];
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.a) + e1, a1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.a) + e2, a2);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.b) + e1, b1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.b) + e2, b2);
-    float dot = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dot += a1[i] * b1[i] + a2[i] * b2[i];
-#pragma unroll
-    for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  if constexpr (kMode == kPrepFwd) {
     if (live) {
-      if (c == 0) {
-        p.delta[r] = dot;
-        p.lse2[r] = p.lse[r] * kLog2e;
+      store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e1, y1);
+      store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e2, y2);
+    }
+  } else {
+    const BwdExponents ex = bwd_exponents(p.maxes);
+    const float s_rot = exp2i(kMode == kPrepBwdQ ? ex.q : ex.k);
+    const float s_x2 = exp2i(kMode == kPrepBwdQ ? ex.dout : ex.v);
+    float a1[8], a2[8];
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.x2) + e1, a1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.x2) + e2, a2);
+    if (live) {
+      store8_bf16_scaled_f16(static_cast<__half*>(p.y) + e1, y1, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(p.y) + e2, y2, s_rot);
+      // x2 is already bf16: scaling by a power of two and storing fp16 is exact
+      store8_bf16_scaled_f16(static_cast<__half*>(p.y2) + e1, a1, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(p.y2) + e2, a2, s_x2);
+    }
+    if constexpr (kMode == kPrepBwdQ) {
+      float o1[8], o2[8];
+      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e1, o1);
+      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e2, o2);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
+#pragma unroll
+      for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (live) {
+        if (c == 0) {
+          p.delta[r] = dot * exp2i(ex.dout + ex.v);
+          p.lse2[r] = p.lse[r] * kLog2e;
+        }
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        store8(p.dqacc + e1, z);
+        store8(p.dqacc + e2, z);
       }
-      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      store8(p.dqacc + e1, z);
-      store8(p.dqacc + e2, z);
     }
   }
 }
@@ -116,8 +177,8 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
 template <int D>
 __global__ void __launch_bounds__(256)
     dq_finalize_kernel(const float* __restrict__ dqacc, float* __restrict__ dq, long long rows,
-                       int S, float scale, const float* __restrict__ cos_tab,
-                       const float* __restrict__ sin_tab) {
+                       int S, float scale, const float* __restrict__ maxes,
+                       const float* __restrict__ cos_tab, const float* __restrict__ sin_tab) {
   constexpr int T = D / 16;
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -127,6 +188,8 @@ __global__ void __launch_bounds__(256)
   const int pos = static_cast<int>(row % S);
   const long long e1 = row * D + 8 * c;
   const long long e2 = e1 + H;
+  const BwdExponents ex = bwd_exponents(maxes);
+  const float f = scale * exp2i(-(ex.dout + ex.v + ex.k));
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
   load8(dqacc + e1, x1);
   load8(dqacc + e2, x2);
@@ -135,14 +198,23 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     // transpose of the rotation: rotation by -angle
-    y1[i] = scale * (x1[i] * cs[i] + x2[i] * sn[i]);
-    y2[i] = scale * (x2[i] * cs[i] - x1[i] * sn[i]);
+    y1[i] = f * (x1[i] * cs[i] + x2[i] * sn[i]);
+    y2[i] = f * (x2[i] * cs[i] - x1[i] * sn[i]);
   }
   store8(dq + e1, y1);
   store8(dq + e2, y2);
 }
 
 long long blocks_for(long long threads) { return (threads + 255) / 256; }
+
+template <int D>
+void launch_prep_d(const RowPrepParams& p, unsigned grid, cudaStream_t stream) {
+  switch (p.mode) {
+    case kPrepFwd: row_prep_kernel<D, kPrepFwd><<<grid, 256, 0, stream>>>(p); break;
+    case kPrepBwdQ: row_prep_kernel<D, kPrepBwdQ><<<grid, 256, 0, stream>>>(p); break;
+    default: row_prep_kernel<D, kPrepBwdK><<<grid, 256, 0, stream>>>(p); break;
+  }
+}
 
 }  // namespace
 
@@ -153,29 +225,35 @@ cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, doub
   return cudaGetLastError();
 }
 
+cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
+  long long most = 0;
+  for (int t = 0; t < 4; ++t) most = p.n[t] > most ? p.n[t] : most;
+  long long blocks = blocks_for(most / 8);
+  if (blocks > 4 * 152 * 8) blocks = 4 * 152 * 8;  // grid-stride beyond a few waves
+  if (blocks < 1) blocks = 1;
+  absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
   const long long threads = p.rows * (p.D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
-  const bool bwd = p.delta != nullptr;
-  if (p.D == 128) {
-    if (bwd) row_prep_kernel<128, true><<<grid, 256, 0, stream>>>(p);
-    else row_prep_kernel<128, false><<<grid, 256, 0, stream>>>(p);
-  } else {
-    if (bwd) row_prep_kernel<64, true><<<grid, 256, 0, stream>>>(p);
-    else row_prep_kernel<64, false><<<grid, 256, 0, stream>>>(p);
-  }
+  if (p.D == 128) launch_prep_d<128>(p, grid, stream);
+  else launch_prep_d<64>(p, grid, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
-                               float scale, const float* cos_tab, const float* sin_tab,
-                               cudaStream_t stream) {
+                               float scale, const float* maxes, const float* cos_tab,
+                               const float* sin_tab, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
   if (D == 128)
-    dq_finalize_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, cos_tab, sin_tab);
+    dq_finalize_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
+                                                       sin_tab);
   else
-    dq_finalize_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, cos_tab, sin_tab);
+    dq_finalize_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
+                                                      sin_tab);
   return cudaGetLastError();
 }
 
