@@ -127,6 +127,27 @@ int attn_debug_inject_timeout(int enable);
 /* Library version string. */
 const char* attn_version(void);
 
+/* Forward pass that allocates nothing (no counterpart on the source pages: it exists
+ * for callers of this library that may not allocate GPU memory, e.g. services that
+ * reserve all device memory up front or runtimes that own the allocator).
+ * Arguments, layouts, results and argument errors are those of attn_fwd. Instead of
+ * attn_fwd's pooled workspace and cached RoPE tables it uses one fixed array of
+ * ATTN_FWD_NOALLOC_SCRATCH_BYTES in device memory that the CUDA runtime reserves on
+ * every GPU where the library's code is loaded and keeps until the process exits.
+ * Limit: 256 + 2*round256(4*S*D/2) + round256(2*B*Hq*S*D) + round256(2*B*Hkv*S*D)
+ * bytes must fit in that array (e.g. B=1, Hq=32, Hkv=8, S=4096, D=128 needs 44 MB);
+ * larger problems return ATTN_ERR_UNSUPPORTED.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * All calls on a device share the array and leave their contents in it: calls whose
+ * GPU work overlaps (other streams, other host threads) race and give undefined
+ * results. A kernel wait that expires here leaves out/lse undefined and is not
+ * reported by attn_sync_status. No cudaMalloc, cudaFree or allocating routine. */
+#define ATTN_FWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int S, int D, float rope_theta, float scale, int causal,
+                     attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

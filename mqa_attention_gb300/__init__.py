@@ -19,6 +19,7 @@ __all__ = [
     "lib",
     "attn_fwd",
     "attn_bwd",
+    "attn_fwd_noalloc",
     "forward",
     "backward",
     "sync_status",
@@ -52,6 +53,7 @@ EXPORTED_SYMBOLS = (
     "attn_profile_query",
     "attn_debug_inject_timeout",
     "attn_version",
+    "attn_fwd_noalloc",
 )
 
 
@@ -99,6 +101,8 @@ def lib() -> ctypes.CDLL:
             L.attn_debug_inject_timeout.restype = _I
             L.attn_version.argtypes = []
             L.attn_version.restype = ctypes.c_char_p
+            L.attn_fwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P]
+            L.attn_fwd_noalloc.restype = _I
             _lib = L
         return _lib
 
@@ -131,6 +135,17 @@ def attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, str
     _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
                           int(Hkv), int(S), int(D), float(rope_theta), float(scale),
                           1 if causal else 0, _stream(stream)), "attn_fwd")
+
+
+def attn_fwd_noalloc(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal,
+                     stream=None):
+    """C ABI attn_fwd_noalloc: attn_fwd for callers that may not allocate GPU memory
+    (it works in a fixed array the library reserves on each GPU; see attn.h for the
+    size limit and the rule that overlapping calls race)."""
+    _check(lib().attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
+                                  int(Hq), int(Hkv), int(S), int(D), float(rope_theta),
+                                  float(scale), 1 if causal else 0, _stream(stream)),
+           "attn_fwd_noalloc")
 
 
 def attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
