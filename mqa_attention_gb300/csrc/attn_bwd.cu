@@ -461,6 +461,373 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// D = 128: double-buffered variant. Two (Sᵀ, dPᵀ) accumulator buffers let the
+// MMAs of step s+2 run while the softmax of step s+1 works, so the softmax is
+// no longer serialised behind the score MMAs. TMEM (512 columns):
+//   buffer b in {0,1}: Sᵀ_b [128b, 128b+64), dPᵀ_b [128b+64, 128b+128)
+//   dV [256, 384), dK [384, 512)
+// Pᵀ of a step is written back over that step's Sᵀ columns (each softmax half
+// inside its own 32 columns: half h packs into [128b+32h, 128b+32h+16)), and the
+// step's dQᵀ partial is accumulated over its dPᵀ columns, both after the softmax
+// has read them.
+struct DbCfg {
+  static constexpr int D = 128;
+  static constexpr int BQ = 64;
+  static constexpr int kKRegionBytes = 128 * 128;
+  static constexpr int kQRegionBytes = BQ * 128;
+  static constexpr int kKTileBytes = 2 * kKRegionBytes;
+  static constexpr int kQTileBytes = 2 * kQRegionBytes;
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
+  static constexpr int kDsBytes = 16384;  // dSᵀ: 128 key rows x 64 queries fp16
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKTileBytes;
+  static constexpr int kStageOff = 2 * kKTileBytes;
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kDsOff + 2 * kDsBytes + 1024;
+  __device__ static constexpr uint32_t col_st(int buf) { return buf ? 128u : 0u; }
+  __device__ static constexpr uint32_t col_dpt(int buf) { return buf ? 192u : 64u; }
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 384;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_db_kernel(const __grid_constant__ BwdParams p) {
+  using C = DbCfg;
+  constexpr int D = C::D;
+  constexpr int BQ = C::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
+
+  // ---- work item: key tile kt of KV head (b, hkv); heaviest (kt = 0) first
+  const int BHk = p.B * p.Hkv;
+  const int kt = static_cast<int>(blockIdx.x) / BHk;
+  const int bhk = static_cast<int>(blockIdx.x) % BHk;
+  const int b = bhk / p.Hkv;
+  const int hkv = bhk % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int k0 = kt * kTile;
+  const int kv_row = bhk * p.S + k0;
+  const int nqt = p.S / BQ;
+  const int qt_begin = p.causal ? k0 / BQ : 0;
+  const int per_head = nqt - qt_begin;
+  const int n = G * per_head;
+  const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
+  auto step_qt = [&](int s) { return qt_begin + s % per_head; };
+  auto step_row = [&](int s) {
+    const int h = hkv * G + s / per_head;
+    return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
+  };
+
+  // ---- setup
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_kv), 1);
+    mbar_init(smem_u32(&bar_done), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_never), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bar_stage_full[s]), 1);
+      mbar_init(smem_u32(&bar_stage_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_s_full[i]), 1);
+      mbar_init(smem_u32(&bar_ds_full[i]), 256);
+      mbar_init(smem_u32(&bar_dq_full[i]), 1);
+      mbar_init(smem_u32(&bar_dq_free[i]), 128);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+  auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
+  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s & 1) * C::kDsBytes; };
+
+  if (warp == kWarpLoad) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.map_q);
+      tma_prefetch_desc(&p.map_do);
+      const uint32_t kvb = smem_u32(&bar_kv);
+      mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
+      for (int r = 0; r < 2; ++r) {
+        tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
+        tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
+      }
+      int issued = 0;
+      for (int s = 0; s < n; ++s) {
+        const int st = s % C::kStages;
+        if (!bounded_wait(smem_u32(&bar_stage_empty[st]), ((s / C::kStages) & 1) ^ 1, abort_ptr,
+                          p.status, kSiteStageEmpty))
+          break;
+        const uint32_t full = smem_u32(&bar_stage_full[st]);
+        const uint32_t dst = stage_addr(s);
+        const int row = step_row(s);
+        mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
+        for (int r = 0; r < 2; ++r) {
+          tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
+          tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
+        }
+        bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
+        bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
+        ++issued;
+      }
+      drain_wait(kvb, 0);
+      for (int i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i)
+        drain_wait(smem_u32(&bar_stage_full[i % C::kStages]), (i / C::kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer (whole warp)
+    constexpr uint32_t idesc_st = idesc_fp16(128, BQ, 0, 0);
+    constexpr uint32_t idesc_acc = idesc_fp16(128, D, 0, 1);
+    constexpr uint32_t idesc_dq = idesc_fp16(128, BQ, 1, 1);
+    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);
+    constexpr uint64_t kMnQ = sdesc_hi(C::kQRegionBytes, 1024);
+    constexpr uint64_t kMnK = sdesc_hi(C::kKRegionBytes, 1024);
+    constexpr uint64_t kMnDs = sdesc_hi(16384, 1024);
+    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
+    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
+    };
+    const uint32_t kaddr = sbase + C::kKOff;
+    const uint32_t vaddr = sbase + C::kVOff;
+    // Sᵀ_b = K~ Q~ᵀ and dPᵀ_b = V dOᵀ of step s (b = s & 1)
+    auto issue_s = [&](int s) {
+      const uint32_t qaddr = stage_addr(s);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
+        const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
+        mma_ss_w(tmem + C::col_st(s & 1), desc(kKmaj, kaddr + ok_), desc(kKmaj, qaddr + oq),
+                 idesc_st, kk > 0);
+      }
+    };
+    auto issue_dp = [&](int s) {
+      const uint32_t doaddr = stage_addr(s) + C::kQTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
+        const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
+        mma_ss_w(tmem + C::col_dpt(s & 1), desc(kKmaj, vaddr + ok_), desc(kKmaj, doaddr + oq),
+                 idesc_st, kk > 0);
+      }
+    };
+    auto issue_dvdk = [&](int s, bool first) {
+      const uint32_t qaddr = stage_addr(s);
+      const uint32_t doaddr = qaddr + C::kQTileBytes;
+      const uint32_t pt = tmem + C::col_st(s & 1);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk)  // queries 16kk.. sit at (kk/2)*32 + (kk%2)*8
+        mma_ts_w(tmem + C::kColDV, pt + (kk >> 1) * 32 + (kk & 1) * 8,
+                 desc(kMnQ, doaddr + kk * 2048), idesc_acc, (!first || kk > 0) ? 1u : 0u);
+      const uint32_t dsaddr = ds_addr(s);
+#pragma unroll
+      for (int kk = 0; kk < BQ / 16; ++kk)
+        mma_ss_w(tmem + C::kColDK, desc(kKmaj, dsaddr + kk * 32), desc(kMnQ, qaddr + kk * 2048),
+                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
+    };
+    auto issue_dq = [&](int s) {  // dQᵀ [D x BQ] = K~ᵀ dSᵀ over the step's dPᵀ columns
+      const uint32_t dsaddr = ds_addr(s);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ss_w(tmem + C::col_dpt(s & 1), desc(kMnK, kaddr + kk * 2048),
+                 desc(kMnDs, dsaddr + kk * 2048), idesc_dq, kk > 0);
+    };
+
+    bool ok = true;
+    if (p.inject_timeout)  // nothing ever arrives on bar_never
+      ok = wait(smem_u32(&bar_never), 0, kSiteInject);
+    ok = ok && wait(smem_u32(&bar_kv), 0, kSiteKv);
+    for (int s = 0; s < 2 && s < n && ok; ++s) {
+      ok = wait(smem_u32(&bar_stage_full[s]), 0, kSiteStageFull);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(s);
+      issue_dp(s);
+      mma_commit_w(smem_u32(&bar_s_full[s]));
+    }
+    for (int s = 0; s < n && ok; ++s) {
+      const int buf = s & 1;
+      ok = wait(smem_u32(&bar_ds_full[buf]), (s >> 1) & 1, kSiteDsFull);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dvdk(s, s == 0);
+      mma_commit_w(smem_u32(&bar_stage_empty[s % C::kStages]));
+      issue_dq(s);
+      mma_commit_w(smem_u32(&bar_dq_full[buf]));
+      if (s + 2 < n) {
+        ok = wait(smem_u32(&bar_stage_full[(s + 2) % C::kStages]), ((s + 2) / C::kStages) & 1,
+                  kSiteStageFull);
+        if (!ok) break;
+        issue_s(s + 2);  // after dV(s) in issue order: Pᵀ(s) is read before it is overwritten
+        ok = wait(smem_u32(&bar_dq_free[buf]), (s >> 1) & 1, kSiteDqFree);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(s + 2);  // the drain has read dQᵀ(s) from these columns
+        mma_commit_w(smem_u32(&bar_s_full[buf]));
+      }
+    }
+    if (ok) mma_commit_w(smem_u32(&bar_done));
+    mma_commit_w(smem_u32(&bar_drain));
+    drain_wait(smem_u32(&bar_drain), 0);
+    __syncwarp();
+  } else if (warp >= 8) {
+    // ================================================================ dQ drain
+    const int r = tid & 127;  // TMEM lane = d
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int s = 0; s < n; ++s) {
+      const int buf = s & 1;
+      const bool got = bounded_wait(smem_u32(&bar_dq_full[buf]), (s >> 1) & 1, abort_ptr, p.status,
+                                    kSiteDqFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      uint32_t u0[32], u1[32];
+      tmem_ld32x2(tmem + lane_base + C::col_dpt(buf), tmem + lane_base + C::col_dpt(buf) + 32, u0,
+                  u1);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_dq_free[buf]));
+      float* base = p.dqacc + static_cast<long long>(step_row(s)) * D + r;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+    }
+  } else {
+    // ================================================================ softmax
+    const int half = warp >> 2;
+    const int r = tid & 127;  // key row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
+    const int key = k0 + r;
+    const int qb = half * 32;  // this half's first query column
+    for (int s = 0; s < n; ++s) {
+      const int buf = s & 1;
+      const bool got = bounded_wait(smem_u32(&bar_s_full[buf]), (s >> 1) & 1, abort_ptr, p.status,
+                                    kSiteSFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint32_t st = stage_addr(s);
+      const float4* lse4 =
+          reinterpret_cast<const float4*>(sgen + (st - sbase) + 2 * C::kQTileBytes) + qb / 4;
+      const float4* del4 = lse4 + BQ / 4;
+      const int q0 = step_qt(s) * BQ;
+      uint32_t sv[32], dpv[32];
+      tmem_ld32x2(tmem + lane_base + C::col_st(buf) + qb, tmem + lane_base + C::col_dpt(buf) + qb,
+                  sv, dpv);
+      uint32_t pk[16], dk[16];
+      // keys after the query are masked on the diagonal steps only
+      const int lim = (p.causal && q0 < k0 + kTile) ? key - q0 - qb : -1;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const float4 l4 = lse4[g];
+        const float4 d4 = del4[g];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pr[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float pv = ex2(fmaf(__uint_as_float(sv[4 * g + e]), sl2, -lv[e]));
+          pv = (4 * g + e < lim) ? 0.f : pv;
+          pr[e] = pv;
+          dsv[e] = pv * (__uint_as_float(dpv[4 * g + e]) - dl[e]);
+        }
+        pk[2 * g] = pack_fp16(pr[0], pr[1]);
+        pk[2 * g + 1] = pack_fp16(pr[2], pr[3]);
+        dk[2 * g] = pack_fp16(dsv[0], dsv[1]);
+        dk[2 * g + 1] = pack_fp16(dsv[2], dsv[3]);
+      }
+      // Pᵀ over this half's own (already read) Sᵀ columns
+      tmem_st16(tmem + lane_base + C::col_st(buf) + qb, pk);
+      // dSᵀ row r, query columns qb..qb+31 (chunks 4*half ..), swizzled K-major
+      const uint32_t dsb = ds_addr(s);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        st_shared_v4(dsb + sw128_offset(r, half * 4 + q4), dk[4 * q4], dk[4 * q4 + 1],
+                     dk[4 * q4 + 2], dk[4 * q4 + 3]);
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_ds_full[buf]));
+    }
+    // ------------------------------------------------------------ dK / dV epilogue
+    bounded_wait(smem_u32(&bar_done), 0, abort_ptr, p.status, kSiteDone);
+    __syncwarp();
+    tc_fence_after();
+    const long long grow = kv_row + r;
+    if (half == 0) {
+      const float f = exp2i(-ex.dout);
+      float* dst = p.dv + grow * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(dst + cc * 32)[i] =
+              make_float4(f * __uint_as_float(u[4 * i]), f * __uint_as_float(u[4 * i + 1]),
+                          f * __uint_as_float(u[4 * i + 2]), f * __uint_as_float(u[4 * i + 3]));
+      }
+    } else {
+      const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
+      float* dst = p.dk + grow * D;
+      const float* cs = p.cos_tab + (long long)key * (D / 2);
+      const float* sn = p.sin_tab + (long long)key * (D / 2);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t x1[32], x2[32];
+        tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 32,
+                    tmem + lane_base + C::kColDK + D / 2 + ch * 32, x1, x2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
+          const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
+          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+          const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+          float y1[4], y2[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = __uint_as_float(x1[4 * i + e]);
+            const float bb = __uint_as_float(x2[4 * i + e]);
+            y1[e] = f * (a * cc[e] + bb * ss[e]);
+            y2[e] = f * (bb * cc[e] - a * ss[e]);
+          }
+          reinterpret_cast<float4*>(dst + ch * 32)[i] = make_float4(y1[0], y1[1], y1[2], y1[3]);
+          reinterpret_cast<float4*>(dst + D / 2 + ch * 32)[i] =
+              make_float4(y2[0], y2[1], y2[2], y2[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -475,7 +842,16 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
-  return p.D == 128 ? launch_bwd_d<128>(p, stream) : launch_bwd_d<64>(p, stream);
+  if (p.D == 128) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_db_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DbCfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv);
+    attn_bwd_db_kernel<<<grid, kThreads, DbCfg::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  }
+  return launch_bwd_d<64>(p, stream);
 }
 
 }  // namespace gbattn

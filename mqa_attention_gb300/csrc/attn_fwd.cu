@@ -261,13 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
       }
-      const bool diag = p.causal && j == qt;
-      float mx = -INFINITY;
+      if (p.causal && j == qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        if (diag && i > r) s[i] = -INFINITY;
-        mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < 128; ++i) s[i] = i > r ? -INFINITY : s[i];
       }
+      // Row maximum as 8 independent partial chains (latency, not issue, bound).
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[i + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float mx2 = mx * sl2;
       float alpha = 1.f;
       bool grew = false;
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         grew = true;
         m = mx2;
       }
-      float rs = 0.f;
+      float rp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -286,11 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int i = 0; i < 32; ++i) {
           const float a0 = ex2(fmaf(s[hh * 64 + 2 * i], sl2, -m));
           const float a1 = ex2(fmaf(s[hh * 64 + 2 * i + 1], sl2, -m));
-          rs += a0 + a1;
+          rp[i & 7] += a0 + a1;
           pk[i] = pack_bf16(a0, a1);
         }
         tmem_st32(tS + hh * 32, pk);
       }
+      const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       l = l * alpha + rs;
       if (j > 0 && __any_sync(0xffffffffu, grew)) {
         const float f = grew ? alpha : 1.f;
