@@ -238,16 +238,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   bool ok = true;
   {
     gbattn::RowPrepParams rp{};
-    rp.mode = gbattn::kPrepFwd;
+    rp.bwd = 0;
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
+    rp.seg[0] = {q, qr, nullptr, nullptr, qrows};
+    rp.seg[1] = {k, kr, nullptr, nullptr, krows};
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
-    rp.x = q; rp.y = qr; rp.rows = qrows;
-    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
-    rp.x = k; rp.y = kr; rp.rows = krows;
-    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
+    ok = gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
   }
   gbattn::FwdParams fp{};
@@ -302,6 +301,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   float* lse2 = reinterpret_cast<float*>(w); w += rowbytes;
   float* maxes = reinterpret_cast<float*>(w);
 
+  // Two CTAs per (KV head, key tile), each with half of the group's query heads,
+  // when the group splits evenly.
+  const int hsplit = (Hq / Hkv) % 2 == 0 ? 2 : 1;
   bool ok = true;
   {
     LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
@@ -314,18 +316,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     ok = cudaMemsetAsync(maxes, 0, 4 * sizeof(float), stream) == cudaSuccess &&
          gbattn::launch_absmax(ap, stream) == cudaSuccess;
     gbattn::RowPrepParams rp{};
+    rp.bwd = 1;
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
     rp.maxes = maxes;
-    rp.mode = gbattn::kPrepBwdQ;
-    rp.x = q; rp.y = qr; rp.rows = qrows; rp.x2 = dout; rp.y2 = dos;
+    rp.seg[0] = {q, qr, dout, dos, qrows};
+    rp.seg[1] = {k, kr, v, vs, krows};
     rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
-    ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
-    rp.mode = gbattn::kPrepBwdK;
-    rp.x = k; rp.y = kr; rp.rows = krows; rp.x2 = v; rp.y2 = vs;
-    rp.out = nullptr; rp.delta = nullptr; rp.lse = nullptr; rp.lse2 = nullptr; rp.dqacc = nullptr;
+    if (hsplit > 1) {  // the main kernel adds dK/dV partials of two CTAs
+      rp.dk_zero = dk;
+      rp.dv_zero = dv;
+    }
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
   }
@@ -350,6 +353,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     bp.scale_log2 = scale * 1.4426950408889634f;
     bp.causal = causal ? 1 : 0;
     bp.inject_timeout = g_inject_timeout ? 1 : 0;
+    bp.hsplit = hsplit;
     LaunchTimer tm(ATTN_KERNEL_BWD_MAIN, stream);
     ok = gbattn::launch_bwd_main(bp, stream) == cudaSuccess;
     tm.done();

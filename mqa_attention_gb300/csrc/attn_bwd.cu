@@ -14,7 +14,10 @@
 //
 // GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
 // shared memory and walks the (query head, query tile) steps that see its keys
-// (only tiles on or below the diagonal when causal). Per step s, in TMEM:
+// (only tiles on or below the diagonal when causal). When the group has an even
+// number of query heads, two CTAs share a key tile, each taking half of the
+// heads, and add their dK/dV partials into zeroed outputs: the heaviest
+// (first) key tiles then no longer outlast the average SM's load. Per step s, in TMEM:
 //   Sᵀ  = K~ Q~ᵀ      [128 keys x BQ]    (SS MMA)
 //   dPᵀ = V dOᵀ       [128 keys x BQ]    (SS MMA)
 //   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta);
@@ -89,6 +92,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Writes 4 consecutive floats, or adds them (fp32 reduction) when several CTAs
+// contribute to the same row.
+__device__ __forceinline__ void put4(float* dst, float a, float b, float c, float d, bool add) {
+  if (add) red_add_v4_f32(dst, a, b, c, d);
+  else *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -106,24 +116,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
 
-  // ---- work item: key tile kt of KV head (b, hkv); heaviest (kt = 0) first
-  const int BHk = p.B * p.Hkv;
-  const int kt = static_cast<int>(blockIdx.x) / BHk;
-  const int bhk = static_cast<int>(blockIdx.x) % BHk;
+  // ---- work item: key tile kt of KV head (b, hkv), query heads of part `part`
+  // of the group (hsplit parts); heaviest (kt = 0) first
+  const int units = p.B * p.Hkv * p.hsplit;
+  const int kt = static_cast<int>(blockIdx.x) / units;
+  const int unit = static_cast<int>(blockIdx.x) % units;
+  const int bhk = unit / p.hsplit;
+  const int part = unit % p.hsplit;
   const int b = bhk / p.Hkv;
   const int hkv = bhk % p.Hkv;
   const int G = p.Hq / p.Hkv;
+  const int Gc = G / p.hsplit;  // query heads of this CTA
+  const int h_first = hkv * G + part * Gc;
   const int k0 = kt * kTile;
   const int kv_row = bhk * p.S + k0;
   const int nqt = p.S / BQ;
   const int qt_begin = p.causal ? k0 / BQ : 0;
   const int per_head = nqt - qt_begin;
-  const int n = G * per_head;
+  const int n = Gc * per_head;
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   // step s -> (query head, query tile)
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
-    const int h = hkv * G + s / per_head;
+    const int h = h_first + s / per_head;
     return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
   };
 
@@ -405,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     __syncwarp();
     tc_fence_after();
     const long long grow = kv_row + r;
+    const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
     if (half == 0) {
       // dV accumulated Pᵀ (dO 2^edo)
       const float f = exp2i(-ex.dout);
@@ -415,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst + cc * 32)[i] =
-              make_float4(f * __uint_as_float(u[4 * i]), f * __uint_as_float(u[4 * i + 1]),
-                          f * __uint_as_float(u[4 * i + 2]), f * __uint_as_float(u[4 * i + 3]));
+          put4(dst + cc * 32 + 4 * i, f * __uint_as_float(u[4 * i]),
+               f * __uint_as_float(u[4 * i + 1]), f * __uint_as_float(u[4 * i + 2]),
+               f * __uint_as_float(u[4 * i + 3]), sum_parts);
       }
     } else {
       // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2); dK
@@ -445,9 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             y1[e] = f * (a * cc[e] + bb * ss[e]);
             y2[e] = f * (bb * cc[e] - a * ss[e]);
           }
-          reinterpret_cast<float4*>(dst + ch * 32)[i] = make_float4(y1[0], y1[1], y1[2], y1[3]);
-          reinterpret_cast<float4*>(dst + D / 2 + ch * 32)[i] =
-              make_float4(y2[0], y2[1], y2[2], y2[3]);
+          put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
+          put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
         }
       }
     }
@@ -511,23 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
 
-  // ---- work item: key tile kt of KV head (b, hkv); heaviest (kt = 0) first
-  const int BHk = p.B * p.Hkv;
-  const int kt = static_cast<int>(blockIdx.x) / BHk;
-  const int bhk = static_cast<int>(blockIdx.x) % BHk;
+  // ---- work item: key tile kt of KV head (b, hkv), query heads of part `part`
+  // of the group (hsplit parts); heaviest (kt = 0) first
+  const int units = p.B * p.Hkv * p.hsplit;
+  const int kt = static_cast<int>(blockIdx.x) / units;
+  const int unit = static_cast<int>(blockIdx.x) % units;
+  const int bhk = unit / p.hsplit;
+  const int part = unit % p.hsplit;
   const int b = bhk / p.Hkv;
   const int hkv = bhk % p.Hkv;
   const int G = p.Hq / p.Hkv;
+  const int Gc = G / p.hsplit;  // query heads of this CTA
+  const int h_first = hkv * G + part * Gc;
   const int k0 = kt * kTile;
   const int kv_row = bhk * p.S + k0;
   const int nqt = p.S / BQ;
   const int qt_begin = p.causal ? k0 / BQ : 0;
   const int per_head = nqt - qt_begin;
-  const int n = G * per_head;
+  const int n = Gc * per_head;
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
-    const int h = hkv * G + s / per_head;
+    const int h = h_first + s / per_head;
     return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
   };
 
@@ -775,6 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     const long long grow = kv_row + r;
+    const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
     if (half == 0) {
       const float f = exp2i(-ex.dout);
       float* dst = p.dv + grow * D;
@@ -784,9 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst + cc * 32)[i] =
-              make_float4(f * __uint_as_float(u[4 * i]), f * __uint_as_float(u[4 * i + 1]),
-                          f * __uint_as_float(u[4 * i + 2]), f * __uint_as_float(u[4 * i + 3]));
+          put4(dst + cc * 32 + 4 * i, f * __uint_as_float(u[4 * i]),
+               f * __uint_as_float(u[4 * i + 1]), f * __uint_as_float(u[4 * i + 2]),
+               f * __uint_as_float(u[4 * i + 3]), sum_parts);
       }
     } else {
       const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
@@ -812,9 +833,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             y1[e] = f * (a * cc[e] + bb * ss[e]);
             y2[e] = f * (bb * cc[e] - a * ss[e]);
           }
-          reinterpret_cast<float4*>(dst + ch * 32)[i] = make_float4(y1[0], y1[1], y1[2], y1[3]);
-          reinterpret_cast<float4*>(dst + D / 2 + ch * 32)[i] =
-              make_float4(y2[0], y2[1], y2[2], y2[3]);
+          put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
+          put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
         }
       }
     }
@@ -834,7 +854,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv);
+  const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv * p.hsplit);
   attn_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
@@ -847,7 +867,7 @@ cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DbCfg::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv);
+    const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv * p.hsplit);
     attn_bwd_db_kernel<<<grid, kThreads, DbCfg::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
   }

@@ -68,27 +68,33 @@ struct AbsMaxParams {
 };
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream);
 
-enum RowPrepMode { kPrepFwd = 0, kPrepBwdQ = 1, kPrepBwdK = 2 };
-// kPrepFwd : y = bf16(R x)                       (forward RoPE pre-pass)
-// kPrepBwdQ: y = fp16(bf16(R q) 2^eq), y2 = fp16(dout 2^edo),
-//            delta = (dout . out) 2^(edo+ev), lse2 = lse log2(e), dqacc row = 0
-// kPrepBwdK: y = fp16(bf16(R k) 2^ek),  y2 = fp16(v 2^ev)
-struct RowPrepParams {
-  int mode;
+// Row pre-pass over the query rows (segment 0) and key rows (segment 1) of one
+// call, in one launch. Forward (bwd == 0): y = bf16(R x) for both segments.
+// Backward (bwd == 1):
+//   query rows: y = fp16(bf16(R q) 2^eq), y2 = fp16(dout 2^edo),
+//               delta = (dout . out) 2^(edo+ev), lse2 = lse log2(e), dqacc row = 0
+//   key rows:   y = fp16(bf16(R k) 2^ek),  y2 = fp16(v 2^ev)
+struct RowSegment {
   const void* x;
   void* y;
+  const void* x2;  // backward: dout (query rows) or v (key rows)
+  void* y2;
   long long rows;
+};
+struct RowPrepParams {
+  int bwd;
+  RowSegment seg[2];
   int S, D;
   const float* cos_tab;
   const float* sin_tab;
-  const float* maxes;  // backward modes
-  const void* x2;      // dout (BwdQ) or v (BwdK)
-  void* y2;
-  const void* out;     // BwdQ
+  const float* maxes;  // backward
+  const void* out;     // backward, query rows
   float* delta;
   const float* lse;
   float* lse2;
   float* dqacc;
+  float* dk_zero;  // backward, key rows: zeroed when the main kernel sums dK/dV partials
+  float* dv_zero;
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
@@ -131,6 +137,7 @@ struct BwdParams {
   float scale_log2;
   int causal;
   int inject_timeout;
+  int hsplit;  // CTAs sharing one (KV head, key tile): 1, or 2 (dK/dV summed with reductions)
 };
 // Query-tile rows used by the backward main kernel for head dimension D.
 inline int bwd_query_tile(int D) { return D == 128 ? 64 : 128; }

@@ -128,14 +128,13 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   ok = ok && gbattn::launch_rope_table(cs, sn, S, D, static_cast<double>(rope_theta), stream) ==
                  cudaSuccess;
   gbattn::RowPrepParams rp{};
-  rp.mode = gbattn::kPrepFwd;
+  rp.bwd = 0;
   rp.S = S;
   rp.D = D;
   rp.cos_tab = cs;
   rp.sin_tab = sn;
-  rp.x = q; rp.y = qr; rp.rows = qrows;
-  ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
-  rp.x = k; rp.y = kr; rp.rows = krows;
+  rp.seg[0] = {q, qr, nullptr, nullptr, qrows};
+  rp.seg[1] = {k, kr, nullptr, nullptr, krows};
   ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
   gbattn::FwdParams fp{};
   ok = ok && map_bf16(&fp.map_q, qr, qrows, D) && map_bf16(&fp.map_k, kr, krows, D) &&

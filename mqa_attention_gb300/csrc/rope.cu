@@ -80,52 +80,75 @@ __device__ __forceinline__ void store8_bf16_scaled_f16(void* p, const float (&o)
   *reinterpret_cast<Vec8x16*>(p) = x;
 }
 
+// Largest |x| of bf16 tensors. For a non-negative bf16 value the bit pattern
+// orders like the value, so the maximum is taken on the 15-bit magnitudes of
+// packed pairs (__vmaxu2) and converted back to float once per thread.
 __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
-  __shared__ float red[8];
+  __shared__ uint32_t red[4][8];
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  uint32_t m[4] = {0u, 0u, 0u, 0u};
 #pragma unroll 1
   for (int t = 0; t < 4; ++t) {
     if (p.x[t] == nullptr) continue;
+    const uint4* src = static_cast<const uint4*>(p.x[t]);
     const long long chunks = p.n[t] / 8;
-    float m = 0.f;
-    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
-         c += (long long)gridDim.x * blockDim.x) {
-      float v[8];
-      load8_bf16(static_cast<const __nv_bfloat16*>(p.x[t]) + c * 8, v);
+    uint32_t acc = 0u;
+    long long c = t0;
+    for (; c + 3 * stride < chunks; c += 4 * stride) {
+      const uint4 a = __ldg(src + c), b = __ldg(src + c + stride);
+      const uint4 d = __ldg(src + c + 2 * stride), g = __ldg(src + c + 3 * stride);
+      const uint4 v[4] = {a, b, d, g};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+      for (int i = 0; i < 4; ++i)
+        acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu),
+                                     __vmaxu2(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu)));
     }
+    for (; c < chunks; c += stride) {
+      const uint4 a = __ldg(src + c);
+      acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(a.x & 0x7fff7fffu, a.y & 0x7fff7fffu),
+                                   __vmaxu2(a.z & 0x7fff7fffu, a.w & 0x7fff7fffu)));
+    }
+    m[t] = max(acc & 0xffffu, acc >> 16);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float b = 0.f;
-      for (int w = 0; w < 8; ++w) b = fmaxf(b, red[w]);
-      // non-negative floats order like their bit patterns
-      atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), __float_as_uint(b));
-    }
-    __syncthreads();
+  for (int t = 0; t < 4; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[t] = max(m[t], __shfl_xor_sync(0xffffffffu, m[t], o));
+    if ((threadIdx.x & 31) == 0) red[t][threadIdx.x >> 5] = m[t];
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    const int t = threadIdx.x;
+    uint32_t b = 0u;
+    for (int w = 0; w < 8; ++w) b = max(b, red[t][w]);
+    // bf16 magnitude bits -> float bits; non-negative floats order like their bits
+    if (p.x[t] != nullptr) atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), b << 16);
   }
 }
 
 // One thread per (row, c) with c < D/16: elements [8c, 8c+8) and [D/2+8c, D/2+8c+8).
-template <int D, int kMode>
+// Rows [0, seg[0].rows) are query rows, the next seg[1].rows are key rows.
+template <int D, bool kBwd>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long row = t / T;
+  const long long grow = t / T;
   const int c = static_cast<int>(t % T);
-  // Threads past the last row read row 0 (a valid address), take part in the
-  // shuffles below and write nothing.
-  const bool live = row < p.rows;
-  const long long r = live ? row : 0;
+  const bool is_q = grow < p.seg[0].rows;
+  const RowSegment& sg = is_q ? p.seg[0] : p.seg[1];
+  const long long row0 = is_q ? grow : grow - p.seg[0].rows;
+  // Threads past the last row read row 0 of the segment (a valid address), take
+  // part in the shuffles below and write nothing.
+  const bool live = row0 < sg.rows;
+  const long long r = live ? row0 : 0;
   const int pos = static_cast<int>(r % p.S);
   const long long e1 = r * D + 8 * c;
   const long long e2 = e1 + H;
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
-  load8_bf16(static_cast<const __nv_bfloat16*>(p.x) + e1, x1);
-  load8_bf16(static_cast<const __nv_bfloat16*>(p.x) + e2, x2);
+  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e1, x1);
+  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
   load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
   load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
 #pragma unroll
@@ -133,43 +156,52 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
     y1[i] = x1[i] * cs[i] - x2[i] * sn[i];
     y2[i] = x2[i] * cs[i] + x1[i] * sn[i];
   }
-  if constexpr (kMode == kPrepFwd) {
+  if constexpr (!kBwd) {
     if (live) {
-      store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e1, y1);
-      store8_bf16(static_cast<__nv_bfloat16*>(p.y) + e2, y2);
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + e1, y1);
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + e2, y2);
     }
   } else {
     const BwdExponents ex = bwd_exponents(p.maxes);
-    const float s_rot = exp2i(kMode == kPrepBwdQ ? ex.q : ex.k);
-    const float s_x2 = exp2i(kMode == kPrepBwdQ ? ex.dout : ex.v);
+    const float s_rot = exp2i(is_q ? ex.q : ex.k);
+    const float s_x2 = exp2i(is_q ? ex.dout : ex.v);
     float a1[8], a2[8];
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.x2) + e1, a1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.x2) + e2, a2);
+    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
     if (live) {
-      store8_bf16_scaled_f16(static_cast<__half*>(p.y) + e1, y1, s_rot);
-      store8_bf16_scaled_f16(static_cast<__half*>(p.y) + e2, y2, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + e1, y1, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + e2, y2, s_rot);
       // x2 is already bf16: scaling by a power of two and storing fp16 is exact
-      store8_bf16_scaled_f16(static_cast<__half*>(p.y2) + e1, a1, s_x2);
-      store8_bf16_scaled_f16(static_cast<__half*>(p.y2) + e2, a2, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + e1, a1, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + e2, a2, s_x2);
     }
-    if constexpr (kMode == kPrepBwdQ) {
-      float o1[8], o2[8];
-      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e1, o1);
-      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e2, o2);
-      float dot = 0.f;
+    // delta for query rows. Every thread computes it and takes part in the
+    // shuffle (a warp may straddle the query/key boundary); key rows read an
+    // in-bounds row of `out` (there are no more key rows than query rows) and
+    // write nothing.
+    float o1[8], o2[8];
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e1, o1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e2, o2);
+    float dot = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
+    for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
 #pragma unroll
-      for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      if (live) {
-        if (c == 0) {
-          p.delta[r] = dot * exp2i(ex.dout + ex.v);
-          p.lse2[r] = p.lse[r] * kLog2e;
-        }
-        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        store8(p.dqacc + e1, z);
-        store8(p.dqacc + e2, z);
+    for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (!is_q && live && p.dk_zero != nullptr) {
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      store8(p.dk_zero + e1, z);
+      store8(p.dk_zero + e2, z);
+      store8(p.dv_zero + e1, z);
+      store8(p.dv_zero + e2, z);
+    }
+    if (is_q && live) {
+      if (c == 0) {
+        p.delta[r] = dot * exp2i(ex.dout + ex.v);
+        p.lse2[r] = p.lse[r] * kLog2e;
       }
+      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      store8(p.dqacc + e1, z);
+      store8(p.dqacc + e2, z);
     }
   }
 }
@@ -207,15 +239,6 @@ __global__ void __launch_bounds__(256)
 
 long long blocks_for(long long threads) { return (threads + 255) / 256; }
 
-template <int D>
-void launch_prep_d(const RowPrepParams& p, unsigned grid, cudaStream_t stream) {
-  switch (p.mode) {
-    case kPrepFwd: row_prep_kernel<D, kPrepFwd><<<grid, 256, 0, stream>>>(p); break;
-    case kPrepBwdQ: row_prep_kernel<D, kPrepBwdQ><<<grid, 256, 0, stream>>>(p); break;
-    default: row_prep_kernel<D, kPrepBwdK><<<grid, 256, 0, stream>>>(p); break;
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
@@ -226,20 +249,20 @@ cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, doub
 }
 
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
-  long long most = 0;
-  for (int t = 0; t < 4; ++t) most = p.n[t] > most ? p.n[t] : most;
-  long long blocks = blocks_for(most / 8);
-  if (blocks > 4 * 152 * 8) blocks = 4 * 152 * 8;  // grid-stride beyond a few waves
-  if (blocks < 1) blocks = 1;
-  absmax_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+  absmax_kernel<<<152 * 8, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
-  const long long threads = p.rows * (p.D / 16);
+  const long long threads = (p.seg[0].rows + p.seg[1].rows) * (p.D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
-  if (p.D == 128) launch_prep_d<128>(p, grid, stream);
-  else launch_prep_d<64>(p, grid, stream);
+  if (p.D == 128) {
+    if (p.bwd) row_prep_kernel<128, true><<<grid, 256, 0, stream>>>(p);
+    else row_prep_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+  } else {
+    if (p.bwd) row_prep_kernel<64, true><<<grid, 256, 0, stream>>>(p);
+    else row_prep_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
