@@ -317,7 +317,8 @@ def run_ours(args, rank, world, local):
         n, tot = M.profile_query(kind)
         if n:
             kern[name] = {"launches": n, "avg_ms": tot / n}
-    launches_per_step = 2 + 1 + ((2 + 1 + 1) if wl.backward else 0)
+    # our kernels per step: RoPE pre-pass + forward; abs-max + pre-pass + main + dq finalisation
+    launches_per_step = 2 + (4 if wl.backward else 0)
 
     # ---- end to end through host buffers
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))

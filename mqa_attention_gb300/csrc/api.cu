@@ -302,8 +302,14 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   float* maxes = reinterpret_cast<float*>(w);
 
   // Two CTAs per (KV head, key tile), each with half of the group's query heads,
-  // when the group splits evenly.
-  const int hsplit = (Hq / Hkv) % 2 == 0 ? 2 : 1;
+  // when one CTA per key tile would not fill the GPU (and the group splits
+  // evenly); otherwise one CTA per key tile, with no dK/dV zeroing.
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const long long key_tiles = static_cast<long long>(B) * Hkv * (S / kTile);
+  const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
   bool ok = true;
   {
     LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);

@@ -482,10 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 // no longer serialised behind the score MMAs. TMEM (512 columns):
 //   buffer b in {0,1}: Sᵀ_b [128b, 128b+64), dPᵀ_b [128b+64, 128b+128)
 //   dV [256, 384), dK [384, 512)
-// Pᵀ of a step is written back over that step's Sᵀ columns (each softmax half
-// inside its own 32 columns: half h packs into [128b+32h, 128b+32h+16)), and the
-// step's dQᵀ partial is accumulated over its dPᵀ columns, both after the softmax
-// has read them.
+// Pᵀ and dSᵀ of a step are written back over that step's Sᵀ columns as packed
+// fp16 (each softmax half inside its own 32 columns: half h puts Pᵀ at
+// [128b+32h, +16) and dSᵀ at [128b+32h+16, +16)), and the step's dQᵀ partial
+// is accumulated over its dPᵀ columns, all after the softmax has read them.
+// dV and dK then take Pᵀ and dSᵀ from TMEM (TS MMAs); dSᵀ also goes to shared
+// memory, where the dQᵀ MMA reads it as its B operand.
 struct DbCfg {
   static constexpr int D = 128;
   static constexpr int BQ = 64;
@@ -660,11 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < BQ / 16; ++kk)  // queries 16kk.. sit at (kk/2)*32 + (kk%2)*8
         mma_ts_w(tmem + C::kColDV, pt + (kk >> 1) * 32 + (kk & 1) * 8,
                  desc(kMnQ, doaddr + kk * 2048), idesc_acc, (!first || kk > 0) ? 1u : 0u);
-      const uint32_t dsaddr = ds_addr(s);
 #pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk)
-        mma_ss_w(tmem + C::kColDK, desc(kKmaj, dsaddr + kk * 32), desc(kMnQ, qaddr + kk * 2048),
-                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < BQ / 16; ++kk)  // dSᵀ sits 16 columns after Pᵀ
+        mma_ts_w(tmem + C::kColDK, pt + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
+                 desc(kMnQ, qaddr + kk * 2048), idesc_acc, (!first || kk > 0) ? 1u : 0u);
     };
     auto issue_dq = [&](int s) {  // dQᵀ [D x BQ] = K~ᵀ dSᵀ over the step's dPᵀ columns
       const uint32_t dsaddr = ds_addr(s);
@@ -777,8 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dk[2 * g] = pack_fp16(dsv[0], dsv[1]);
         dk[2 * g + 1] = pack_fp16(dsv[2], dsv[3]);
       }
-      // Pᵀ over this half's own (already read) Sᵀ columns
-      tmem_st16(tmem + lane_base + C::col_st(buf) + qb, pk);
+      // Pᵀ and dSᵀ over this half's own (already read) Sᵀ columns
+      tmem_st32(tmem + lane_base + C::col_st(buf) + qb, pk, dk);
       // dSᵀ row r, query columns qb..qb+31 (chunks 4*half ..), swizzled K-major
       const uint32_t dsb = ds_addr(s);
 #pragma unroll

@@ -268,6 +268,20 @@ GB_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Stores two 16-column halves (lo then hi) into 32 consecutive columns.
+GB_DEV void tmem_st32(uint32_t taddr, const uint32_t (&lo)[16], const uint32_t (&hi)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]), "r"(lo[6]),
+      "r"(lo[7]), "r"(lo[8]), "r"(lo[9]), "r"(lo[10]), "r"(lo[11]), "r"(lo[12]), "r"(lo[13]),
+      "r"(lo[14]), "r"(lo[15]), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]),
+      "r"(hi[5]), "r"(hi[6]), "r"(hi[7]), "r"(hi[8]), "r"(hi[9]), "r"(hi[10]), "r"(hi[11]),
+      "r"(hi[12]), "r"(hi[13]), "r"(hi[14]), "r"(hi[15])
+      : "memory");
+}
 // Stores 16 consecutive columns of this thread's lane.
 GB_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
