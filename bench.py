@@ -40,6 +40,8 @@ from mqa_attention_gb300 import inputs as I  # noqa: E402
 from mqa_attention_gb300.workloads import WORKLOADS, by_name  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama3_8b_gqa_s4096"
+METRIC = ("causal GQA attn fwd+bwd TFLOP/s (Llama-3-8B S=4096 shape), % of GB300 bf16 peak in "
+          "roofline")
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -233,7 +235,7 @@ def run_reference(args, rank, world):
     unit = "TFLOP/s"
     line = {
         "impl": "reference",
-        "metric": "causal GQA attn fwd+bwd TFLOP/s (fp64 CPU oracle)",
+        "metric": METRIC,
         "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -383,8 +385,7 @@ def run_ours(args, rank, world, local):
                "sample": f"{heads} of {wl.B * wl.Hq} query heads, full S={wl.S}, "
                          f"fwd{'+bwd' if wl.backward else ''} in fp64 ({secs:.1f} s)"}
     line = {
-        "metric": "causal GQA attn fwd+bwd TFLOP/s (Llama-3-8B S=4096 shape), % of GB300 bf16 "
-                  "peak in roofline",
+        "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",

@@ -45,7 +45,7 @@ struct FwdCfg {
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 B (64 bf16)
   static constexpr int kRegions = D / 64;
   static constexpr int kTileBytes = kRegions * kRegionBytes;
-  static constexpr int kSlots = D == 128 ? 4 : 6;      // K/V ring depth (tiles)
+  static constexpr int kSlots = D == 128 ? 5 : 10;     // K/V ring depth (tiles)
   static constexpr int kKvOff = 2 * kTileBytes;        // after Q_0, Q_1
   static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
   __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
@@ -255,11 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tc_fence_after();
       float s[128];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tS + cc * 32, u);
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t u[32], w[32];
+        tmem_ld32x2(tS + cc * 64, tS + cc * 64 + 32, u, w);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[cc * 64 + i] = __uint_as_float(u[i]);
+          s[cc * 64 + 32 + i] = __uint_as_float(w[i]);
+        }
       }
       if (p.causal && j == qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
