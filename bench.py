@@ -93,6 +93,25 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when
+    the record is for another workload or the kernel source changed since."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if rec["workload"] != workload or h.hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+        return float(rec["bytes"])
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -375,7 +394,8 @@ def run_ours(args, rank, world, local):
     if dom[0] in algo_flops:
         achieved = algo_flops[dom[0]] / (dom[1]["avg_ms"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                "traffic": ncu_traffic(dom[0], wl.name),
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "step_frac_of_peak": value / world / peak_tf}
     cpu = None
