@@ -13,30 +13,35 @@
 // query head of the group.
 //
 // GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
-// shared memory and walks the (query head, query tile) steps that see its keys
-// (only tiles on or below the diagonal when causal). When the group has an even
-// number of query heads, two CTAs share a key tile, each taking half of the
-// heads, and add their dK/dV partials into zeroed outputs: the heaviest
-// (first) key tiles then no longer outlast the average SM's load. Per step s, in TMEM:
-//   Sᵀ  = K~ Q~ᵀ      [128 keys x BQ]    (SS MMA)
-//   dPᵀ = V dOᵀ       [128 keys x BQ]    (SS MMA)
-//   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta);
-//                  Pᵀ to its own TMEM buffer, dSᵀ to a shared-memory buffer
-//   dV += Pᵀ dO       (TS MMA, A from TMEM)
-//   dK += dSᵀ Q~      (SS MMA)
-//   dQ partial = dS K~ (D = 64: [BQ x D]) or its transpose K~ᵀ dSᵀ (D = 128:
-//                [D x BQ]), drained by its own warps with fp32 global reductions.
-// The MMA warp issues Sᵀ/dPᵀ of step s+1 before dV/dK/dQ of step s, so the
-// softmax of step s+1 overlaps three MMAs of step s. Pᵀ and dSᵀ buffers are
-// double-buffered where TMEM allows (D = 128); with D = 64 one Pᵀ buffer fits
-// and the softmax holds its results in registers until step s-1 is consumed.
+// shared memory and walks the (query head, 64-query tile) steps that see its
+// keys (only tiles on or below the diagonal when causal). When one CTA per key
+// tile would not fill the GPU and the group has an even number of query heads,
+// two CTAs share a key tile, each taking half of the heads, and add their dK/dV
+// partials into zeroed outputs.
+//
+// Per step s (buffer b = s & 1), in TMEM:
+//   Sᵀ_b  = K~ Q~ᵀ  [128 keys x 64 queries]   (SS MMA)
+//   dPᵀ_b = V dOᵀ   [128 keys x 64 queries]   (SS MMA)
+//   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta), packed as
+//     fp16 back over the step's own Sᵀ columns (softmax half h: Pᵀ at
+//     [128b+32h, +16), dSᵀ at [128b+32h+16, +16)); dSᵀ also to shared memory
+//   dV += Pᵀ dO, dK += dSᵀ Q~                 (TS MMAs, A from TMEM)
+//   D = 128: dQᵀ = K~ᵀ dSᵀ [128 d x 64 queries] over the step's dPᵀ columns;
+//   D = 64:  dQ = dS K~ [128 queries x 64 d] once per pair of steps (the two
+//            64-query tiles of one head that follow each other), in its own
+//            64 columns, A taken from the pair's two adjacent dSᵀ buffers.
+// The dQ drain warps add the partials into an fp32 buffer with global
+// reductions. Two (Sᵀ, dPᵀ) buffers let the score MMAs of step s+2 run while
+// the softmax of step s+1 works.
+// TMEM columns: Sᵀ_0 [0,64) dPᵀ_0 [64,128) Sᵀ_1 [128,192) dPᵀ_1 [192,256), then
+//   D = 128: dV [256,384) dK [384,512);  D = 64: dQ [256,320) dV [320,384) dK [384,448).
 // All products run in fp16 (kind::f16 with fp16 A and B): the operands q~, k~,
 // v, dO arrive from the pre-pass multiplied by exact powers of two (q~ and k~
 // hold their bf16-rounded values, so the recomputed scores equal the
 // forward's), and Pᵀ, dSᵀ are rounded to fp16 (2^-11) instead of bf16 (2^-9);
 // the scales are undone in the epilogues.
-// Warp roles: 0-7 softmax (two column halves), 8-11 dQ drain, 12 TMA producer,
-// 13 MMA issuer and TMEM owner.
+// Warp roles: 0-7 softmax (two 32-query halves), 8-11 dQ drain, 12 TMA
+// producer, 13 MMA issuer (whole warp, one elected lane issues) and TMEM owner.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -51,37 +56,33 @@ constexpr int kWarpMma = 13;
 
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
-  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteConsumed = 26
+  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25
 };
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BQ = D == 128 ? 64 : 128;  // query rows per step
-  static constexpr bool kDqT = D == 128;          // dQ computed transposed ([D x BQ])
-  static constexpr int kNPT = D == 128 ? 2 : 1;   // Pᵀ TMEM buffers
-  static constexpr int kRegions = D / 64;
+  static constexpr int BQ = 64;                    // query rows per step
+  static constexpr bool kDqPair = D == 64;         // dQ once per pair of steps
+  static constexpr int kRegions = D / 64;          // 64-column swizzle regions per row
   static constexpr int kKRegionBytes = 128 * 128;  // 128 key rows x 128 B
-  static constexpr int kQRegionBytes = BQ * 128;   // BQ query rows x 128 B
+  static constexpr int kQRegionBytes = BQ * 128;   // 64 query rows x 128 B
   static constexpr int kKTileBytes = kRegions * kKRegionBytes;
   static constexpr int kQTileBytes = kRegions * kQRegionBytes;
   static constexpr int kStages = 3;
   static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
-  static constexpr int kDsRegions = BQ / 64;
-  static constexpr int kDsBytes = kDsRegions * 16384;  // dSᵀ: 128 key rows x BQ fp16
+  static constexpr int kDsBufs = kDqPair ? 4 : 2;  // dSᵀ buffers (pairs stay adjacent)
+  static constexpr int kDsBytes = 16384;           // dSᵀ: 128 key rows x 64 queries fp16
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKTileBytes;
   static constexpr int kStageOff = 2 * kKTileBytes;
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kSmemBytes = kDsOff + 2 * kDsBytes + 1024;
-  // TMEM columns
-  static constexpr uint32_t kColST = 0;
-  static constexpr uint32_t kColDPT = BQ;
-  static constexpr uint32_t kColPT = 2 * BQ;  // kNPT buffers of BQ/2 packed columns
-  __device__ static constexpr uint32_t col_pt(int buf) { return kColPT + buf * (BQ / 2); }
-  static constexpr uint32_t kColDQ = kColPT + kNPT * (BQ / 2);
-  static constexpr uint32_t kColDV = kColDQ + 64;
-  static constexpr uint32_t kColDK = kColDV + D;
-  static_assert(kColDK + D == 512, "TMEM budget");
+  static constexpr int kSmemBytes = kDsOff + kDsBufs * kDsBytes + 1024;
+  __device__ static constexpr uint32_t col_st(int buf) { return buf ? 128u : 0u; }
+  __device__ static constexpr uint32_t col_dpt(int buf) { return buf ? 192u : 64u; }
+  static constexpr uint32_t kColDQ = 256;  // D = 64 only
+  static constexpr uint32_t kColDV = kDqPair ? 320 : 256;
+  static constexpr uint32_t kColDK = 384;
+  static_assert(kColDK + D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -104,9 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_kv, bar_s_full, bar_ds_full, bar_done, bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never;
   __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_consumed[2], bar_dq_full, bar_dq_free;
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -132,10 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const int kv_row = bhk * p.S + k0;
   const int nqt = p.S / BQ;
   const int qt_begin = p.causal ? k0 / BQ : 0;
-  const int per_head = nqt - qt_begin;
+  const int per_head = nqt - qt_begin;  // even: S and k0 are multiples of 128
   const int n = Gc * per_head;
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
-  // step s -> (query head, query tile)
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
     const int h = h_first + s / per_head;
@@ -150,18 +150,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_kv), 1);
-    mbar_init(smem_u32(&bar_s_full), 1);
-    mbar_init(smem_u32(&bar_ds_full), 256);
     mbar_init(smem_u32(&bar_done), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     mbar_init(smem_u32(&bar_never), 1);
-    mbar_init(smem_u32(&bar_dq_full), 1);
-    mbar_init(smem_u32(&bar_dq_free), 128);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_stage_full[s]), 1);
       mbar_init(smem_u32(&bar_stage_empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bar_consumed[i]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_s_full[i]), 1);
+      mbar_init(smem_u32(&bar_ds_full[i]), 256);
+      mbar_init(smem_u32(&bar_dq_full[i]), 1);
+      mbar_init(smem_u32(&bar_dq_free[i]), 128);
+    }
     fence_mbar_init();
   }
   tc_fence_before();
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
   auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
-  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s & 1) * C::kDsBytes; };
+  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s % C::kDsBufs) * C::kDsBytes; };
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
@@ -209,424 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
-    // ================================================================ MMA issuer
-    // The whole warp runs this loop with warp-uniform operands; elect.sync inside
-    // the MMA / commit wrappers lets one lane issue.
-    constexpr uint32_t idesc_st = idesc_fp16(128, BQ, 0, 0);
-    constexpr uint32_t idesc_acc = idesc_fp16(128, D, 0, 1);
-    constexpr uint32_t idesc_dq = C::kDqT ? idesc_fp16(128, BQ, 1, 1) : idesc_fp16(128, D, 1, 1);
-    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);                   // K-major operand
-    constexpr uint64_t kMnQ = sdesc_hi(C::kQRegionBytes, 1024);      // MN-major, BQ-row tiles
-    constexpr uint64_t kMnK = sdesc_hi(C::kKRegionBytes, 1024);      // MN-major, 128-row tiles
-    constexpr uint64_t kMnDs = sdesc_hi(16384, 1024);                // MN-major dSᵀ
-    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
-    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
-      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
-    };
-    const uint32_t kaddr = sbase + C::kKOff;
-    const uint32_t vaddr = sbase + C::kVOff;
-
-    auto issue_st = [&](int s) {
-      const uint32_t qaddr = stage_addr(s);
-      const uint32_t doaddr = qaddr + C::kQTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
-        const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
-        mma_ss_w(tmem + C::kColST, desc(kKmaj, kaddr + ok_), desc(kKmaj, qaddr + oq), idesc_st,
-                 kk > 0);
-        mma_ss_w(tmem + C::kColDPT, desc(kKmaj, vaddr + ok_), desc(kKmaj, doaddr + oq), idesc_st,
-                 kk > 0);
-      }
-    };
-    auto issue_dvdk = [&](int s, bool first) {
-      const uint32_t qaddr = stage_addr(s);
-      const uint32_t doaddr = qaddr + C::kQTileBytes;
-      const uint32_t pt = tmem + C::col_pt(s % C::kNPT);
-      const uint32_t dsaddr = ds_addr(s);
-#pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk)
-        mma_ts_w(tmem + C::kColDV, pt + kk * 8, desc(kMnQ, doaddr + kk * 2048), idesc_acc,
-                 (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < BQ / 16; ++kk) {
-        const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_ss_w(tmem + C::kColDK, desc(kKmaj, dsaddr + oa), desc(kMnQ, qaddr + kk * 2048),
-                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
-      }
-    };
-    auto issue_dq = [&](int s) {
-      const uint32_t dsaddr = ds_addr(s);
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        if constexpr (C::kDqT) {
-          // dQᵀ [D x BQ] = K~ᵀ (MN-major A) x dSᵀ (MN-major B), K = keys
-          mma_ss_w(tmem + C::kColDQ, desc(kMnK, kaddr + kk * 2048), desc(kMnDs, dsaddr + kk * 2048),
-                   idesc_dq, kk > 0);
-        } else {
-          // dQ [BQ x D] = dS (MN-major A, from dSᵀ) x K~ (MN-major B), K = keys
-          mma_ss_w(tmem + C::kColDQ, desc(kMnDs, dsaddr + kk * 2048), desc(kMnK, kaddr + kk * 2048),
-                   idesc_dq, kk > 0);
-        }
-      }
-    };
-
-    bool ok = true;
-    if (p.inject_timeout)  // nothing ever arrives on bar_never
-      ok = wait(smem_u32(&bar_never), 0, kSiteInject);
-    ok = ok && wait(smem_u32(&bar_kv), 0, kSiteKv);
-    ok = ok && wait(smem_u32(&bar_stage_full[0]), 0, kSiteStageFull);
-    if (ok) {
-      tc_fence_after();
-      issue_st(0);
-      mma_commit_w(smem_u32(&bar_s_full));
-    }
-    for (int s = 0; s < n && ok; ++s) {
-      ok = wait(smem_u32(&bar_ds_full), s & 1, kSiteDsFull);
-      if (!ok) break;
-      tc_fence_after();
-      if (s + 1 < n) {
-        // Sᵀ/dPᵀ of the next step first: the softmax warps have already read
-        // this step's, and the next softmax then overlaps dV/dK/dQ below.
-        ok = wait(smem_u32(&bar_stage_full[(s + 1) % C::kStages]), ((s + 1) / C::kStages) & 1,
-                  kSiteStageFull);
-        if (!ok) break;
-        issue_st(s + 1);
-        mma_commit_w(smem_u32(&bar_s_full));
-      }
-      issue_dvdk(s, s == 0);
-      mma_commit_w(smem_u32(&bar_stage_empty[s % C::kStages]));
-      ok = wait(smem_u32(&bar_dq_free), (s & 1) ^ 1, kSiteDqFree);
-      if (!ok) break;
-      tc_fence_after();
-      issue_dq(s);
-      mma_commit_w(smem_u32(&bar_dq_full));
-      mma_commit_w(smem_u32(&bar_consumed[s & 1]));
-    }
-    if (ok) mma_commit_w(smem_u32(&bar_done));
-    // Every MMA issued above completes before the tensor memory is released.
-    mma_commit_w(smem_u32(&bar_drain));
-    drain_wait(smem_u32(&bar_drain), 0);
-    __syncwarp();
-  } else if (warp >= 8) {
-    // ================================================================ dQ drain
-    const int r = tid & 127;  // TMEM lane: d (D = 128) or query row (D = 64)
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int s = 0; s < n; ++s) {
-      const bool got =
-          bounded_wait(smem_u32(&bar_dq_full), s & 1, abort_ptr, p.status, kSiteDqFull);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after();
-      uint32_t u0[32], u1[32];
-      tmem_ld32(tmem + lane_base + C::kColDQ, u0);
-      tmem_ld32(tmem + lane_base + C::kColDQ + 32, u1);
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dq_free));
-      const long long row0 = step_row(s);
-      if constexpr (C::kDqT) {
-        // lane r = d; columns = the BQ = 64 query rows of the step
-        float* base = p.dqacc + row0 * D + r;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
-      } else {
-        // lane r = query row; columns = d
-        float* base = p.dqacc + (row0 + r) * D;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          red_add_v4_f32(base + 4 * i, __uint_as_float(u0[4 * i]), __uint_as_float(u0[4 * i + 1]),
-                         __uint_as_float(u0[4 * i + 2]), __uint_as_float(u0[4 * i + 3]));
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          red_add_v4_f32(base + 32 + 4 * i, __uint_as_float(u1[4 * i]),
-                         __uint_as_float(u1[4 * i + 1]), __uint_as_float(u1[4 * i + 2]),
-                         __uint_as_float(u1[4 * i + 3]));
-      }
-    }
-  } else {
-    // ================================================================ softmax
-    constexpr int HC = BQ / 2;  // query columns of this half
-    constexpr int NCH = HC / 32;
-    const int half = warp >> 2;
-    const int r = tid & 127;  // key row in the tile == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // Sᵀ arrives multiplied by 2^(eq+ek), dPᵀ and delta by 2^(edo+ev)
-    const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
-    const int key = k0 + r;
-    for (int s = 0; s < n; ++s) {
-      const bool got = bounded_wait(smem_u32(&bar_s_full), s & 1, abort_ptr, p.status, kSiteSFull);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after();
-      const uint32_t st = stage_addr(s);
-      const float* lse2 = reinterpret_cast<const float*>(sgen + (st - sbase) + 2 * C::kQTileBytes);
-      const float* delta = lse2 + BQ;
-      const int q0 = step_qt(s) * BQ;
-      const bool mask = p.causal && q0 < k0 + kTile;
-      uint32_t pk[NCH][16], dk[NCH][16];
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        const int qb = half * HC + ch * 32;  // first query column of this chunk
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tmem + lane_base + C::kColST + qb, sv);
-        tmem_ld32(tmem + lane_base + C::kColDPT + qb, dpv);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pr[2], dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = qb + 2 * i + e;
-            float pv = ex2(fmaf(__uint_as_float(sv[2 * i + e]), sl2, -lse2[q]));
-            if (mask && key > q0 + q) pv = 0.f;
-            pr[e] = pv;
-            dsv[e] = pv * (__uint_as_float(dpv[2 * i + e]) - delta[q]);
-          }
-          pk[ch][i] = pack_fp16(pr[0], pr[1]);
-          dk[ch][i] = pack_fp16(dsv[0], dsv[1]);
-        }
-      }
-      // The Pᵀ / dSᵀ buffers of this step were last read by step s - kNPT
-      // (dSᵀ: s - 2); wait until that step's MMAs are done.
-      if (s >= C::kNPT) {
-        const int prev = s - C::kNPT;
-        const bool free_ok = bounded_wait(smem_u32(&bar_consumed[prev & 1]), (prev >> 1) & 1,
-                                          abort_ptr, p.status, kSiteConsumed);
-        if (!__all_sync(0xffffffffu, free_ok)) break;
-        tc_fence_after();
-      }
-      const uint32_t pt = tmem + lane_base + C::col_pt(s % C::kNPT);
-      const uint32_t dsb = ds_addr(s);
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        const int qb = half * HC + ch * 32;
-        // Pᵀ row r, queries qb..qb+31 -> packed columns qb/2 ..
-        tmem_st16(pt + qb / 2, pk[ch]);
-        // dSᵀ row r, query columns qb..qb+31, 128-byte-swizzled K-major layout
-        const uint32_t region = dsb + (qb / 64) * 16384;
-        const uint32_t c0 = (qb % 64) / 8;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(region + sw128_offset(r, c0 + q4), dk[ch][4 * q4], dk[ch][4 * q4 + 1],
-                       dk[ch][4 * q4 + 2], dk[ch][4 * q4 + 3]);
-      }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_ds_full));
-    }
-    // ------------------------------------------------------------ dK / dV epilogue
-    bounded_wait(smem_u32(&bar_done), 0, abort_ptr, p.status, kSiteDone);
-    __syncwarp();
-    tc_fence_after();
-    const long long grow = kv_row + r;
-    const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
-    if (half == 0) {
-      // dV accumulated Pᵀ (dO 2^edo)
-      const float f = exp2i(-ex.dout);
-      float* dst = p.dv + grow * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          put4(dst + cc * 32 + 4 * i, f * __uint_as_float(u[4 * i]),
-               f * __uint_as_float(u[4 * i + 1]), f * __uint_as_float(u[4 * i + 2]),
-               f * __uint_as_float(u[4 * i + 3]), sum_parts);
-      }
-    } else {
-      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2); dK
-      // accumulated (dS 2^(edo+ev)) (q~ 2^eq)
-      const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
-      float* dst = p.dk + grow * D;
-      const float* cs = p.cos_tab + (long long)key * (D / 2);
-      const float* sn = p.sin_tab + (long long)key * (D / 2);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 64; ++ch) {
-        uint32_t x1[32], x2[32];
-        tmem_ld32(tmem + lane_base + C::kColDK + ch * 32, x1);
-        tmem_ld32(tmem + lane_base + C::kColDK + D / 2 + ch * 32, x2);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
-          const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
-          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-          const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-          float y1[4], y2[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = __uint_as_float(x1[4 * i + e]);
-            const float bb = __uint_as_float(x2[4 * i + e]);
-            y1[e] = f * (a * cc[e] + bb * ss[e]);
-            y2[e] = f * (bb * cc[e] - a * ss[e]);
-          }
-          put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
-          put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// D = 128: double-buffered variant. Two (Sᵀ, dPᵀ) accumulator buffers let the
-// MMAs of step s+2 run while the softmax of step s+1 works, so the softmax is
-// no longer serialised behind the score MMAs. TMEM (512 columns):
-//   buffer b in {0,1}: Sᵀ_b [128b, 128b+64), dPᵀ_b [128b+64, 128b+128)
-//   dV [256, 384), dK [384, 512)
-// Pᵀ and dSᵀ of a step are written back over that step's Sᵀ columns as packed
-// fp16 (each softmax half inside its own 32 columns: half h puts Pᵀ at
-// [128b+32h, +16) and dSᵀ at [128b+32h+16, +16)), and the step's dQᵀ partial
-// is accumulated over its dPᵀ columns, all after the softmax has read them.
-// dV and dK then take Pᵀ and dSᵀ from TMEM (TS MMAs); dSᵀ also goes to shared
-// memory, where the dQᵀ MMA reads it as its B operand.
-struct DbCfg {
-  static constexpr int D = 128;
-  static constexpr int BQ = 64;
-  static constexpr int kKRegionBytes = 128 * 128;
-  static constexpr int kQRegionBytes = BQ * 128;
-  static constexpr int kKTileBytes = 2 * kKRegionBytes;
-  static constexpr int kQTileBytes = 2 * kQRegionBytes;
-  static constexpr int kStages = 3;
-  static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
-  static constexpr int kDsBytes = 16384;  // dSᵀ: 128 key rows x 64 queries fp16
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKTileBytes;
-  static constexpr int kStageOff = 2 * kKTileBytes;
-  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kSmemBytes = kDsOff + 2 * kDsBytes + 1024;
-  __device__ static constexpr uint32_t col_st(int buf) { return buf ? 128u : 0u; }
-  __device__ static constexpr uint32_t col_dpt(int buf) { return buf ? 192u : 64u; }
-  static constexpr uint32_t kColDV = 256;
-  static constexpr uint32_t kColDK = 384;
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
-
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_db_kernel(const __grid_constant__ BwdParams p) {
-  using C = DbCfg;
-  constexpr int D = C::D;
-  constexpr int BQ = C::BQ;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never;
-  __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
-
-  // ---- work item: key tile kt of KV head (b, hkv), query heads of part `part`
-  // of the group (hsplit parts); heaviest (kt = 0) first
-  const int units = p.B * p.Hkv * p.hsplit;
-  const int kt = static_cast<int>(blockIdx.x) / units;
-  const int unit = static_cast<int>(blockIdx.x) % units;
-  const int bhk = unit / p.hsplit;
-  const int part = unit % p.hsplit;
-  const int b = bhk / p.Hkv;
-  const int hkv = bhk % p.Hkv;
-  const int G = p.Hq / p.Hkv;
-  const int Gc = G / p.hsplit;  // query heads of this CTA
-  const int h_first = hkv * G + part * Gc;
-  const int k0 = kt * kTile;
-  const int kv_row = bhk * p.S + k0;
-  const int nqt = p.S / BQ;
-  const int qt_begin = p.causal ? k0 / BQ : 0;
-  const int per_head = nqt - qt_begin;
-  const int n = Gc * per_head;
-  const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
-  auto step_qt = [&](int s) { return qt_begin + s % per_head; };
-  auto step_row = [&](int s) {
-    const int h = h_first + s / per_head;
-    return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
-  };
-
-  // ---- setup
-  if (warp == kWarpMma) {
-    tmem_alloc(smem_u32(&tmem_slot), 512);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(smem_u32(&bar_kv), 1);
-    mbar_init(smem_u32(&bar_done), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
-    mbar_init(smem_u32(&bar_never), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&bar_stage_full[s]), 1);
-      mbar_init(smem_u32(&bar_stage_empty[s]), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_s_full[i]), 1);
-      mbar_init(smem_u32(&bar_ds_full[i]), 256);
-      mbar_init(smem_u32(&bar_dq_full[i]), 1);
-      mbar_init(smem_u32(&bar_dq_free[i]), 128);
-    }
-    fence_mbar_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-  volatile int* abort_ptr = &abort_flag;
-  auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
-  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s & 1) * C::kDsBytes; };
-
-  if (warp == kWarpLoad) {
-    // ================================================================ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.map_q);
-      tma_prefetch_desc(&p.map_do);
-      const uint32_t kvb = smem_u32(&bar_kv);
-      mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
-      for (int r = 0; r < 2; ++r) {
-        tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
-        tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
-      }
-      int issued = 0;
-      for (int s = 0; s < n; ++s) {
-        const int st = s % C::kStages;
-        if (!bounded_wait(smem_u32(&bar_stage_empty[st]), ((s / C::kStages) & 1) ^ 1, abort_ptr,
-                          p.status, kSiteStageEmpty))
-          break;
-        const uint32_t full = smem_u32(&bar_stage_full[st]);
-        const uint32_t dst = stage_addr(s);
-        const int row = step_row(s);
-        mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
-        for (int r = 0; r < 2; ++r) {
-          tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
-          tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
-        }
-        bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
-        bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
-        ++issued;
-      }
-      drain_wait(kvb, 0);
-      for (int i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i)
-        drain_wait(smem_u32(&bar_stage_full[i % C::kStages]), (i / C::kStages) & 1);
-    }
-    __syncwarp();
-  } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer (whole warp)
     constexpr uint32_t idesc_st = idesc_fp16(128, BQ, 0, 0);
     constexpr uint32_t idesc_acc = idesc_fp16(128, D, 0, 1);
-    constexpr uint32_t idesc_dq = idesc_fp16(128, BQ, 1, 1);
+    constexpr uint32_t idesc_dq = C::kDqPair ? idesc_fp16(128, D, 1, 1) : idesc_fp16(128, BQ, 1, 1);
     constexpr uint64_t kKmaj = sdesc_hi(16, 1024);
     constexpr uint64_t kMnQ = sdesc_hi(C::kQRegionBytes, 1024);
     constexpr uint64_t kMnK = sdesc_hi(C::kKRegionBytes, 1024);
-    constexpr uint64_t kMnDs = sdesc_hi(16384, 1024);
+    constexpr uint64_t kMnDs = sdesc_hi(C::kDsBytes, 1024);
     auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
     auto wait = [&](uint32_t bar, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
@@ -667,12 +258,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts_w(tmem + C::kColDK, pt + (kk >> 1) * 32 + 16 + (kk & 1) * 8,
                  desc(kMnQ, qaddr + kk * 2048), idesc_acc, (!first || kk > 0) ? 1u : 0u);
     };
-    auto issue_dq = [&](int s) {  // dQᵀ [D x BQ] = K~ᵀ dSᵀ over the step's dPᵀ columns
-      const uint32_t dsaddr = ds_addr(s);
+    // D = 128: dQᵀ [D x 64] = K~ᵀ dSᵀ of step s, over the step's dPᵀ columns.
+    // D = 64 : dQ [128 x D] = dS K~ of steps s-1, s (A: the pair's dSᵀ buffers).
+    auto issue_dq = [&](int s) {
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_ss_w(tmem + C::col_dpt(s & 1), desc(kMnK, kaddr + kk * 2048),
-                 desc(kMnDs, dsaddr + kk * 2048), idesc_dq, kk > 0);
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        if constexpr (C::kDqPair) {
+          mma_ss_w(tmem + C::kColDQ, desc(kMnDs, ds_addr(s - 1) + kk * 2048),
+                   desc(kMnK, kaddr + kk * 2048), idesc_dq, kk > 0);
+        } else {
+          mma_ss_w(tmem + C::col_dpt(s & 1), desc(kMnK, kaddr + kk * 2048),
+                   desc(kMnDs, ds_addr(s) + kk * 2048), idesc_dq, kk > 0);
+        }
+      }
     };
 
     bool ok = true;
@@ -694,51 +292,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       issue_dvdk(s, s == 0);
       mma_commit_w(smem_u32(&bar_stage_empty[s % C::kStages]));
-      issue_dq(s);
-      mma_commit_w(smem_u32(&bar_dq_full[buf]));
+      if constexpr (C::kDqPair) {
+        if (s & 1) {
+          const int m = s >> 1;  // pair index; its drain frees the single dQ buffer
+          ok = wait(smem_u32(&bar_dq_free[0]), (m & 1) ^ 1, kSiteDqFree);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dq(s);
+          mma_commit_w(smem_u32(&bar_dq_full[0]));
+        }
+      } else {
+        issue_dq(s);
+        mma_commit_w(smem_u32(&bar_dq_full[buf]));
+      }
       if (s + 2 < n) {
         ok = wait(smem_u32(&bar_stage_full[(s + 2) % C::kStages]), ((s + 2) / C::kStages) & 1,
                   kSiteStageFull);
         if (!ok) break;
         issue_s(s + 2);  // after dV(s) in issue order: Pᵀ(s) is read before it is overwritten
-        ok = wait(smem_u32(&bar_dq_free[buf]), (s >> 1) & 1, kSiteDqFree);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp(s + 2);  // the drain has read dQᵀ(s) from these columns
+        if constexpr (!C::kDqPair) {
+          ok = wait(smem_u32(&bar_dq_free[buf]), (s >> 1) & 1, kSiteDqFree);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_dp(s + 2);  // D = 128: the drain has read dQᵀ(s) from these columns
         mma_commit_w(smem_u32(&bar_s_full[buf]));
       }
     }
     if (ok) mma_commit_w(smem_u32(&bar_done));
+    // Every MMA issued above completes before the tensor memory is released.
     mma_commit_w(smem_u32(&bar_drain));
     drain_wait(smem_u32(&bar_drain), 0);
     __syncwarp();
   } else if (warp >= 8) {
     // ================================================================ dQ drain
-    const int r = tid & 127;  // TMEM lane = d
+    const int r = tid & 127;  // TMEM lane: d (D = 128) or query row of the pair (D = 64)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int s = 0; s < n; ++s) {
-      const int buf = s & 1;
-      const bool got = bounded_wait(smem_u32(&bar_dq_full[buf]), (s >> 1) & 1, abort_ptr, p.status,
-                                    kSiteDqFull);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after();
-      uint32_t u0[32], u1[32];
-      tmem_ld32x2(tmem + lane_base + C::col_dpt(buf), tmem + lane_base + C::col_dpt(buf) + 32, u0,
-                  u1);
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_dq_free[buf]));
-      float* base = p.dqacc + static_cast<long long>(step_row(s)) * D + r;
+    if constexpr (C::kDqPair) {
+      for (int m = 0; m < n / 2; ++m) {
+        const bool got =
+            bounded_wait(smem_u32(&bar_dq_full[0]), m & 1, abort_ptr, p.status, kSiteDqFull);
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after();
+        uint32_t u0[32], u1[32];
+        tmem_ld32x2(tmem + lane_base + C::kColDQ, tmem + lane_base + C::kColDQ + 32, u0, u1);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_dq_free[0]));
+        // query rows of steps 2m, 2m+1 are consecutive rows of one head
+        float* base = p.dqacc + (static_cast<long long>(step_row(2 * m)) + r) * D;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
+        for (int i = 0; i < 8; ++i)
+          red_add_v4_f32(base + 4 * i, __uint_as_float(u0[4 * i]), __uint_as_float(u0[4 * i + 1]),
+                         __uint_as_float(u0[4 * i + 2]), __uint_as_float(u0[4 * i + 3]));
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+        for (int i = 0; i < 8; ++i)
+          red_add_v4_f32(base + 32 + 4 * i, __uint_as_float(u1[4 * i]),
+                         __uint_as_float(u1[4 * i + 1]), __uint_as_float(u1[4 * i + 2]),
+                         __uint_as_float(u1[4 * i + 3]));
+      }
+    } else {
+      for (int s = 0; s < n; ++s) {
+        const int buf = s & 1;
+        const bool got = bounded_wait(smem_u32(&bar_dq_full[buf]), (s >> 1) & 1, abort_ptr,
+                                      p.status, kSiteDqFull);
+        if (!__all_sync(0xffffffffu, got)) break;
+        tc_fence_after();
+        uint32_t u0[32], u1[32];
+        tmem_ld32x2(tmem + lane_base + C::col_dpt(buf), tmem + lane_base + C::col_dpt(buf) + 32,
+                    u0, u1);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_dq_free[buf]));
+        // lane r = d; columns = the 64 query rows of the step
+        float* base = p.dqacc + static_cast<long long>(step_row(s)) * D + r;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+      }
     }
   } else {
     // ================================================================ softmax
     const int half = warp >> 2;
     const int r = tid & 127;  // key row in the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // Sᵀ arrives multiplied by 2^(eq+ek), dPᵀ and delta by 2^(edo+ev)
     const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
     const int key = k0 + r;
     const int qb = half * 32;  // this half's first query column
@@ -778,7 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         dk[2 * g] = pack_fp16(dsv[0], dsv[1]);
         dk[2 * g + 1] = pack_fp16(dsv[2], dsv[3]);
       }
-      // Pᵀ and dSᵀ over this half's own (already read) Sᵀ columns
+      // Pᵀ and dSᵀ over this half's own (already read) Sᵀ columns. The previous
+      // readers of these TMEM columns and of this step's dSᵀ shared-memory buffer
+      // belong to earlier steps whose MMAs were issued before Sᵀ(s), so they had
+      // completed when s_full(s) arrived.
       tmem_st32(tmem + lane_base + C::col_st(buf) + qb, pk, dk);
       // dSᵀ row r, query columns qb..qb+31 (chunks 4*half ..), swizzled K-major
       const uint32_t dsb = ds_addr(s);
@@ -798,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long grow = kv_row + r;
     const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
     if (half == 0) {
+      // dV accumulated Pᵀ (dO 2^edo)
       const float f = exp2i(-ex.dout);
       float* dst = p.dv + grow * D;
 #pragma unroll 1
@@ -811,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                f * __uint_as_float(u[4 * i + 3]), sum_parts);
       }
     } else {
+      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2); dK
+      // accumulated (dS 2^(edo+ev)) (q~ 2^eq)
       const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
       float* dst = p.dk + grow * D;
       const float* cs = p.cos_tab + (long long)key * (D / 2);
@@ -863,16 +507,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
-  if (p.D == 128) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_db_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DbCfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv * p.hsplit);
-    attn_bwd_db_kernel<<<grid, kThreads, DbCfg::kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
-  }
-  return launch_bwd_d<64>(p, stream);
+  return p.D == 128 ? launch_bwd_d<128>(p, stream) : launch_bwd_d<64>(p, stream);
 }
 
 }  // namespace gbattn

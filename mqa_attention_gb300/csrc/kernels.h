@@ -140,7 +140,7 @@ struct BwdParams {
   int hsplit;  // CTAs sharing one (KV head, key tile): 1, or 2 (dK/dV summed with reductions)
 };
 // Query-tile rows used by the backward main kernel for head dimension D.
-inline int bwd_query_tile(int D) { return D == 128 ? 64 : 128; }
+inline int bwd_query_tile(int) { return 64; }
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
 
 }  // namespace gbattn
