@@ -94,6 +94,11 @@ SMALL = [
     (1, 32, 1, 128, 64, True),
     (2, 2, 1, 256, 64, False),
     (1, 4, 2, 384, 128, False),
+    # more steps than SMs: CTAs of the persistent backward cross key-tile units,
+    # some units whole in one CTA, others split between two
+    (2, 8, 2, 1024, 64, True),
+    (1, 8, 8, 1536, 128, True),
+    (1, 4, 2, 1152, 128, False),
 ]
 
 
