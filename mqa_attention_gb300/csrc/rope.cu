@@ -82,39 +82,34 @@ __device__ __forceinline__ void store8_bf16_scaled_f16(void* p, const float (&o)
 
 // Largest |x| of bf16 tensors. For a non-negative bf16 value the bit pattern
 // orders like the value, so the maximum is taken on the 15-bit magnitudes of
-// packed pairs (__vmaxu2) and converted back to float once per thread. The
-// tensors form one index space of 16-byte chunks (tensor 0's chunks, then
-// tensor 1's, ...); each thread loads kAbsChunks chunks, 256 apart, before it
-// uses any of them, so that enough loads are in flight to reach HBM bandwidth
-// even for the small K and V tensors.
-constexpr int kAbsChunks = 8;
+// packed pairs (__vmaxu2) and converted back to float once per thread.
 __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
   __shared__ uint32_t red[4][8];
-  // chunk index where each tensor ends (a null tensor holds none)
-  const long long e0 = p.x[0] != nullptr ? p.n[0] / 8 : 0;
-  const long long e1 = e0 + (p.x[1] != nullptr ? p.n[1] / 8 : 0);
-  const long long e2 = e1 + (p.x[2] != nullptr ? p.n[2] / 8 : 0);
-  const long long e3 = e2 + (p.x[3] != nullptr ? p.n[3] / 8 : 0);
-  const long long c0 = static_cast<long long>(blockIdx.x) * (256 * kAbsChunks) + threadIdx.x;
-  uint4 v[kAbsChunks];
-  int tt[kAbsChunks];
-#pragma unroll
-  for (int i = 0; i < kAbsChunks; ++i) {
-    const long long c = c0 + i * 256;
-    const int t = c < e0 ? 0 : c < e1 ? 1 : c < e2 ? 2 : c < e3 ? 3 : 4;
-    tt[i] = t;
-    const long long first = t == 0 ? 0 : t == 1 ? e0 : t == 2 ? e1 : e2;
-    const void* src = t == 0 ? p.x[0] : t == 1 ? p.x[1] : t == 2 ? p.x[2] : p.x[3];
-    v[i] = t < 4 ? __ldg(static_cast<const uint4*>(src) + (c - first)) : make_uint4(0u, 0u, 0u, 0u);
-  }
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
+  for (int t = 0; t < 4; ++t) {
+    if (p.x[t] == nullptr) continue;
+    const uint4* src = static_cast<const uint4*>(p.x[t]);
+    const long long chunks = p.n[t] / 8;
+    uint32_t acc = 0u;
+    long long c = t0;
+    for (; c + 3 * stride < chunks; c += 4 * stride) {
+      const uint4 a = __ldg(src + c), b = __ldg(src + c + stride);
+      const uint4 d = __ldg(src + c + 2 * stride), g = __ldg(src + c + 3 * stride);
+      const uint4 v[4] = {a, b, d, g};
 #pragma unroll
-  for (int i = 0; i < kAbsChunks; ++i) {
-    const uint32_t x = __vmaxu2(__vmaxu2(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu),
-                                __vmaxu2(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu));
-    const uint32_t y = max(x & 0xffffu, x >> 16);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) m[t] = tt[i] == t ? max(m[t], y) : m[t];
+      for (int i = 0; i < 4; ++i)
+        acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu),
+                                     __vmaxu2(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu)));
+    }
+    for (; c < chunks; c += stride) {
+      const uint4 a = __ldg(src + c);
+      acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(a.x & 0x7fff7fffu, a.y & 0x7fff7fffu),
+                                   __vmaxu2(a.z & 0x7fff7fffu, a.w & 0x7fff7fffu)));
+    }
+    m[t] = max(acc & 0xffffu, acc >> 16);
   }
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -128,8 +123,7 @@ __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
     uint32_t b = 0u;
     for (int w = 0; w < 8; ++w) b = max(b, red[t][w]);
     // bf16 magnitude bits -> float bits; non-negative floats order like their bits
-    const bool present = t == 0 ? e0 > 0 : t == 1 ? e1 > e0 : t == 2 ? e2 > e1 : e3 > e2;
-    if (present && b != 0u) atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), b << 16);
+    if (p.x[t] != nullptr) atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), b << 16);
   }
 }
 
@@ -255,11 +249,7 @@ cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, doub
 }
 
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
-  long long chunks = 0;
-  for (int t = 0; t < 4; ++t) chunks += p.x[t] != nullptr ? p.n[t] / 8 : 0;
-  const long long per_block = 256LL * kAbsChunks;
-  const unsigned grid = static_cast<unsigned>((chunks + per_block - 1) / per_block);
-  if (grid > 0) absmax_kernel<<<grid, 256, 0, stream>>>(p);
+  absmax_kernel<<<152 * 8, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
