@@ -5,10 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
-#include <algorithm>
-#include <functional>
 #include <mutex>
-#include <queue>
 #include <tuple>
 #include <vector>
 
@@ -198,98 +195,6 @@ int rope_table(DeviceState* d, int S, int D, float theta, cudaStream_t stream, f
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// ---------------------------------------------------------------- backward work plan
-// Longest-piece-first schedule of the backward main kernel's CTAs on `nsm` SMs:
-// the time the last SM finishes, in steps, with a start-up cost per CTA (K~/V
-// load, pipeline fill, dK/dV epilogue) of a few steps.
-double schedule_length(std::vector<double>& pieces, int nsm) {
-  std::sort(pieces.begin(), pieces.end(), std::greater<double>());
-  std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
-  for (int i = 0; i < nsm; ++i) sm.push(0.0);
-  double end = 0.0;
-  for (double x : pieces) {
-    const double t = sm.top() + x;
-    sm.pop();
-    sm.push(t);
-    end = std::max(end, t);
-  }
-  return end;
-}
-
-// Picks which key tiles' units to cut and into how many pieces (threshold K,
-// factor c: the units of key tiles kt < K are cut into c pieces) by comparing
-// the schedule lengths of every candidate; plans are cached per shape.
-gbattn::BwdPlan make_bwd_plan(int B, int Hq, int Hkv, int S, int causal, int nsm) {
-  static std::map<std::tuple<int, int, int, int, int, int>, gbattn::BwdPlan> cache;
-  const auto key = std::make_tuple(B, Hq, Hkv, S, causal, nsm);
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-  }
-  gbattn::BwdPlan pl;
-  std::memset(&pl, 0, sizeof(pl));
-  pl.nq = S / kTile;
-  pl.nu = B * Hkv;
-  pl.G = Hq / Hkv;
-  pl.causal = causal ? 1 : 0;
-  pl.nent = 0;
-  pl.split_below = 0;
-  const long long units = static_cast<long long>(pl.nq) * pl.nu;
-  // Many units already balance under the longest-first order; more key tiles
-  // than the table holds imply many units too.
-  if (pl.nq <= gbattn::kPlanMaxTiles && units < 4LL * nsm) {
-    constexpr double kStartSteps = 2.5, kSumSteps = 0.5;
-    static const int kFactors[] = {2, 3, 4, 6, 8};
-    double best = -1.0;
-    int best_k = 0, best_c = 1;
-    std::vector<double> pieces;
-    for (int K = 0; K <= pl.nq; ++K) {
-      for (int c : kFactors) {
-        if (K == 0 && c != kFactors[0]) continue;  // K = 0: nothing is cut
-        bool ok = true;
-        pieces.clear();
-        for (int kt = 0; kt < pl.nq && ok; ++kt) {
-          const int T = pl.unit_steps(kt);
-          const int cc = kt < K ? c : 1;
-          if (T / cc < 2) ok = false;
-          for (int part = 0; part < cc && ok; ++part) {
-            const int len = gbattn::BwdPlan::piece_begin(T, part + 1, cc) -
-                            gbattn::BwdPlan::piece_begin(T, part, cc);
-            const double cost = len + kStartSteps + (cc > 1 ? kSumSteps : 0.0);
-            for (int u = 0; u < pl.nu; ++u) pieces.push_back(cost);
-          }
-        }
-        if (!ok) continue;
-        const double len = schedule_length(pieces, nsm);
-        if (best < 0.0 || len < best - 1e-9) {
-          best = len;
-          best_k = K;
-          best_c = K == 0 ? 1 : c;
-        }
-      }
-    }
-    if (best_k > 0) {
-      pl.split_below = best_k;
-      for (int kt = 0; kt < pl.nq; ++kt) pl.parts[kt] = static_cast<uint8_t>(kt < best_k ? best_c : 1);
-      // entries longest piece first
-      std::vector<int> ord(pl.nq);
-      for (int kt = 0; kt < pl.nq; ++kt) ord[kt] = kt;
-      auto piece = [&](int kt) { return static_cast<double>(pl.unit_steps(kt)) / pl.parts[kt]; };
-      std::stable_sort(ord.begin(), ord.end(), [&](int a, int b) { return piece(a) > piece(b); });
-      pl.nent = pl.nq;
-      pl.start[0] = 0;
-      for (int e = 0; e < pl.nq; ++e) {
-        pl.order[e] = static_cast<int16_t>(ord[e]);
-        pl.start[e + 1] = pl.start[e] + pl.nu * pl.parts[ord[e]];
-      }
-    }
-  }
-  std::lock_guard<std::mutex> lk(g_mu);
-  cache.emplace(key, pl);
-  return pl;
-}
-
 }  // namespace
 
 extern "C" {
@@ -396,13 +301,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
   float* lse2 = reinterpret_cast<float*>(w); w += rowbytes;
   float* maxes = reinterpret_cast<float*>(w);
 
-  // Work plan of the main kernel: the heaviest key tiles' units cut into
-  // pieces so that the CTAs finish close together.
+  // Two CTAs per (KV head, key tile), each with half of the group's query heads,
+  // when one CTA per key tile would not fill the GPU (and the group splits
+  // evenly); otherwise one CTA per key tile, with no dK/dV zeroing.
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const gbattn::BwdPlan plan = make_bwd_plan(B, Hq, Hkv, S, causal, nsm);
+  const long long key_tiles = static_cast<long long>(B) * Hkv * (S / kTile);
+  const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
   bool ok = true;
   {
     LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
@@ -424,10 +331,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     rp.seg[0] = {q, qr, dout, dos, qrows};
     rp.seg[1] = {k, kr, v, vs, krows};
     rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
-    if (plan.split_below > 0) {  // pieces of a unit add their dK/dV partials
+    if (hsplit > 1) {  // the main kernel adds dK/dV partials of two CTAs
       rp.dk_zero = dk;
       rp.dv_zero = dv;
-      rp.split_below = plan.split_below;
     }
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
@@ -453,7 +359,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     bp.scale_log2 = scale * 1.4426950408889634f;
     bp.causal = causal ? 1 : 0;
     bp.inject_timeout = g_inject_timeout ? 1 : 0;
-    bp.plan = plan;
+    bp.hsplit = hsplit;
     LaunchTimer tm(ATTN_KERNEL_BWD_MAIN, stream);
     ok = gbattn::launch_bwd_main(bp, stream) == cudaSuccess;
     tm.done();

@@ -12,11 +12,12 @@
 // reduced inside the CTA: dK and dV accumulate in tensor memory across every
 // query head of the group.
 //
-// GB300 design: one CTA per (batch, KV head, 128-key tile) unit, or per piece
-// of a heavy unit (BwdPlan), keeps K~ and V in shared memory and walks its
-// (query head, 64-query tile) steps (only tiles on or below the diagonal when
-// causal). The pieces of a unit add their dK/dV partials into zeroed outputs;
-// CTAs are launched longest piece first, the pieces of one unit side by side.
+// GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
+// shared memory and walks the (query head, 64-query tile) steps that see its
+// keys (only tiles on or below the diagonal when causal). When one CTA per key
+// tile would not fill the GPU and the group has an even number of query heads,
+// two CTAs share a key tile, each taking half of the heads, and add their dK/dV
+// partials into zeroed outputs.
 //
 // Per step s (buffer b = s & 1), in TMEM:
 //   Sᵀ_b  = K~ Q~ᵀ  [128 keys x 64 queries]   (SS MMA)
@@ -116,41 +117,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
 
-  // ---- work item: piece `part` of the unit (key tile kt, KV head bhk); its
-  // steps lo + s, s < n, of the unit's head-major (query head, 64-query tile)
-  // steps
-  const BwdPlan& pl = p.plan;
-  int kt, idx;
-  if (pl.nent > 0) {
-    int lo_e = 0, hi_e = pl.nent;  // start[lo_e] <= blockIdx < start[hi_e]
-    while (hi_e - lo_e > 1) {
-      const int mid = (lo_e + hi_e) >> 1;
-      if (pl.start[mid] <= static_cast<int>(blockIdx.x)) lo_e = mid;
-      else hi_e = mid;
-    }
-    kt = pl.order[lo_e];
-    idx = static_cast<int>(blockIdx.x) - pl.start[lo_e];
-  } else {
-    kt = static_cast<int>(blockIdx.x) / pl.nu;
-    idx = static_cast<int>(blockIdx.x) % pl.nu;
-  }
-  const int nparts = pl.nparts(kt);
-  const int bhk = idx / nparts;
-  const int part = idx % nparts;
+  // ---- work item: key tile kt of KV head (b, hkv), query heads of part `part`
+  // of the group (hsplit parts); heaviest (kt = 0) first
+  const int units = p.B * p.Hkv * p.hsplit;
+  const int kt = static_cast<int>(blockIdx.x) / units;
+  const int unit = static_cast<int>(blockIdx.x) % units;
+  const int bhk = unit / p.hsplit;
+  const int part = unit % p.hsplit;
   const int b = bhk / p.Hkv;
   const int hkv = bhk % p.Hkv;
-  const int G = pl.G;
+  const int G = p.Hq / p.Hkv;
+  const int Gc = G / p.hsplit;  // query heads of this CTA
+  const int h_first = hkv * G + part * Gc;
   const int k0 = kt * kTile;
   const int kv_row = bhk * p.S + k0;
+  const int nqt = p.S / BQ;
   const int qt_begin = p.causal ? k0 / BQ : 0;
-  const int per_head = pl.steps_per_head(kt);  // even
-  const int T = G * per_head;
-  const int lo = BwdPlan::piece_begin(T, part, nparts);
-  const int n = BwdPlan::piece_begin(T, part + 1, nparts) - lo;  // even
+  const int per_head = nqt - qt_begin;  // even: S and k0 are multiples of 128
+  const int n = Gc * per_head;
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
-  auto step_qt = [&](int s) { return qt_begin + (lo + s) % per_head; };
+  auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
-    const int h = hkv * G + (lo + s) / per_head;
+    const int h = h_first + s / per_head;
     return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
   };
 
@@ -449,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     __syncwarp();
     tc_fence_after();
     const long long grow = kv_row + r;
-    const bool sum_parts = nparts > 1;  // other CTAs add into the same dk/dv rows
+    const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
     if (half == 0) {
       // dV accumulated Pᵀ (dO 2^edo)
       const float f = exp2i(-ex.dout);
@@ -511,7 +499,8 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_bwd_kernel<D><<<p.plan.ctas(), kThreads, C::kSmemBytes, stream>>>(p);
+  const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv * p.hsplit);
+  attn_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

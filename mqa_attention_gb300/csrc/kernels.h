@@ -68,48 +68,12 @@ struct AbsMaxParams {
 };
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream);
 
-// Work of the backward main kernel. A unit is one (batch, KV head, 128-key
-// tile); its steps are the (query head of the group, 64-query tile) pairs that
-// see the tile's keys (tiles on or below the diagonal when causal), head-major.
-// Under the causal mask the units of the first key tiles hold far more steps
-// than the last, so the heaviest (key tiles kt < split_below) are cut into
-// parts[kt] pieces of consecutive
-// steps (an even number each, so the two 64-query tiles of a 128-row tile stay
-// together); the pieces of one unit add their dK/dV into zeroed rows. CTAs run
-// longest piece first: entry e covers blockIdx [start[e], start[e + 1]) with
-// key tile order[e], bhk-major, the pieces of one unit adjacent. With more key
-// tiles than the table holds (nent == 0), CTA i takes the whole unit
-// (kt, bhk) = (i / nu, i % nu).
-constexpr int kPlanMaxTiles = 256;
-struct BwdPlan {
-  int nq;      // S / 128
-  int nu;      // B * Hkv
-  int G;       // Hq / Hkv
-  int causal;
-  int nent;    // table entries (0: whole units in key-tile order)
-  int split_below;
-  uint8_t parts[kPlanMaxTiles];
-  int16_t order[kPlanMaxTiles];
-  int start[kPlanMaxTiles + 1];
-  __host__ __device__ int steps_per_head(int kt) const { return 2 * (causal ? nq - kt : nq); }
-  __host__ __device__ int unit_steps(int kt) const { return G * steps_per_head(kt); }
-  __host__ __device__ int nparts(int kt) const { return nent > 0 ? parts[kt] : 1; }
-  // First step of piece `part` of a unit of T steps cut into c pieces.
-  __host__ __device__ static int piece_begin(int T, int part, int c) {
-    return part >= c ? T : (static_cast<int>(static_cast<long long>(T) * part / c) & ~1);
-  }
-  __host__ __device__ unsigned ctas() const {
-    return nent > 0 ? static_cast<unsigned>(start[nent]) : static_cast<unsigned>(nq * nu);
-  }
-};
-
 // Row pre-pass over the query rows (segment 0) and key rows (segment 1) of one
 // call, in one launch. Forward (bwd == 0): y = bf16(R x) for both segments.
 // Backward (bwd == 1):
 //   query rows: y = fp16(bf16(R q) 2^eq), y2 = fp16(dout 2^edo),
 //               delta = (dout . out) 2^(edo+ev), lse2 = lse log2(e), dqacc row = 0
-//   key rows:   y = fp16(bf16(R k) 2^ek),  y2 = fp16(v 2^ev), and the dk, dv
-//               rows of units the plan cuts into pieces zeroed
+//   key rows:   y = fp16(bf16(R k) 2^ek),  y2 = fp16(v 2^ev)
 struct RowSegment {
   const void* x;
   void* y;
@@ -129,9 +93,8 @@ struct RowPrepParams {
   const float* lse;
   float* lse2;
   float* dqacc;
-  float* dk_zero;  // backward, key rows of units cut into pieces: zeroed
+  float* dk_zero;  // backward, key rows: zeroed when the main kernel sums dK/dV partials
   float* dv_zero;
-  int split_below;  // the plan cuts the units of key tiles kt < split_below
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
@@ -174,7 +137,7 @@ struct BwdParams {
   float scale_log2;
   int causal;
   int inject_timeout;
-  BwdPlan plan;
+  int hsplit;  // CTAs sharing one (KV head, key tile): 1, or 2 (dK/dV summed with reductions)
 };
 // Query-tile rows used by the backward main kernel for head dimension D.
 inline int bwd_query_tile(int) { return 64; }

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
     for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
 #pragma unroll
     for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (!is_q && live && p.dk_zero != nullptr && pos / kTile < p.split_below) {
+    if (!is_q && live && p.dk_zero != nullptr) {
       const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       store8(p.dk_zero + e1, z);
       store8(p.dk_zero + e2, z);
