@@ -338,17 +338,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_ld32x2(tmem + lane_base + C::kColDQ, tmem + lane_base + C::kColDQ + 32, u0, u1);
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dq_free[0]));
-        // query rows of steps 2m, 2m+1 are consecutive rows of one head
-        float* base = p.dqacc + (static_cast<long long>(step_row(2 * m)) + r) * D;
+        // Query rows of steps 2m, 2m+1 are consecutive rows of one head. Within
+        // each group of 8 lanes (8 rows), an 8 x 8 transpose of 16-byte chunks
+        // (three exchange stages) gives lane i chunk i of each of the 8 rows, so
+        // that every vector reduction covers 4 whole 128-byte row segments.
+        const int gl = lane & 7;
+        float* rows0 = p.dqacc + (static_cast<long long>(step_row(2 * m)) + (r & ~7)) * D;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          red_add_v4_f32(base + 4 * i, __uint_as_float(u0[4 * i]), __uint_as_float(u0[4 * i + 1]),
-                         __uint_as_float(u0[4 * i + 2]), __uint_as_float(u0[4 * i + 3]));
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          red_add_v4_f32(base + 32 + 4 * i, __uint_as_float(u1[4 * i]),
-                         __uint_as_float(u1[4 * i + 1]), __uint_as_float(u1[4 * i + 2]),
-                         __uint_as_float(u1[4 * i + 3]));
+          for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[c][e] = __uint_as_float(hf ? u1[4 * c + e] : u0[4 * c + e]);
+#pragma unroll
+          for (int mk = 4; mk > 0; mk >>= 1) {
+            const bool up = (gl & mk) != 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              if (c & mk) continue;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // lanes without bit mk send chunk c|mk and keep c; the others send
+                // chunk c and keep c|mk
+                const float send = up ? x[c][e] : x[c | mk][e];
+                const float got = __shfl_xor_sync(0xffffffffu, send, mk);
+                if (up) x[c][e] = got;
+                else x[c | mk][e] = got;
+              }
+            }
+          }
+          // now x[k] = chunk gl of row (group base + k)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            red_add_v4_f32(rows0 + static_cast<long long>(k) * D + 32 * hf + 4 * gl, x[k][0],
+                           x[k][1], x[k][2], x[k][3]);
+        }
       }
     } else {
       for (int s = 0; s < n; ++s) {
