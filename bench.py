@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[w.name for w in WORKLOADS])
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", choices=["half", "interleaved"], default="half",
+                    help="RoPE pair layout (interleaved runs attn_fwd_ex / attn_bwd_ex)")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
@@ -269,9 +271,9 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, n, l2):
+def config_of(wl, n, l2, rope="half"):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
-            "rope_theta": wl.theta, "causal": wl.causal,
+            "rope_theta": wl.theta, "rope": rope, "causal": wl.causal,
             "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
             "l2": l2}
 
@@ -300,11 +302,25 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     dims = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, wl.scale, wl.causal)
+    mode = M.ROPE_MODES[args.rope]
+    dims_ex = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, mode, wl.scale, wl.causal)
+
+    def fwd(q_, k_, v_, out_, lse_, st):
+        if args.rope == "half":
+            M.attn_fwd(q_, k_, v_, out_, lse_, *dims, stream=st)
+        else:
+            M.attn_fwd_ex(q_, k_, v_, out_, lse_, *dims_ex, stream=st)
+
+    def bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, st):
+        if args.rope == "half":
+            M.attn_bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims, stream=st)
+        else:
+            M.attn_bwd_ex(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims_ex, stream=st)
 
     def step():
-        M.attn_fwd(q, k, v, out, lse, *dims, stream=stream)
+        fwd(q, k, v, out, lse, stream)
         if wl.backward:
-            M.attn_bwd(q, k, v, out, lse, do, dq, dk, dv, *dims, stream=stream)
+            bwd(q, k, v, out, lse, do, dq, dk, dv, stream)
 
     for _ in range(args.warmup):
         step()
@@ -378,10 +394,10 @@ def run_ours(args, rank, world, local):
         stream.wait_event(ev["in"][b])
         if used[b]:
             stream.wait_event(ev["out"][b])  # step i-2's results have left the device
-        M.attn_fwd(d["q"], d["k"], d["v"], d["out"], d["lse"], *dims, stream=stream)
+        fwd(d["q"], d["k"], d["v"], d["out"], d["lse"], stream)
         if wl.backward:
-            M.attn_bwd(d["q"], d["k"], d["v"], d["out"], d["lse"], d["dout"], d["dq"], d["dk"],
-                       d["dv"], *dims, stream=stream)
+            bwd(d["q"], d["k"], d["v"], d["out"], d["lse"], d["dout"], d["dq"], d["dk"], d["dv"],
+                stream)
         ev["comp"][b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev["comp"][b])
@@ -435,7 +451,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
-        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)"),
+        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)", rope=args.rope),
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers; each step's inputs in and results out on two "

@@ -90,6 +90,28 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
              int D, float rope_theta, float scale, int causal, attn_stream_t stream);
 
+/* RoPE pair layouts of attn_fwd_ex / attn_bwd_ex. Both rotate pair i of a row at
+ * position p by the angle p * rope_theta^(-2i/D), i < D/2:
+ *   ATTN_ROPE_HALF        pairs (x_i, x_{i+D/2}): x*cos + rotate_half(x)*sin with
+ *                         rotate_half(x) = cat(-x2, x1) (Picotron §1; PaLM §2.3);
+ *                         the layout of attn_fwd / attn_bwd.
+ *   ATTN_ROPE_INTERLEAVED pairs (x_{2i}, x_{2i+1}) read as the complex number
+ *                         x_2i + j x_2i+1 and multiplied by polar(1, angle)
+ *                         (llama3-from-scratch §RoPE). */
+enum { ATTN_ROPE_HALF = 0, ATTN_ROPE_INTERLEAVED = 1 };
+
+/* attn_fwd / attn_bwd with the RoPE pair layout chosen by rope_mode (one of the
+ * ATTN_ROPE_* values; anything else returns ATTN_ERR_INVALID). Arguments, layouts,
+ * ownership and errors are otherwise those of attn_fwd / attn_bwd; attn_fwd(...) is
+ * attn_fwd_ex(..., rope_theta, ATTN_ROPE_HALF, scale, ...). */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
+                int causal, attn_stream_t stream);
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+                int D, float rope_theta, int rope_mode, float scale, int causal,
+                attn_stream_t stream);
+
 /* Waits for all work on `stream`, then reads and clears the device status word of the
  * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait since the
  * last call (its outputs are then undefined). Synchronises the host with `stream`. */

@@ -20,6 +20,8 @@ __all__ = [
     "attn_fwd",
     "attn_bwd",
     "attn_fwd_noalloc",
+    "attn_fwd_ex",
+    "attn_bwd_ex",
     "forward",
     "backward",
     "sync_status",
@@ -46,6 +48,8 @@ KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL = ran
 EXPORTED_SYMBOLS = (
     "attn_fwd",
     "attn_bwd",
+    "attn_fwd_ex",
+    "attn_bwd_ex",
     "attn_sync_status",
     "attn_status_string",
     "attn_profile_begin",
@@ -103,6 +107,11 @@ def lib() -> ctypes.CDLL:
             L.attn_version.restype = ctypes.c_char_p
             L.attn_fwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P]
             L.attn_fwd_noalloc.restype = _I
+            L.attn_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _I, _P]
+            L.attn_fwd_ex.restype = _I
+            L.attn_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _I, _I, _I, _I, _I, _F, _I, _F, _I, _P]
+            L.attn_bwd_ex.restype = _I
             _lib = L
         return _lib
 
@@ -157,26 +166,53 @@ def attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, 
                           _stream(stream)), "attn_bwd")
 
 
+ROPE_MODES = {"half": 0, "interleaved": 1}  # ATTN_ROPE_HALF, ATTN_ROPE_INTERLEAVED
+
+
+def attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, rope_mode, scale, causal,
+                stream=None):
+    """C ABI attn_fwd_ex: attn_fwd with the RoPE pair layout rope_mode (0 half-split,
+    1 interleaved complex pairs)."""
+    _check(lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(Hq),
+                             int(Hkv), int(S), int(D), float(rope_theta), int(rope_mode),
+                             float(scale), 1 if causal else 0, _stream(stream)), "attn_fwd_ex")
+
+
+def attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
+                scale, causal, stream=None):
+    """C ABI attn_bwd_ex: attn_bwd with the RoPE pair layout rope_mode."""
+    _check(lib().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                             _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S),
+                             int(D), float(rope_theta), int(rope_mode), float(scale),
+                             1 if causal else 0, _stream(stream)), "attn_bwd_ex")
+
+
 def _shapes(q, k):
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     return B, Hq, Hkv, S, D
 
 
-def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None):
-    """Allocates out / lse like q and runs attn_fwd. q: [B,Hq,S,D], k, v: [B,Hkv,S,D]."""
+def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None, rope="half"):
+    """Allocates out / lse like q and runs attn_fwd (attn_fwd_ex for rope="interleaved").
+    q: [B,Hq,S,D], k, v: [B,Hkv,S,D]."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, stream)
+    if rope == "half":
+        attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, stream)
+    else:
+        attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, ROPE_MODES[rope], scale,
+                    causal, stream)
     return out, lse
 
 
-def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None):
-    """Allocates fp32 dq, dk, dv and runs attn_bwd."""
+def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None,
+             rope="half"):
+    """Allocates fp32 dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved")."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
@@ -184,8 +220,12 @@ def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, strea
     dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
     dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
-    attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
-             stream)
+    if rope == "half":
+        attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
+                 stream)
+    else:
+        attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
+                    ROPE_MODES[rope], scale, causal, stream)
     return dq, dk, dv
 
 

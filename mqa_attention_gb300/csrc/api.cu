@@ -212,12 +212,13 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
-             int Hkv, int S, int D, float rope_theta, float scale, int causal,
-             attn_stream_t stream_) {
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
+                int causal, attn_stream_t stream_) {
   const void* ptrs[] = {q, k, v, out, lse};
   int st = validate(ptrs, 5, B, Hq, Hkv, S, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
+  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -239,6 +240,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   {
     gbattn::RowPrepParams rp{};
     rp.bwd = 0;
+    rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
@@ -267,12 +269,22 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-             const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
-             int D, float rope_theta, float scale, int causal, attn_stream_t stream_) {
+int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float rope_theta, float scale, int causal,
+             attn_stream_t stream) {
+  return attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, ATTN_ROPE_HALF, scale,
+                     causal, stream);
+}
+
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+                int D, float rope_theta, int rope_mode, float scale, int causal,
+                attn_stream_t stream_) {
   const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv};
   int st = validate(ptrs, 9, B, Hq, Hkv, S, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
+  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  const int inter = rope_mode == ATTN_ROPE_INTERLEAVED;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -323,6 +335,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
          gbattn::launch_absmax(ap, stream) == cudaSuccess;
     gbattn::RowPrepParams rp{};
     rp.bwd = 1;
+    rp.rope_interleaved = inter;
     rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
@@ -360,18 +373,26 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
     bp.causal = causal ? 1 : 0;
     bp.inject_timeout = g_inject_timeout ? 1 : 0;
     bp.hsplit = hsplit;
+    bp.rope_interleaved = inter;
     LaunchTimer tm(ATTN_KERNEL_BWD_MAIN, stream);
     ok = gbattn::launch_bwd_main(bp, stream) == cudaSuccess;
     tm.done();
   }
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
-    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, maxes, cs, sn, stream) ==
+    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, maxes, cs, sn, inter, stream) ==
          cudaSuccess;
     tm.done();
   }
   cudaFreeAsync(ws, stream);
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+             const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+             int D, float rope_theta, float scale, int causal, attn_stream_t stream) {
+  return attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
+                     ATTN_ROPE_HALF, scale, causal, stream);
 }
 
 int attn_sync_status(attn_stream_t stream_) {

@@ -478,33 +478,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                f * __uint_as_float(u[4 * i + 3]), sum_parts);
       }
     } else {
-      // dk = scale * R_keyᵀ dk~ (rotation by -angle), pairs (i, i + D/2); dK
+      // dk = scale * R_keyᵀ dk~ (rotation by -angle); dK
       // accumulated (dS 2^(edo+ev)) (q~ 2^eq)
       const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
       float* dst = p.dk + grow * D;
       const float* cs = p.cos_tab + (long long)key * (D / 2);
       const float* sn = p.sin_tab + (long long)key * (D / 2);
+      if (p.rope_interleaved) {
+        // complex pairs (2j, 2j+1) at frequency j: columns [64 ch, 64 ch + 64) hold
+        // the frequencies [32 ch, 32 ch + 32)
 #pragma unroll 1
-      for (int ch = 0; ch < D / 64; ++ch) {
-        uint32_t x1[32], x2[32];
-        tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 32,
-                    tmem + lane_base + C::kColDK + D / 2 + ch * 32, x1, x2);
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t x1[32], x2[32];
+          tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 64,
+                      tmem + lane_base + C::kColDK + ch * 64 + 32, x1, x2);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
-          const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
-          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-          const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-          float y1[4], y2[4];
+          for (int i = 0; i < 8; ++i) {
+            const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
+            const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
+            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+            float y[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = __uint_as_float(x1[4 * i + e]);
-            const float bb = __uint_as_float(x2[4 * i + e]);
-            y1[e] = f * (a * cc[e] + bb * ss[e]);
-            y2[e] = f * (bb * cc[e] - a * ss[e]);
+            for (int e = 0; e < 4; ++e) {
+              const int k = 8 * (i & 3) + 2 * e;
+              const float xe = __uint_as_float(i < 4 ? x1[k] : x2[k]);
+              const float xo = __uint_as_float(i < 4 ? x1[k + 1] : x2[k + 1]);
+              y[2 * e] = f * (xe * cc[e] + xo * ss[e]);
+              y[2 * e + 1] = f * (xo * cc[e] - xe * ss[e]);
+            }
+            put4(dst + ch * 64 + 8 * i, y[0], y[1], y[2], y[3], sum_parts);
+            put4(dst + ch * 64 + 8 * i + 4, y[4], y[5], y[6], y[7], sum_parts);
           }
-          put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
-          put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t x1[32], x2[32];
+          tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 32,
+                      tmem + lane_base + C::kColDK + D / 2 + ch * 32, x1, x2);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
+            const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
+            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+            float y1[4], y2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = __uint_as_float(x1[4 * i + e]);
+              const float bb = __uint_as_float(x2[4 * i + e]);
+              y1[e] = f * (a * cc[e] + bb * ss[e]);
+              y2[e] = f * (bb * cc[e] - a * ss[e]);
+            }
+            put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
+            put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
+          }
         }
       }
     }

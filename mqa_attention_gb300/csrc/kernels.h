@@ -83,6 +83,7 @@ struct RowSegment {
 };
 struct RowPrepParams {
   int bwd;
+  int rope_interleaved;  // 0: half-split pairs (i, i + D/2); 1: pairs (2i, 2i + 1)
   RowSegment seg[2];
   int S, D;
   const float* cos_tab;
@@ -101,7 +102,7 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 // dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in, fp32 out).
 cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
                                float scale, const float* maxes, const float* cos_tab,
-                               const float* sin_tab, cudaStream_t stream);
+                               const float* sin_tab, int rope_interleaved, cudaStream_t stream);
 
 // ---------------------------------------------------------------- main kernels
 struct FwdParams {
@@ -138,6 +139,7 @@ struct BwdParams {
   int causal;
   int inject_timeout;
   int hsplit;  // CTAs sharing one (KV head, key tile): 1, or 2 (dK/dV summed with reductions)
+  int rope_interleaved;  // rotation pairs of the dk epilogue (see RowPrepParams)
 };
 // Query-tile rows used by the backward main kernel for head dimension D.
 inline int bwd_query_tile(int) { return 64; }

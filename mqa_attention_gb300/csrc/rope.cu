@@ -9,7 +9,9 @@
 // RoPE is the half-split rotation x*cos + rotate_half(x)*sin with
 // rotate_half(x) = cat(-x2, x1) and inverse frequencies theta^(-2i/D)
 // ("Picotron模型实现解析Llama架构与Flash Attention集成", §1 嵌入层与位置编码;
-//  "ColossalAI 中的 PaLM 教学实现…", §2.3 RotaryEmbedding).
+//  "ColossalAI 中的 PaLM 教学实现…", §2.3 RotaryEmbedding), or, in the interleaved
+// mode, the rotation of the complex pairs x_2i + j x_2i+1 by the same angles
+// ("深度学习系统设计llama3-from-scratch：并行计算架构", §RoPE).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,6 +34,36 @@ __global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict
   sincos(static_cast<double>(p) * inv_freq, &s, &c);
   cos_tab[idx] = static_cast<float>(c);
   sin_tab[idx] = static_cast<float>(s);
+}
+
+// Element offsets (within a row) of the two 8-element groups a thread holds
+// for its chunk c < D/16, and their rotation. Half-split: elements [8c, 8c+8)
+// and [D/2 + 8c, +8), pairs (a_i, b_i) at frequency 8c + i. Interleaved:
+// elements [16c, 16c+16), pairs (a_2j, a_2j+1) at frequency 8c + j and
+// (b_2j, b_2j+1) at 8c + 4 + j. Both use the table entries [8c, 8c+8) of the
+// row's position; sgn = 1 rotates by +angle, -1 by -angle (the transpose).
+__device__ __forceinline__ int rope_off_a(int c, bool inter) { return inter ? 16 * c : 8 * c; }
+__device__ __forceinline__ int rope_off_b(int c, int D, bool inter) {
+  return inter ? 16 * c + 8 : D / 2 + 8 * c;
+}
+__device__ __forceinline__ void rotate16(const float (&a)[8], const float (&b)[8],
+                                         const float (&cs)[8], const float (&sn)[8], bool inter,
+                                         float sgn, float (&ya)[8], float (&yb)[8]) {
+  if (!inter) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      ya[i] = a[i] * cs[i] - sgn * (b[i] * sn[i]);
+      yb[i] = b[i] * cs[i] + sgn * (a[i] * sn[i]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      ya[2 * j] = a[2 * j] * cs[j] - sgn * (a[2 * j + 1] * sn[j]);
+      ya[2 * j + 1] = a[2 * j + 1] * cs[j] + sgn * (a[2 * j] * sn[j]);
+      yb[2 * j] = b[2 * j] * cs[4 + j] - sgn * (b[2 * j + 1] * sn[4 + j]);
+      yb[2 * j + 1] = b[2 * j + 1] * cs[4 + j] + sgn * (b[2 * j] * sn[4 + j]);
+    }
+  }
 }
 
 struct alignas(16) Vec8x16 {
@@ -127,8 +159,9 @@ __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
   }
 }
 
-// One thread per (row, c) with c < D/16: elements [8c, 8c+8) and [D/2+8c, D/2+8c+8).
-// Rows [0, seg[0].rows) are query rows, the next seg[1].rows are key rows.
+// One thread per (row, c) with c < D/16 and the two element groups of
+// rope_off_a / rope_off_b. Rows [0, seg[0].rows) are query rows, the next
+// seg[1].rows are key rows.
 template <int D, bool kBwd>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   constexpr int T = D / 16;  // threads per row
@@ -144,18 +177,15 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   const bool live = row0 < sg.rows;
   const long long r = live ? row0 : 0;
   const int pos = static_cast<int>(r % p.S);
-  const long long e1 = r * D + 8 * c;
-  const long long e2 = e1 + H;
+  const bool inter = p.rope_interleaved != 0;
+  const long long e1 = r * D + rope_off_a(c, inter);
+  const long long e2 = r * D + rope_off_b(c, D, inter);
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
   load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e1, x1);
   load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
   load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
   load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y1[i] = x1[i] * cs[i] - x2[i] * sn[i];
-    y2[i] = x2[i] * cs[i] + x1[i] * sn[i];
-  }
+  rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
   if constexpr (!kBwd) {
     if (live) {
       store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + e1, y1);
@@ -210,7 +240,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
     dq_finalize_kernel(const float* __restrict__ dqacc, float* __restrict__ dq, long long rows,
                        int S, float scale, const float* __restrict__ maxes,
-                       const float* __restrict__ cos_tab, const float* __restrict__ sin_tab) {
+                       const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
+                       int rope_interleaved) {
   constexpr int T = D / 16;
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -218,8 +249,9 @@ __global__ void __launch_bounds__(256)
   if (row >= rows) return;
   const int c = static_cast<int>(t % T);
   const int pos = static_cast<int>(row % S);
-  const long long e1 = row * D + 8 * c;
-  const long long e2 = e1 + H;
+  const bool inter = rope_interleaved != 0;
+  const long long e1 = row * D + rope_off_a(c, inter);
+  const long long e2 = row * D + rope_off_b(c, D, inter);
   const BwdExponents ex = bwd_exponents(maxes);
   const float f = scale * exp2i(-(ex.dout + ex.v + ex.k));
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
@@ -227,11 +259,11 @@ __global__ void __launch_bounds__(256)
   load8(dqacc + e2, x2);
   load8(cos_tab + (long long)pos * H + 8 * c, cs);
   load8(sin_tab + (long long)pos * H + 8 * c, sn);
+  rotate16(x1, x2, cs, sn, inter, -1.f, y1, y2);  // transpose: rotation by -angle
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    // transpose of the rotation: rotation by -angle
-    y1[i] = f * (x1[i] * cs[i] + x2[i] * sn[i]);
-    y2[i] = f * (x2[i] * cs[i] - x1[i] * sn[i]);
+    y1[i] *= f;
+    y2[i] *= f;
   }
   store8(dq + e1, y1);
   store8(dq + e2, y2);
@@ -268,15 +300,15 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
 
 cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
                                float scale, const float* maxes, const float* cos_tab,
-                               const float* sin_tab, cudaStream_t stream) {
+                               const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
   if (D == 128)
     dq_finalize_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
-                                                       sin_tab);
+                                                       sin_tab, rope_interleaved);
   else
     dq_finalize_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
-                                                      sin_tab);
+                                                      sin_tab, rope_interleaved);
   return cudaGetLastError();
 }
 

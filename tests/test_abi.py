@@ -79,6 +79,16 @@ def test_bwd_rejects_bad_arguments(built_lib, kw, code):
     assert bwd_code(built_lib, **kw) == code
 
 
+@pytest.mark.parametrize("mode", [-1, 2, 7])
+def test_ex_entry_points_reject_unknown_rope_modes(built_lib, mode):
+    """attn_fwd_ex / attn_bwd_ex take ATTN_ROPE_HALF (0) or ATTN_ROPE_INTERLEAVED (1)."""
+    lib = built_lib
+    assert lib.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 128, 64, 10000.0, mode, 0.125,
+                           1, None) == M.ATTN_ERR_INVALID
+    assert lib.attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 128, 64,
+                           10000.0, mode, 0.125, 1, None) == M.ATTN_ERR_INVALID
+
+
 def test_profile_arguments(built_lib):
     assert built_lib.attn_profile_begin(0) == M.ATTN_ERR_INVALID
     n, ms = ctypes.c_int(), ctypes.c_float()

@@ -33,12 +33,13 @@ def gen(wl: Workload):
     return dev, f64
 
 
-def run_gpu(wl: Workload, dev, backward=True):
-    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+def run_gpu(wl: Workload, dev, backward=True, rope="half"):
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal, rope=rope)
     res = {"out": out, "lse": lse}
     if backward:
         res["dq"], res["dk"], res["dv"] = M.backward(dev["q"], dev["k"], dev["v"], out, lse,
-                                                     dev["dout"], wl.theta, wl.scale, wl.causal)
+                                                     dev["dout"], wl.theta, wl.scale, wl.causal,
+                                                     rope=rope)
     torch.cuda.synchronize()
     assert M.sync_status() == 0
     return {k: v.double().cpu() for k, v in res.items()}
@@ -66,18 +67,18 @@ def grad_bounds(wl):
     return MAX_ABS * f, MEAN_ABS * f
 
 
-def check_all(wl, g, f, backward=True):
+def check_all(wl, g, f, backward=True, rope="half"):
     """Full oracle comparison (both RoPE precisions)."""
     gmax, gmean = grad_bounds(wl)
     for rr in (True, False):
         out, lse = O.attention_forward(f["q"], f["k"], f["v"], wl.scale, wl.theta, wl.causal,
-                                       round_rotated=rr)
+                                       rope=rope, round_rotated=rr)
         assert_close(f"out(rr={rr})", g["out"], out)
         if rr:
             assert_close("lse", g["lse"], lse, LSE_ABS, LSE_ABS)
         if backward:
             dq, dk, dv = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta,
-                                              wl.causal, round_rotated=rr)
+                                              wl.causal, rope=rope, round_rotated=rr)
             assert_close(f"dq(rr={rr})", g["dq"], dq, gmax, gmean)
             assert_close(f"dk(rr={rr})", g["dk"], dk, gmax, gmean)
             assert_close(f"dv(rr={rr})", g["dv"], dv, gmax, gmean)
@@ -109,6 +110,37 @@ def test_small_shapes(B, Hq, Hkv, S, D, causal):
     dev, f = gen(wl)
     g = run_gpu(wl, dev)
     check_all(wl, g, f)
+
+
+INTERLEAVED = [
+    # (B, Hq, Hkv, S, D, causal): both head sizes, a split key-tile grid (dk summed
+    # from two CTAs), non-causal, and a Llama-like group at S = 1024
+    (1, 4, 1, 256, 64, True),
+    (1, 2, 1, 384, 128, True),
+    (2, 4, 2, 256, 128, False),
+    (1, 8, 2, 1024, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", INTERLEAVED)
+def test_interleaved_rope(B, Hq, Hkv, S, D, causal):
+    """attn_fwd_ex / attn_bwd_ex with ATTN_ROPE_INTERLEAVED against the oracle's
+    complex-pair rotation ("深度学习系统设计llama3-from-scratch：并行计算架构", §RoPE)."""
+    wl = Workload(200 + S // 128 + D, "interleaved", B, Hq, Hkv, S, D,
+                  10000.0 if D == 64 else 500000.0, True, causal)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev, rope="interleaved")
+    check_all(wl, g, f, rope="interleaved")
+
+
+def test_interleaved_differs_from_half_split():
+    """The two layouts really rotate different pairs (guards against a mode flag
+    that is ignored)."""
+    wl = Workload(230, "interleaved", 1, 2, 1, 256, 64, 10000.0, True, True)
+    dev, _ = gen(wl)
+    a = run_gpu(wl, dev, rope="interleaved")
+    b = run_gpu(wl, dev, rope="half")
+    assert (a["out"] - b["out"]).abs().max().item() > 1e-2
 
 
 def test_tiny_mqa_forward_workload():
