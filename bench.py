@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rope", choices=["half", "interleaved"], default="half",
                     help="RoPE pair layout (interleaved runs attn_fwd_ex / attn_bwd_ex)")
+    ap.add_argument("--grads", choices=["fp32", "bf16"], default="fp32",
+                    help="gradient dtype (bf16 runs attn_bwd_bf16)")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
@@ -271,9 +273,9 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, n, l2, rope="half"):
+def config_of(wl, n, l2, rope="half", grads="fp32"):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
-            "rope_theta": wl.theta, "rope": rope, "causal": wl.causal,
+            "rope_theta": wl.theta, "rope": rope, "grads": grads, "causal": wl.causal,
             "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
             "l2": l2}
 
@@ -296,9 +298,10 @@ def run_ours(args, rank, world, local):
     q, k, v, do = dev["q"], dev["k"], dev["v"], dev["dout"]
     out = torch.empty_like(q)
     lse = torch.empty((wl.B, wl.Hq, wl.S), dtype=torch.float32, device="cuda")
-    dq = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-    dk = torch.empty(k.shape, dtype=torch.float32, device="cuda")
-    dv = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+    gdt = torch.bfloat16 if args.grads == "bf16" else torch.float32
+    dq = torch.empty(q.shape, dtype=gdt, device="cuda")
+    dk = torch.empty(k.shape, dtype=gdt, device="cuda")
+    dv = torch.empty(v.shape, dtype=gdt, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     dims = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, wl.scale, wl.causal)
@@ -312,7 +315,9 @@ def run_ours(args, rank, world, local):
             M.attn_fwd_ex(q_, k_, v_, out_, lse_, *dims_ex, stream=st)
 
     def bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, st):
-        if args.rope == "half":
+        if args.grads == "bf16":
+            M.attn_bwd_bf16(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims_ex, stream=st)
+        elif args.rope == "half":
             M.attn_bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims, stream=st)
         else:
             M.attn_bwd_ex(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims_ex, stream=st)
@@ -365,7 +370,7 @@ def run_ours(args, rank, world, local):
           "lse": torch.empty(lse.shape, dtype=torch.float32).pin_memory()}
     if wl.backward:
         for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-            ho[n] = torch.empty(t.shape, dtype=torch.float32).pin_memory()
+            ho[n] = torch.empty(t.shape, dtype=gdt).pin_memory()
     h2d = sum(t.numel() * t.element_size() for n, t in hp.items()
               if wl.backward or n != "dout")
     d2h = sum(t.numel() * t.element_size() for t in ho.values())
@@ -451,7 +456,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
-        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)", rope=args.rope),
+        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)", rope=args.rope,
+                            grads=args.grads),
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers; each step's inputs in and results out on two "

@@ -112,6 +112,18 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
                 int D, float rope_theta, int rope_mode, float scale, int causal,
                 attn_stream_t stream);
 
+/* attn_bwd_ex writing bf16 gradients: dq [B,Hq,S,D], dk, dv [B,Hkv,S,D] bf16, each the
+ * value attn_bwd_ex writes in fp32 rounded to nearest even (dk and dv bit for bit;
+ * dq's fp32 value sums its partial products in a run-dependent order, so it may
+ * differ from another run's by one bf16 ulp). The rounding alone can exceed the
+ * fp32 path's error by half a bf16 ulp of the gradient (|dv| ~ 11 at the PaLM-MQA
+ * shape gives ~0.03), which is why fp32 is the primary output. Uses
+ * 2 * B*Hkv*S*D*4 bytes more workspace than attn_bwd_ex. */
+int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+                  int D, float rope_theta, int rope_mode, float scale, int causal,
+                  attn_stream_t stream);
+
 /* Waits for all work on `stream`, then reads and clears the device status word of the
  * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait since the
  * last call (its outputs are then undefined). Synchronises the host with `stream`. */

@@ -22,6 +22,7 @@ __all__ = [
     "attn_fwd_noalloc",
     "attn_fwd_ex",
     "attn_bwd_ex",
+    "attn_bwd_bf16",
     "forward",
     "backward",
     "sync_status",
@@ -50,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd",
     "attn_fwd_ex",
     "attn_bwd_ex",
+    "attn_bwd_bf16",
     "attn_sync_status",
     "attn_status_string",
     "attn_profile_begin",
@@ -112,6 +114,8 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       _I, _I, _I, _I, _I, _F, _I, _F, _I, _P]
             L.attn_bwd_ex.restype = _I
+            L.attn_bwd_bf16.argtypes = L.attn_bwd_ex.argtypes
+            L.attn_bwd_bf16.restype = _I
             _lib = L
         return _lib
 
@@ -187,6 +191,16 @@ def attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_thet
                              1 if causal else 0, _stream(stream)), "attn_bwd_ex")
 
 
+def attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
+                  scale, causal, stream=None):
+    """C ABI attn_bwd_bf16: attn_bwd_ex writing bf16 dq, dk, dv (the fp32 values
+    rounded to nearest even)."""
+    _check(lib().attn_bwd_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S),
+                               int(D), float(rope_theta), int(rope_mode), float(scale),
+                               1 if causal else 0, _stream(stream)), "attn_bwd_bf16")
+
+
 def _shapes(q, k):
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -211,16 +225,21 @@ def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None, rope="hal
 
 
 def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None,
-             rope="half"):
-    """Allocates fp32 dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved")."""
+             rope="half", grad_dtype=None):
+    """Allocates dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved",
+    attn_bwd_bf16 for grad_dtype=torch.bfloat16; fp32 gradients otherwise)."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
-    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
-    if rope == "half":
+    gd = torch.bfloat16 if grad_dtype == torch.bfloat16 else torch.float32
+    dq = torch.empty(q.shape, dtype=gd, device=q.device)
+    dk = torch.empty(k.shape, dtype=gd, device=q.device)
+    dv = torch.empty(v.shape, dtype=gd, device=q.device)
+    if gd == torch.bfloat16:
+        attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
+                      ROPE_MODES[rope], scale, causal, stream)
+    elif rope == "half":
         attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
                  stream)
     else:

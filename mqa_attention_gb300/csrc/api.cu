@@ -276,11 +276,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                      causal, stream);
 }
 
-int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
-                int D, float rope_theta, int rope_mode, float scale, int causal,
-                attn_stream_t stream_) {
-  const void* ptrs[] = {q, k, v, out, lse, dout, dq, dk, dv};
+// The backward pass with fp32 gradients, or (bf16_grads) with gradients rounded
+// to bf16 at the end: dq by the finalisation, dk and dv by a conversion pass over
+// fp32 copies kept in the workspace, so that every gradient is the fp32 result
+// rounded to nearest even.
+static int bwd_common(const void* q, const void* k, const void* v, const void* out,
+                      const float* lse, const void* dout, void* dq_out, void* dk_out, void* dv_out,
+                      int B, int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode,
+                      float scale, int causal, attn_stream_t stream_, bool bf16_grads) {
+  const void* ptrs[] = {q, k, v, out, lse, dout, dq_out, dk_out, dv_out};
   int st = validate(ptrs, 9, B, Hq, Hkv, S, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
   if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
@@ -298,9 +302,12 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
   const size_t accbytes = round256(static_cast<size_t>(qrows) * D * 4);
   const size_t rowbytes = round256(static_cast<size_t>(qrows) * 4);
   const size_t maxbytes = 256;
+  const size_t gradbytes = bf16_grads ? round256(static_cast<size_t>(krows) * D * 4) : 0;
   uint8_t* ws = nullptr;
   if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
-                              2 * qbytes + 2 * kbytes + accbytes + 2 * rowbytes + maxbytes, d->pool,
+                              2 * qbytes + 2 * kbytes + accbytes + 2 * rowbytes + maxbytes +
+                                  2 * gradbytes,
+                              d->pool,
                               stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   uint8_t* w = ws;
@@ -311,7 +318,10 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
   float* dqacc = reinterpret_cast<float*>(w); w += accbytes;
   float* delta = reinterpret_cast<float*>(w); w += rowbytes;
   float* lse2 = reinterpret_cast<float*>(w); w += rowbytes;
-  float* maxes = reinterpret_cast<float*>(w);
+  float* maxes = reinterpret_cast<float*>(w); w += maxbytes;
+  // fp32 dk, dv: the caller's buffers, or workspace copies rounded to bf16 at the end
+  float* dk = bf16_grads ? reinterpret_cast<float*>(w) : static_cast<float*>(dk_out);
+  float* dv = bf16_grads ? reinterpret_cast<float*>(w + gradbytes) : static_cast<float*>(dv_out);
 
   // Two CTAs per (KV head, key tile), each with half of the group's query heads,
   // when one CTA per key tile would not fill the GPU (and the group splits
@@ -380,12 +390,31 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
   }
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
-    ok = gbattn::launch_dq_finalize(dqacc, dq, qrows, S, D, scale, maxes, cs, sn, inter, stream) ==
-         cudaSuccess;
+    ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, S, D, scale, maxes, cs, sn,
+                                    inter, stream) == cudaSuccess;
+    if (bf16_grads)
+      ok = ok && gbattn::launch_f32_to_bf16(dk, dk_out, krows * D, stream) == cudaSuccess &&
+           gbattn::launch_f32_to_bf16(dv, dv_out, krows * D, stream) == cudaSuccess;
     tm.done();
   }
   cudaFreeAsync(ws, stream);
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
+                int D, float rope_theta, int rope_mode, float scale, int causal,
+                attn_stream_t stream) {
+  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
+                    scale, causal, stream, false);
+}
+
+int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
+                  int D, float rope_theta, int rope_mode, float scale, int causal,
+                  attn_stream_t stream) {
+  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
+                    scale, causal, stream, true);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,

@@ -99,10 +99,13 @@ struct RowPrepParams {
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
-// dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in, fp32 out).
-cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
-                               float scale, const float* maxes, const float* cos_tab,
+// dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in; fp32 out, or bf16 rounded to
+// nearest even when dq_bf16).
+cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
+                               int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream);
+// y = bf16(x) (nearest even), n a multiple of 8.
+cudaError_t launch_f32_to_bf16(const float* x, void* y, long long n, cudaStream_t stream);
 
 // ---------------------------------------------------------------- main kernels
 struct FwdParams {

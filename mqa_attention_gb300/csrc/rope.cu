@@ -236,9 +236,10 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   }
 }
 
-template <int D>
+// dq in fp32, or rounded to bf16 (nearest even) when kBf16.
+template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
-    dq_finalize_kernel(const float* __restrict__ dqacc, float* __restrict__ dq, long long rows,
+    dq_finalize_kernel(const float* __restrict__ dqacc, void* __restrict__ dq, long long rows,
                        int S, float scale, const float* __restrict__ maxes,
                        const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
                        int rope_interleaved) {
@@ -265,8 +266,23 @@ __global__ void __launch_bounds__(256)
     y1[i] *= f;
     y2[i] *= f;
   }
-  store8(dq + e1, y1);
-  store8(dq + e2, y2);
+  if constexpr (kBf16) {
+    store8_bf16(static_cast<__nv_bfloat16*>(dq) + e1, y1);
+    store8_bf16(static_cast<__nv_bfloat16*>(dq) + e2, y2);
+  } else {
+    store8(static_cast<float*>(dq) + e1, y1);
+    store8(static_cast<float*>(dq) + e2, y2);
+  }
+}
+
+// y = bf16(x), nearest even; n a multiple of 8.
+__global__ void __launch_bounds__(256)
+    f32_to_bf16_kernel(const float* __restrict__ x, void* __restrict__ y, long long n8) {
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  float v[8];
+  load8(x + 8 * t, v);
+  store8_bf16(static_cast<__nv_bfloat16*>(y) + 8 * t, v);
 }
 
 long long blocks_for(long long threads) { return (threads + 255) / 256; }
@@ -298,17 +314,29 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_finalize(const float* dqacc, float* dq, long long rows, int S, int D,
-                               float scale, const float* maxes, const float* cos_tab,
+cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
+                               int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
-  if (D == 128)
-    dq_finalize_kernel<128><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
-                                                       sin_tab, rope_interleaved);
-  else
-    dq_finalize_kernel<64><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab,
-                                                      sin_tab, rope_interleaved);
+#define GB_FIN(DD, BF)                                                                         \
+  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab, \
+                                                       sin_tab, rope_interleaved)
+  if (D == 128) {
+    if (dq_bf16) GB_FIN(128, true);
+    else GB_FIN(128, false);
+  } else {
+    if (dq_bf16) GB_FIN(64, true);
+    else GB_FIN(64, false);
+  }
+#undef GB_FIN
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* x, void* y, long long n, cudaStream_t stream) {
+  const long long n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  f32_to_bf16_kernel<<<(unsigned)blocks_for(n8), 256, 0, stream>>>(x, y, n8);
   return cudaGetLastError();
 }
 

@@ -143,6 +143,47 @@ def test_interleaved_differs_from_half_split():
     assert (a["out"] - b["out"]).abs().max().item() > 1e-2
 
 
+BF16_GRADS = [
+    # one CTA per key tile (D = 128), two CTAs per key tile adding dK/dV (G even,
+    # few key tiles), D = 64, and the interleaved layout
+    (1, 8, 2, 1024, 128, True, "half"),
+    (1, 4, 1, 512, 128, True, "half"),
+    (2, 8, 1, 512, 64, True, "half"),
+    (1, 4, 2, 384, 64, False, "interleaved"),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,rope", BF16_GRADS)
+def test_bf16_gradients(B, Hq, Hkv, S, D, causal, rope):
+    """attn_bwd_bf16 writes the fp32 path's gradients rounded to nearest even: dk and
+    dv bit for bit; dq, whose fp32 sum of partial products runs in a run-dependent
+    order, within one bf16 ulp. Against the oracle the bounds grow by half a bf16 ulp
+    of the reference value (the rounding itself)."""
+    wl = Workload(250 + S // 128 + D, "bf16grads", B, Hq, Hkv, S, D,
+                  10000.0 if D == 64 else 500000.0, True, causal)
+    dev, f = gen(wl)
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal, rope=rope)
+    g32 = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                     wl.causal, rope=rope)
+    g16 = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                     wl.causal, rope=rope, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert M.sync_status() == 0
+    assert all(t.dtype == torch.bfloat16 for t in g16)
+    for name, a, b in (("dk", g16[1], g32[1]), ("dv", g16[2], g32[2])):
+        assert torch.equal(a, b.to(torch.bfloat16)), name
+    a, b = g16[0].double(), g32[0].to(torch.bfloat16).double()
+    assert ((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + 1e-12).all(), "dq"
+    want = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta, wl.causal,
+                                rope=rope, round_rotated=True)
+    gmax, gmean = grad_bounds(wl)
+    for name, got, ref in zip(("dq", "dk", "dv"), g16, want):
+        e = (got.double().cpu() - ref).abs()
+        half_ulp = ref.abs() * 2.0 ** -8
+        assert (e <= gmax + half_ulp).all(), f"{name}: max excess {(e - half_ulp).max():.3e}"
+        assert e.mean().item() <= gmean + half_ulp.mean().item(), name
+
+
 def test_tiny_mqa_forward_workload():
     wl = by_index(1)
     dev, f = gen(wl)
