@@ -62,6 +62,9 @@ def parse():
                     help="RoPE pair layout (interleaved runs attn_fwd_ex / attn_bwd_ex)")
     ap.add_argument("--grads", choices=["fp32", "bf16"], default="fp32",
                     help="gradient dtype (bf16 runs attn_bwd_bf16)")
+    ap.add_argument("--blocks", type=int, default=1,
+                    help="N > 1: run the step as N x N query / key-value blocks through "
+                         "attn_fwd_partial, attn_merge and attn_bwd_partial")
     a = ap.parse_args()
     a.warmup = max(3, a.warmup)
     return a
@@ -472,11 +475,133 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_blocks(args, rank, world, local):
+    """The step as a context-parallel block schedule on one GPU: the sequence is cut
+    into N query and N key/value blocks; each query block's partial forwards over
+    the key blocks it can see are merged in place, then every such block pair runs
+    its partial backward. Credited the same causal-pair FLOPs as the full step;
+    device time only (each block's outputs stay on the device)."""
+    import mqa_attention_gb300 as M
+    from mqa_attention_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (GB300)")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    barrier(world)
+    M.lib()
+    wl = by_name(args.workload)
+    nb = args.blocks
+    if wl.S % (nb * 128) or not wl.backward:
+        raise SystemExit("--blocks needs a fwd+bwd workload whose S is a multiple of 128 * N")
+    blk = wl.S // nb
+    host = host_inputs(wl, rank)
+    dev = {n: to_bf16_tensor(h, "cuda") for n, h in host.items()}
+    cut = lambda t, i: t[:, :, i * blk:(i + 1) * blk].contiguous()
+    qb = [cut(dev["q"], i) for i in range(nb)]
+    kb = [cut(dev["k"], i) for i in range(nb)]
+    vb = [cut(dev["v"], i) for i in range(nb)]
+    dob = [cut(dev["dout"], i) for i in range(nb)]
+    pairs = [(i, j) for i in range(nb) for j in range(nb) if not wl.causal or j <= i]
+    outs = [torch.empty_like(qb[i]) for i in range(nb)]
+    lses = [torch.empty((wl.B, wl.Hq, blk), dtype=torch.float32, device="cuda") for _ in range(nb)]
+    po, pl = torch.empty_like(qb[0]), torch.empty_like(lses[0])
+    grads = {p: (torch.empty(qb[0].shape, dtype=torch.float32, device="cuda"),
+                 torch.empty(kb[0].shape, dtype=torch.float32, device="cuda"),
+                 torch.empty(kb[0].shape, dtype=torch.float32, device="cuda")) for p in pairs}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    mode = M.ROPE_MODES[args.rope]
+    D = wl.D
+
+    def step():
+        for i in range(nb):
+            first = True
+            for (a, j) in pairs:
+                if a != i:
+                    continue
+                o, l = (outs[i], lses[i]) if first else (po, pl)
+                M.attn_fwd_partial(qb[i], kb[j], vb[j], o, l, wl.B, wl.Hq, wl.Hkv, blk, blk, D,
+                                   i * blk, j * blk, wl.theta, mode, wl.scale, wl.causal, stream)
+                if not first:
+                    M.attn_merge(outs[i], lses[i], po, pl, outs[i], lses[i], lses[i].numel(), D,
+                                 stream)
+                first = False
+        for (i, j) in pairs:
+            g = grads[(i, j)]
+            M.attn_bwd_partial(qb[i], kb[j], vb[j], outs[i], lses[i], dob[i], g[0], g[1], g[2],
+                               wl.B, wl.Hq, wl.Hkv, blk, blk, D, i * blk, j * blk, wl.theta,
+                               mode, wl.scale, wl.causal, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if M.sync_status() != 0:
+        raise SystemExit("device status error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    M.profile_begin(max(4096, 16 * len(pairs) * args.steps))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    M.profile_end()
+    status = M.sync_status()
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
+    kern = {}
+    for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
+                       (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
+                       (M.KERNEL_DQ_FINAL, "dq_finalize")):
+        n, tot = M.profile_query(kind)
+        if n:
+            kern[name] = tot / args.steps  # ms per step over all blocks
+    sampler.stop()
+    if rank != 0:
+        return
+    peak_tf, _, peak_src = peaks()
+    value = wl.flops * world / (ms * 1e-3) / 1e12
+    achieved = wl.bwd_flops / (kern["attn_bwd_main"] * 1e-3) / 1e12
+    nfwd = sum(1 for _ in pairs)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
+        "config": dict(config_of(wl, world, l2="flushed between steps (256 MiB write)",
+                                 rope=args.rope), blocks=f"{nb} x {nb}", block_rows=blk,
+                       block_pairs=len(pairs)),
+        "e2e": None,
+        "note": "block schedule through the partial entry points; device time only",
+        # per pair: RoPE pre-pass + forward (+ merge), abs-max + pre-pass + main +
+        # dq finalisation
+        "gpu_launches": (2 * nfwd + (nfwd - nb) + 4 * nfwd) * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "attn_bwd_main", "achieved": achieved,
+                     "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "traffic": None, "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "kernels_ms": {n: round(v, 5) for n, v in kern.items()},
+        "cpu_baseline": None,
+        "clocks": sampler.summary(t0, t1),
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.blocks > 1:
+        run_blocks(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -112,6 +112,37 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
                 int D, float rope_theta, int rope_mode, float scale, int causal,
                 attn_stream_t stream);
 
+/* Blocks of queries and keys: the pieces a context-parallel (ring) schedule computes
+ * when the sequence is split across devices or passes (Picotron §上下文并行, with the
+ * 32K-token sequences of Megatron-SP). The query block holds Sq rows per head at
+ * positions q_pos0 + i, the K/V block Skv rows at kv_pos0 + j; RoPE rotates every row
+ * by its own position and the causal mask compares positions. Sq, Skv, q_pos0 and
+ * kv_pos0 are multiples of 128 (else ATTN_ERR_UNSUPPORTED; negative: ATTN_ERR_INVALID).
+ *
+ * attn_fwd_partial: out [B,Hq,Sq,D] bf16 and lse [B,Hq,Sq] fp32 of the attention over
+ *   this K/V block alone; a row that sees none of its keys gets out = 0, lse = -inf.
+ *   attn_fwd_ex(...) is attn_fwd_partial with Sq = Skv = S, q_pos0 = kv_pos0 = 0.
+ * attn_bwd_partial: the contributions of this K/V block to the gradients, given the
+ *   out and lse of the query block's whole attention (merged over every K/V block):
+ *   P_ij = exp(s_ij - lse_i) for this block's keys, delta_i = dout_i . out_i. dq
+ *   [B,Hq,Sq,D] (summed over the K/V blocks by the caller), dk, dv [B,Hkv,Skv,D]
+ *   (summed over the query blocks) are fp32, fully overwritten.
+ * attn_merge: out, lse of the union of two disjoint key sets of the same `rows` query
+ *   rows (B*Hq*Sq) from their partial results: lse = ln(e^lse_a + e^lse_b),
+ *   out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b (bf16 out, fp32 lse); out and
+ *   lse may be out_a and lse_a. */
+int attn_fwd_partial(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                     float rope_theta, int rope_mode, float scale, int causal,
+                     attn_stream_t stream);
+int attn_bwd_partial(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, float* dq, float* dk, float* dv, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                     float rope_theta, int rope_mode, float scale, int causal,
+                     attn_stream_t stream);
+int attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
+               void* out, float* lse, long long rows, int D, attn_stream_t stream);
+
 /* attn_bwd_ex writing bf16 gradients: dq [B,Hq,S,D], dk, dv [B,Hkv,S,D] bf16, each the
  * value attn_bwd_ex writes in fp32 rounded to nearest even (dk and dv bit for bit;
  * dq's fp32 value sums its partial products in a run-dependent order, so it may

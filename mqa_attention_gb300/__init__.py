@@ -23,7 +23,13 @@ __all__ = [
     "attn_fwd_ex",
     "attn_bwd_ex",
     "attn_bwd_bf16",
+    "attn_fwd_partial",
+    "attn_bwd_partial",
+    "attn_merge",
     "forward",
+    "forward_partial",
+    "backward_partial",
+    "merge",
     "backward",
     "sync_status",
     "status_string",
@@ -52,6 +58,9 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_ex",
     "attn_bwd_ex",
     "attn_bwd_bf16",
+    "attn_fwd_partial",
+    "attn_bwd_partial",
+    "attn_merge",
     "attn_sync_status",
     "attn_status_string",
     "attn_profile_begin",
@@ -116,6 +125,14 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_ex.restype = _I
             L.attn_bwd_bf16.argtypes = L.attn_bwd_ex.argtypes
             L.attn_bwd_bf16.restype = _I
+            L.attn_fwd_partial.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                           _F, _I, _F, _I, _P]
+            L.attn_fwd_partial.restype = _I
+            L.attn_bwd_partial.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                           _I, _I, _I, _F, _I, _F, _I, _P]
+            L.attn_bwd_partial.restype = _I
+            L.attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_longlong, _I, _P]
+            L.attn_merge.restype = _I
             _lib = L
         return _lib
 
@@ -199,6 +216,74 @@ def attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_th
                                _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(S),
                                int(D), float(rope_theta), int(rope_mode), float(scale),
                                1 if causal else 0, _stream(stream)), "attn_bwd_bf16")
+
+
+def attn_fwd_partial(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0, rope_theta,
+                     rope_mode, scale, causal, stream=None):
+    """C ABI attn_fwd_partial: attention of a query block over one K/V block."""
+    _check(lib().attn_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B),
+                                  int(Hq), int(Hkv), int(Sq), int(Skv), int(D), int(q_pos0),
+                                  int(kv_pos0), float(rope_theta), int(rope_mode), float(scale),
+                                  1 if causal else 0, _stream(stream)), "attn_fwd_partial")
+
+
+def attn_bwd_partial(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, q_pos0,
+                     kv_pos0, rope_theta, rope_mode, scale, causal, stream=None):
+    """C ABI attn_bwd_partial: one K/V block's gradient contributions."""
+    _check(lib().attn_bwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv),
+                                  int(Sq), int(Skv), int(D), int(q_pos0), int(kv_pos0),
+                                  float(rope_theta), int(rope_mode), float(scale),
+                                  1 if causal else 0, _stream(stream)), "attn_bwd_partial")
+
+
+def attn_merge(out_a, lse_a, out_b, lse_b, out, lse, rows, D, stream=None):
+    """C ABI attn_merge: combine two partial results of the same query rows."""
+    _check(lib().attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
+                            _ptr(lse), int(rows), int(D), _stream(stream)), "attn_merge")
+
+
+def forward_partial(q, k, v, rope_theta, q_pos0, kv_pos0, scale=None, causal=True, stream=None,
+                    rope="half"):
+    """Allocates out / lse and runs attn_fwd_partial. q: [B,Hq,Sq,D], k, v: [B,Hkv,Skv,D]."""
+    import torch
+
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    attn_fwd_partial(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0, rope_theta,
+                     ROPE_MODES[rope], scale, causal, stream)
+    return out, lse
+
+
+def backward_partial(q, k, v, out, lse, dout, rope_theta, q_pos0, kv_pos0, scale=None,
+                     causal=True, stream=None, rope="half"):
+    """Allocates fp32 dq, dk, dv and runs attn_bwd_partial (out, lse: the query
+    block's merged attention)."""
+    import torch
+
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    attn_bwd_partial(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, q_pos0,
+                     kv_pos0, rope_theta, ROPE_MODES[rope], scale, causal, stream)
+    return dq, dk, dv
+
+
+def merge(out_a, lse_a, out_b, lse_b, out=None, lse=None, stream=None):
+    """attn_merge into new tensors, or in place when out / lse are given (they may
+    be out_a / lse_a)."""
+    import torch
+
+    out = torch.empty_like(out_a) if out is None else out
+    lse = torch.empty_like(lse_a) if lse is None else lse
+    attn_merge(out_a, lse_a, out_b, lse_b, out, lse, lse_a.numel(), out_a.shape[-1], stream)
+    return out, lse
 
 
 def _shapes(q, k):

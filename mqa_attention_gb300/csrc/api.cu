@@ -128,6 +128,19 @@ int validate(const void* const* ptrs, int nptr, int B, int Hq, int Hkv, int S, i
   return ATTN_OK;
 }
 
+// Query / K-V block arguments of the partial entry points: Sq, Skv multiples of
+// 128 (checked with the other sizes by validate), positions non-negative
+// multiples of 128, the last position below 2^30.
+int validate_blocks(int Sq, int Skv, int q_pos0, int kv_pos0) {
+  if (Sq <= 0 || Skv <= 0 || q_pos0 < 0 || kv_pos0 < 0) return ATTN_ERR_INVALID;
+  if (static_cast<long long>(q_pos0) + Sq > (1LL << 30) ||
+      static_cast<long long>(kv_pos0) + Skv > (1LL << 30))
+    return ATTN_ERR_INVALID;
+  if (Sq % kTile != 0 || Skv % kTile != 0 || q_pos0 % kTile != 0 || kv_pos0 % kTile != 0)
+    return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
 // Current device's state, initialised on first use. Returns an ATTN_* code.
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -212,21 +225,26 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
-                int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
-                int causal, attn_stream_t stream_) {
+// Forward pass of a query block (Sq rows per head at positions q_pos0..) against
+// a K/V block (Skv rows at kv_pos0..); self-attention is Sq = Skv, both 0.
+static int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                      float rope_theta, int rope_mode, float scale, int causal,
+                      attn_stream_t stream_) {
   const void* ptrs[] = {q, k, v, out, lse};
-  int st = validate(ptrs, 5, B, Hq, Hkv, S, D, rope_theta, scale);
+  int st = validate(ptrs, 5, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
+  if ((st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
   if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   float *cs = nullptr, *sn = nullptr;
-  if ((st = rope_table(d, S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  const int npos = q_pos0 + Sq > kv_pos0 + Skv ? q_pos0 + Sq : kv_pos0 + Skv;
+  if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
 
-  const long long qrows = static_cast<long long>(B) * Hq * S;
-  const long long krows = static_cast<long long>(B) * Hkv * S;
+  const long long qrows = static_cast<long long>(B) * Hq * Sq;
+  const long long krows = static_cast<long long>(B) * Hkv * Skv;
   const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
   uint8_t* ws = nullptr;
@@ -241,12 +259,11 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
     gbattn::RowPrepParams rp{};
     rp.bwd = 0;
     rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
-    rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
-    rp.seg[0] = {q, qr, nullptr, nullptr, qrows};
-    rp.seg[1] = {k, kr, nullptr, nullptr, krows};
+    rp.seg[0] = {q, qr, nullptr, nullptr, qrows, Sq, q_pos0};
+    rp.seg[1] = {k, kr, nullptr, nullptr, krows, Skv, kv_pos0};
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
     ok = gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
@@ -255,9 +272,12 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
   ok = ok && make_map(&fp.map_q, qr, qrows, D, kTile) && make_map(&fp.map_k, kr, krows, D, kTile) &&
        make_map(&fp.map_v, v, krows, D, kTile) && make_map(&fp.map_out, out, qrows, D, kTile);
   if (ok) {
+    fp.out = out;
     fp.lse = lse;
     fp.status = d->status;
-    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.S = S; fp.D = D;
+    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.Sq = Sq; fp.Skv = Skv; fp.D = D;
+    fp.q_tile0 = q_pos0 / kTile;
+    fp.kv_tile0 = kv_pos0 / kTile;
     fp.scale_log2 = scale * 1.4426950408889634f;
     fp.causal = causal ? 1 : 0;
     fp.inject_timeout = g_inject_timeout ? 1 : 0;
@@ -267,6 +287,21 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
   }
   cudaFreeAsync(ws, stream);
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
+                int causal, attn_stream_t stream) {
+  return fwd_common(q, k, v, out, lse, B, Hq, Hkv, S, S, D, 0, 0, rope_theta, rope_mode, scale,
+                    causal, stream);
+}
+
+int attn_fwd_partial(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                     float rope_theta, int rope_mode, float scale, int causal,
+                     attn_stream_t stream) {
+  return fwd_common(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0, rope_theta,
+                    rope_mode, scale, causal, stream);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -282,21 +317,24 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 // rounded to nearest even.
 static int bwd_common(const void* q, const void* k, const void* v, const void* out,
                       const float* lse, const void* dout, void* dq_out, void* dk_out, void* dv_out,
-                      int B, int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode,
-                      float scale, int causal, attn_stream_t stream_, bool bf16_grads) {
+                      int B, int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                      float rope_theta, int rope_mode, float scale, int causal,
+                      attn_stream_t stream_, bool bf16_grads) {
   const void* ptrs[] = {q, k, v, out, lse, dout, dq_out, dk_out, dv_out};
-  int st = validate(ptrs, 9, B, Hq, Hkv, S, D, rope_theta, scale);
+  int st = validate(ptrs, 9, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
+  if ((st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
   if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
   const int inter = rope_mode == ATTN_ROPE_INTERLEAVED;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   float *cs = nullptr, *sn = nullptr;
-  if ((st = rope_table(d, S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  const int npos = q_pos0 + Sq > kv_pos0 + Skv ? q_pos0 + Sq : kv_pos0 + Skv;
+  if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
 
-  const long long qrows = static_cast<long long>(B) * Hq * S;
-  const long long krows = static_cast<long long>(B) * Hkv * S;
+  const long long qrows = static_cast<long long>(B) * Hq * Sq;
+  const long long krows = static_cast<long long>(B) * Hkv * Skv;
   const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
   const size_t accbytes = round256(static_cast<size_t>(qrows) * D * 4);
@@ -330,7 +368,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const long long key_tiles = static_cast<long long>(B) * Hkv * (S / kTile);
+  const long long key_tiles = static_cast<long long>(B) * Hkv * (Skv / kTile);
   const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
   bool ok = true;
   {
@@ -346,13 +384,12 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     gbattn::RowPrepParams rp{};
     rp.bwd = 1;
     rp.rope_interleaved = inter;
-    rp.S = S;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
     rp.maxes = maxes;
-    rp.seg[0] = {q, qr, dout, dos, qrows};
-    rp.seg[1] = {k, kr, v, vs, krows};
+    rp.seg[0] = {q, qr, dout, dos, qrows, Sq, q_pos0};
+    rp.seg[1] = {k, kr, v, vs, krows, Skv, kv_pos0};
     rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
     if (hsplit > 1) {  // the main kernel adds dK/dV partials of two CTAs
       rp.dk_zero = dk;
@@ -377,7 +414,9 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     bp.cos_tab = cs;
     bp.sin_tab = sn;
     bp.status = d->status;
-    bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.S = S; bp.D = D;
+    bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.Sq = Sq; bp.Skv = Skv; bp.D = D;
+    bp.q_tile0 = q_pos0 / kTile;
+    bp.kv_tile0 = kv_pos0 / kTile;
     bp.scale = scale;
     bp.scale_log2 = scale * 1.4426950408889634f;
     bp.causal = causal ? 1 : 0;
@@ -390,7 +429,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   }
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
-    ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, S, D, scale, maxes, cs, sn,
+    ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, Sq, q_pos0, D, scale, maxes,
+                                    cs, sn,
                                     inter, stream) == cudaSuccess;
     if (bf16_grads)
       ok = ok && gbattn::launch_f32_to_bf16(dk, dk_out, krows * D, stream) == cudaSuccess &&
@@ -405,16 +445,25 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
                 const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
                 int D, float rope_theta, int rope_mode, float scale, int causal,
                 attn_stream_t stream) {
-  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
-                    scale, causal, stream, false);
+  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, S, D, 0, 0, rope_theta,
+                    rope_mode, scale, causal, stream, false);
+}
+
+int attn_bwd_partial(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, float* dq, float* dk, float* dv, int B,
+                     int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
+                     float rope_theta, int rope_mode, float scale, int causal,
+                     attn_stream_t stream) {
+  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0,
+                    rope_theta, rope_mode, scale, causal, stream, false);
 }
 
 int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int S,
                   int D, float rope_theta, int rope_mode, float scale, int causal,
                   attn_stream_t stream) {
-  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, rope_mode,
-                    scale, causal, stream, true);
+  return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, S, D, 0, 0, rope_theta,
+                    rope_mode, scale, causal, stream, true);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
@@ -422,6 +471,22 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              int D, float rope_theta, float scale, int causal, attn_stream_t stream) {
   return attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
                      ATTN_ROPE_HALF, scale, causal, stream);
+}
+
+int attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
+               void* out, float* lse, long long rows, int D, attn_stream_t stream_) {
+  const void* ptrs[] = {out_a, lse_a, out_b, lse_b, out, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return ATTN_ERR_INVALID;
+  if (rows <= 0 || rows >= (1LL << 31)) return ATTN_ERR_INVALID;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != ATTN_OK) return st;
+  return gbattn::launch_merge(out_a, lse_a, out_b, lse_b, out, lse, rows, D,
+                              reinterpret_cast<cudaStream_t>(stream_)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
 }
 
 int attn_sync_status(attn_stream_t stream_) {

@@ -129,17 +129,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const int G = p.Hq / p.Hkv;
   const int Gc = G / p.hsplit;  // query heads of this CTA
   const int h_first = hkv * G + part * Gc;
-  const int k0 = kt * kTile;
-  const int kv_row = bhk * p.S + k0;
-  const int nqt = p.S / BQ;
-  const int qt_begin = p.causal ? k0 / BQ : 0;
-  const int per_head = nqt - qt_begin;  // even: S and k0 are multiples of 128
-  const int n = Gc * per_head;
+  const int k0 = kt * kTile;                  // first key row of the tile in the block
+  const int k0p = (p.kv_tile0 + kt) * kTile;  // its position
+  const int q0p = p.q_tile0 * kTile;          // position of the query block's first row
+  const int kv_row = bhk * p.Skv + k0;
+  const int nqt = p.Sq / BQ;
+  // causal: the query tiles at or after the key tile's position
+  int qt_begin = p.causal ? (k0p - q0p) / BQ : 0;
+  qt_begin = qt_begin < 0 ? 0 : (qt_begin > nqt ? nqt : qt_begin);
+  const int per_head = nqt - qt_begin;  // even: Sq and the offsets are multiples of 128
+  const int n = Gc * per_head;          // 0: no query of the block sees these keys
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
     const int h = h_first + s / per_head;
-    return (b * p.Hq + h) * p.S + step_qt(s) * BQ;
+    return (b * p.Hq + h) * p.Sq + step_qt(s) * BQ;
   };
 
   // ---- setup
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     // Sᵀ arrives multiplied by 2^(eq+ek), dPᵀ and delta by 2^(edo+ev)
     const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
-    const int key = k0 + r;
+    const int key = k0p + r;  // this thread's key position
     const int qb = half * 32;  // this half's first query column
     for (int s = 0; s < n; ++s) {
       const int buf = s & 1;
@@ -415,13 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const float4* lse4 =
           reinterpret_cast<const float4*>(sgen + (st - sbase) + 2 * C::kQTileBytes) + qb / 4;
       const float4* del4 = lse4 + BQ / 4;
-      const int q0 = step_qt(s) * BQ;
+      const int q0 = q0p + step_qt(s) * BQ;  // position of the step's first query
       uint32_t sv[32], dpv[32];
       tmem_ld32x2(tmem + lane_base + C::col_st(buf) + qb, tmem + lane_base + C::col_dpt(buf) + qb,
                   sv, dpv);
       uint32_t pk[16], dk[16];
       // keys after the query are masked on the diagonal steps only
-      const int lim = (p.causal && q0 < k0 + kTile) ? key - q0 - qb : -1;
+      const int lim = (p.causal && q0 < k0p + kTile) ? key - q0 - qb : -1;
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         const float4 l4 = lse4[g];
@@ -463,7 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tc_fence_after();
     const long long grow = kv_row + r;
     const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
-    if (half == 0) {
+    if (n == 0) {
+      // no query of the block sees these keys: dk = dv = 0 (summed rows start at 0)
+      if (!sum_parts) {
+        float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dv : p.dk) + grow * D);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else if (half == 0) {
       // dV accumulated Pᵀ (dO 2^edo)
       const float f = exp2i(-ex.dout);
       float* dst = p.dv + grow * D;
@@ -553,7 +564,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((p.S / kTile) * p.B * p.Hkv * p.hsplit);
+  const unsigned grid = static_cast<unsigned>((p.Skv / kTile) * p.B * p.Hkv * p.hsplit);
   attn_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
   // ---- work item: heaviest query-tile pairs first
-  const int nq = p.S / kTile;
+  const int nq = p.Sq / kTile;
+  const int nkv = p.Skv / kTile;
   const int npairs = (nq + 1) / 2;
   const int BH = p.B * p.Hq;
   const int c = npairs - 1 - static_cast<int>(blockIdx.x) / BH;
@@ -85,16 +86,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int b = bh / p.Hq;
   const int h = bh % p.Hq;
   const int hkv = h / (p.Hq / p.Hkv);
-  // KV tiles seen by query tile 2c + t (0 when that tile is past the end)
+  // KV tiles seen by query tile 2c + t: those at or before its position when
+  // causal (0 when that tile is past the end, or precedes the whole K/V block)
   auto tiles_of = [&](int t) {
     const int qt = 2 * c + t;
-    return qt < nq ? (p.causal ? qt + 1 : nq) : 0;
+    if (qt >= nq) return 0;
+    if (!p.causal) return nkv;
+    const int vis = p.q_tile0 + qt - p.kv_tile0 + 1;
+    return vis < 0 ? 0 : (vis > nkv ? nkv : vis);
   };
   const int n_0 = tiles_of(0);
   const int n_1 = tiles_of(1);
   const int n = n_0 > n_1 ? n_0 : n_1;
-  const int q_row0 = bh * p.S;
-  const int kv_row0 = (b * p.Hkv + hkv) * p.S;
+  const int q_row0 = bh * p.Sq;
+  const int kv_row0 = (b * p.Hkv + hkv) * p.Skv;
 
   // ---- setup
   if (warp == kWarpMma) {
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (p.inject_timeout)  // nothing ever arrives on bar_never
       ok = wait(smem_u32(&bar_never), 0, kSiteInject);
     ok = ok && wait(smem_u32(&bar_q), 0, kSiteQ);
-    ok = ok && wait_kv(0);
+    ok = ok && n > 0 && wait_kv(0);  // n = 0: both query tiles see no key of the block
     if (ok) {
       tc_fence_after();
       for (int t = 0; t < 2; ++t) {
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           s[cc * 64 + 32 + i] = __uint_as_float(w[i]);
         }
       }
-      if (p.causal && j == qt) {  // diagonal tile: keys after the query are masked
+      if (p.causal && p.kv_tile0 + j == p.q_tile0 + qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = i > r ? -INFINITY : s[i];
       }
@@ -350,6 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         bulk_wait_read_all();
       }
       p.lse[static_cast<long long>(q_row0) + qt * kTile + r] = (m + log2f(l)) * kLn2;
+    } else if (qt < nq) {
+      // a query tile that sees no key of the block: out = 0, lse = -inf
+      const long long row = static_cast<long long>(q_row0) + qt * kTile + r;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * D);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[row] = -INFINITY;
     }
   }
 
@@ -367,7 +379,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int nq = p.S / kTile;
+  const int nq = p.Sq / kTile;
   const unsigned grid = static_cast<unsigned>(((nq + 1) / 2) * p.B * p.Hq);
   attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();

@@ -80,12 +80,14 @@ struct RowSegment {
   const void* x2;  // backward: dout (query rows) or v (key rows)
   void* y2;
   long long rows;
+  int S;     // rows per head; row r sits at position pos0 + r % S
+  int pos0;
 };
 struct RowPrepParams {
   int bwd;
   int rope_interleaved;  // 0: half-split pairs (i, i + D/2); 1: pairs (2i, 2i + 1)
   RowSegment seg[2];
-  int S, D;
+  int D;
   const float* cos_tab;
   const float* sin_tab;
   const float* maxes;  // backward
@@ -100,10 +102,14 @@ struct RowPrepParams {
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
 // dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in; fp32 out, or bf16 rounded to
-// nearest even when dq_bf16).
+// nearest even when dq_bf16); row r sits at position pos0 + r % S.
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
-                               int D, float scale, const float* maxes, const float* cos_tab,
+                               int pos0, int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream);
+// Merge of two partial attention results of the same rows (bf16 out, fp32 lse);
+// o / l may be oa / la.
+cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb, void* o,
+                         float* l, long long rows, int D, cudaStream_t stream);
 // y = bf16(x) (nearest even), n a multiple of 8.
 cudaError_t launch_f32_to_bf16(const float* x, void* y, long long n, cudaStream_t stream);
 
@@ -113,9 +119,13 @@ struct FwdParams {
   CUtensorMap map_k;    // rotated k (bf16), box {64, 128}
   CUtensorMap map_v;    // v (bf16), box {64, 128}
   CUtensorMap map_out;  // out (bf16), box {64, 128}
+  void* out;            // the same rows, for query tiles that see no key
   float* lse;
   int* status;
-  int B, Hq, Hkv, S, D;
+  // Query block of Sq rows per head at positions 128*q_tile0 + i; K/V block of Skv
+  // rows at 128*kv_tile0 + j (self-attention: Sq = Skv = S, both tiles 0).
+  int B, Hq, Hkv, Sq, Skv, D;
+  int q_tile0, kv_tile0;
   float scale_log2;  // scale * log2(e)
   int causal;
   int inject_timeout;
@@ -136,7 +146,8 @@ struct BwdParams {
   const float* cos_tab;
   const float* sin_tab;
   int* status;
-  int B, Hq, Hkv, S, D;
+  int B, Hq, Hkv, Sq, Skv, D;  // query and K/V blocks as in FwdParams
+  int q_tile0, kv_tile0;
   float scale;
   float scale_log2;
   int causal;

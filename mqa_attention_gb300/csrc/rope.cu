@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   // part in the shuffles below and write nothing.
   const bool live = row0 < sg.rows;
   const long long r = live ? row0 : 0;
-  const int pos = static_cast<int>(r % p.S);
+  const int pos = sg.pos0 + static_cast<int>(r % sg.S);
   const bool inter = p.rope_interleaved != 0;
   const long long e1 = r * D + rope_off_a(c, inter);
   const long long e2 = r * D + rope_off_b(c, D, inter);
@@ -206,12 +206,12 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
       store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + e2, a2, s_x2);
     }
     // delta for query rows. Every thread computes it and takes part in the
-    // shuffle (a warp may straddle the query/key boundary); key rows read an
-    // in-bounds row of `out` (there are no more key rows than query rows) and
-    // write nothing.
+    // shuffle (a warp may straddle the query/key boundary); key rows read row 0
+    // of `out` and write nothing.
     float o1[8], o2[8];
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e1, o1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + e2, o2);
+    const long long eo = is_q ? 0 : r * D;
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e1 - eo), o1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e2 - eo), o2);
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
     dq_finalize_kernel(const float* __restrict__ dqacc, void* __restrict__ dq, long long rows,
-                       int S, float scale, const float* __restrict__ maxes,
+                       int S, int pos0, float scale, const float* __restrict__ maxes,
                        const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
                        int rope_interleaved) {
   constexpr int T = D / 16;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(256)
   const long long row = t / T;
   if (row >= rows) return;
   const int c = static_cast<int>(t % T);
-  const int pos = static_cast<int>(row % S);
+  const int pos = pos0 + static_cast<int>(row % S);
   const bool inter = rope_interleaved != 0;
   const long long e1 = row * D + rope_off_a(c, inter);
   const long long e2 = row * D + rope_off_b(c, D, inter);
@@ -273,6 +273,44 @@ __global__ void __launch_bounds__(256)
     store8(static_cast<float*>(dq) + e1, y1);
     store8(static_cast<float*>(dq) + e2, y2);
   }
+}
+
+// Merge of two partial attention results over disjoint key sets of the same
+// query rows: lse = ln(e^lse_a + e^lse_b), out = e^(lse_a - lse) out_a +
+// e^(lse_b - lse) out_b (a row with lse_a = lse_b = -inf gets out = 0, lse = -inf).
+// One thread per 8 elements of a row; the D/8 threads of a row share a warp and
+// read everything before any of them writes, so out / lse may be out_a / lse_a.
+template <int D>
+__global__ void __launch_bounds__(256)
+    merge_kernel(const void* oa, const float* la, const void* ob, const float* lb, void* o,
+                 float* l, long long rows) {
+  constexpr int T = D / 8;
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = t / T;
+  const int c = static_cast<int>(t % T);
+  const bool live = row < rows;
+  const long long rr = live ? row : 0;
+  const float a = la[rr], b = lb[rr];
+  float xa[8], xb[8];
+  load8_bf16(static_cast<const __nv_bfloat16*>(oa) + rr * D + 8 * c, xa);
+  load8_bf16(static_cast<const __nv_bfloat16*>(ob) + rr * D + 8 * c, xb);
+  __syncwarp();
+  if (!live) return;
+  const float m = fmaxf(a, b);
+  float wa = 0.f, wb = 0.f, lse = -INFINITY;
+  if (m != -INFINITY) {
+    wa = expf(a - m);
+    wb = expf(b - m);
+    const float sum = wa + wb;
+    lse = m + logf(sum);
+    wa /= sum;
+    wb /= sum;
+  }
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = wa * xa[i] + wb * xb[i];
+  store8_bf16(static_cast<__nv_bfloat16*>(o) + row * D + 8 * c, y);
+  if (c == 0) l[row] = lse;
 }
 
 // y = bf16(x), nearest even; n a multiple of 8.
@@ -315,13 +353,13 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
-                               int D, float scale, const float* maxes, const float* cos_tab,
+                               int pos0, int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
-#define GB_FIN(DD, BF)                                                                         \
-  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, scale, maxes, cos_tab, \
-                                                       sin_tab, rope_interleaved)
+#define GB_FIN(DD, BF)                                                                   \
+  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, pos0, scale, maxes, \
+                                                       cos_tab, sin_tab, rope_interleaved)
   if (D == 128) {
     if (dq_bf16) GB_FIN(128, true);
     else GB_FIN(128, false);
@@ -330,6 +368,14 @@ cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long 
     else GB_FIN(64, false);
   }
 #undef GB_FIN
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb, void* o,
+                         float* l, long long rows, int D, cudaStream_t stream) {
+  const unsigned grid = (unsigned)blocks_for(rows * (D / 8));
+  if (D == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
+  else merge_kernel<64><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
   return cudaGetLastError();
 }
 

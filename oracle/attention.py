@@ -56,6 +56,9 @@ __all__ = [
     "attention_backward",
     "forward_rows",
     "backward_dq_rows",
+    "attention_forward_partial",
+    "attention_backward_partial",
+    "merge_partials",
     "backward_dkdv_keys",
 ]
 
@@ -297,3 +300,89 @@ def backward_dkdv_keys(q, k, v, dout, keys, scale, theta, causal=True, round_rot
                     dv[bi, gi, sel] += p[:, ks].T @ dout[b, h, rows]
     dk = rope_half_split(dkr, ang[keys], inverse=True)
     return dk, dv
+
+
+# ------------------------------------- a query block against one key/value block
+def attention_forward_partial(q, k, v, scale, theta, q_pos0, kv_pos0, causal=True, rope="half",
+                              round_rotated=False):
+    """Attention of a query block over one key/value block, the piece a
+    context-parallel / ring schedule computes per block ([Picotron] §上下文并行).
+    Query row i sits at position q_pos0 + i, key row j at kv_pos0 + j; RoPE
+    rotates each row by its own position and the causal mask excludes keys
+    after the query's position. Over the visible keys of row i:
+        lse_i = ln sum_j exp(s_ij),   out_i = sum_j exp(s_ij - lse_i) v_j;
+    a row with no visible key has lse_i = -inf and out_i = 0.
+
+    q: [B, Hq, Sq, D]; k, v: [B, Hkv, Skv, D]."""
+    q, k, v = _t(q), _t(k), _t(v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    qr = _maybe_round(_rotate(q, rope_angles(Sq, D, theta, q_pos0), rope), round_rotated)
+    kr = _maybe_round(_rotate(k, rope_angles(Skv, D, theta, kv_pos0), rope), round_rotated)
+    qpos = q_pos0 + torch.arange(Sq)
+    kpos = kv_pos0 + torch.arange(Skv)
+    out = torch.zeros((B, Hq, Sq, D), dtype=F64)
+    lse = torch.full((B, Hq, Sq), float("-inf"), dtype=F64)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            s = scale * (qr[b, h] @ kr[b, g].T)
+            if causal:
+                s = s.masked_fill(kpos[None, :] > qpos[:, None], float("-inf"))
+            vis = torch.isfinite(s).any(dim=1)
+            if vis.any():
+                p, lse[b, h, vis] = _softmax_rows(s[vis])
+                out[b, h, vis] = p @ v[b, g]
+    return out, lse
+
+
+def attention_backward_partial(q, k, v, dout, out, lse, scale, theta, q_pos0, kv_pos0,
+                               causal=True, rope="half", round_rotated=False):
+    """Contributions of one key/value block to the gradients of the whole
+    attention of a query block, given that attention's out and lse (over all
+    key blocks): for this block's keys P_ij = exp(s_ij - lse_i), and with
+    delta_i = dO_i . out_i the steps of attention_backward follow. Summed over
+    the key blocks, dq is the full dq; a block's dk and dv, summed over the
+    query blocks, are its rows of the full dk and dv.
+    Returns (dq [B,Hq,Sq,D], dk, dv [B,Hkv,Skv,D])."""
+    q, k, v, dout, out, lse = _t(q), _t(k), _t(v), _t(dout), _t(out), _t(lse)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    qang = rope_angles(Sq, D, theta, q_pos0)
+    kang = rope_angles(Skv, D, theta, kv_pos0)
+    qr = _maybe_round(_rotate(q, qang, rope), round_rotated)
+    kr = _maybe_round(_rotate(k, kang, rope), round_rotated)
+    qpos = q_pos0 + torch.arange(Sq)
+    kpos = kv_pos0 + torch.arange(Skv)
+    dqr = torch.zeros_like(q)
+    dkr = torch.zeros_like(k)
+    dv = torch.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            s = scale * (qr[b, h] @ kr[b, g].T)
+            if causal:
+                s = s.masked_fill(kpos[None, :] > qpos[:, None], float("-inf"))
+            p = torch.exp(s - lse[b, h][:, None])
+            p = torch.nan_to_num(p, nan=0.0)  # rows with lse = -inf see no key
+            dp = dout[b, h] @ v[b, g].T
+            delta = (dout[b, h] * out[b, h]).sum(dim=1)
+            ds = p * (dp - delta[:, None])
+            dqr[b, h] = scale * (ds @ kr[b, g])
+            dkr[b, g] += scale * (ds.T @ qr[b, h])
+            dv[b, g] += p.T @ dout[b, h]
+    return _rotate(dqr, qang, rope, inverse=True), _rotate(dkr, kang, rope, inverse=True), dv
+
+
+def merge_partials(out_a, lse_a, out_b, lse_b):
+    """The attention over the union of two disjoint key sets from the two
+    partial results: with lse = ln(exp(lse_a) + exp(lse_b)),
+        out = exp(lse_a - lse) out_a + exp(lse_b - lse) out_b
+    (rows that see no key in either: lse = -inf, out = 0)."""
+    out_a, lse_a, out_b, lse_b = _t(out_a), _t(lse_a), _t(out_b), _t(lse_b)
+    lse = torch.logaddexp(lse_a, lse_b)
+    wa = torch.nan_to_num(torch.exp(lse_a - lse), nan=0.0)
+    wb = torch.nan_to_num(torch.exp(lse_b - lse), nan=0.0)
+    return wa[..., None] * out_a + wb[..., None] * out_b, lse

@@ -106,3 +106,16 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(M, "LIB_PATH", "/nonexistent/libmqa_attention_gb300.so")
     with pytest.raises(RuntimeError, match="not built"):
         M.lib()
+
+
+def test_partial_entry_points_reject_unaligned_blocks(built_lib):
+    """Blocks and their positions are multiples of 128; negative positions are invalid."""
+    lib = built_lib
+    f = lambda sq, skv, qp, kp: lib.attn_fwd_partial(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, sq,
+                                                     skv, 64, qp, kp, 10000.0, 0, 0.125, 1, None)
+    assert f(128, 256, 64, 0) == M.ATTN_ERR_UNSUPPORTED
+    assert f(128, 200, 0, 0) == M.ATTN_ERR_UNSUPPORTED
+    assert f(128, 128, -128, 0) == M.ATTN_ERR_INVALID
+    assert lib.attn_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, None) == M.ATTN_ERR_INVALID
+    assert lib.attn_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 96, None) == \
+        M.ATTN_ERR_UNSUPPORTED

@@ -325,3 +325,63 @@ def test_sampled_rows_match_full():
                                       kv_heads=[1], row_block=16)
     assert torch.allclose(dk_k[:, 0], dk[:, 1][:, keys], atol=1e-12)
     assert torch.allclose(dv_k[:, 0], dv[:, 1][:, keys], atol=1e-12)
+
+
+# ------------------------------------------- query / key-value blocks (context parallel)
+def test_partial_over_the_whole_range_is_the_full_attention():
+    """One block holding every query and key (positions from 0) is the plain
+    attention, forward and backward."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 10, 8
+    q, k, v, do = qkvd(B, Hq, Hkv, S, D, seed=81)
+    for causal in (True, False):
+        out, lse = O.attention_forward(q, k, v, 0.4, 10000.0, causal)
+        po, pl = O.attention_forward_partial(q, k, v, 0.4, 10000.0, 0, 0, causal)
+        assert torch.allclose(po, out, atol=1e-13) and torch.allclose(pl, lse, atol=1e-13)
+        full = O.attention_backward(q, k, v, do, 0.4, 10000.0, causal)
+        part = O.attention_backward_partial(q, k, v, do, out, lse, 0.4, 10000.0, 0, 0, causal)
+        for a, b in zip(part, full):
+            assert torch.allclose(a, b, atol=1e-12)
+
+
+@pytest.mark.parametrize("rope", ["half", "interleaved"])
+def test_blocks_merge_to_the_full_attention(rope):
+    """Queries and keys cut into two blocks each (a 2 x 2 ring schedule): merging
+    each query block's partial results over the key blocks gives the full out and
+    lse; the partial gradients, summed over the other blocks, give the full dq,
+    dk, dv."""
+    B, Hq, Hkv, S, D, cut = 1, 2, 1, 12, 8, 5
+    q, k, v, do = qkvd(B, Hq, Hkv, S, D, seed=91)
+    out, lse = O.attention_forward(q, k, v, 0.3, 10000.0, True, rope=rope)
+    dq, dk, dv = O.attention_backward(q, k, v, do, 0.3, 10000.0, True, rope=rope)
+    blocks = [(0, cut), (cut, S)]
+    got_dq = torch.zeros_like(dq)
+    got_dk = torch.zeros_like(dk)
+    got_dv = torch.zeros_like(dv)
+    for q0, q1 in blocks:
+        merged = None
+        for k0, k1 in blocks:
+            po, pl = O.attention_forward_partial(q[:, :, q0:q1], k[:, :, k0:k1], v[:, :, k0:k1],
+                                                 0.3, 10000.0, q0, k0, True, rope=rope)
+            merged = (po, pl) if merged is None else O.merge_partials(*merged, po, pl)
+            g = O.attention_backward_partial(q[:, :, q0:q1], k[:, :, k0:k1], v[:, :, k0:k1],
+                                             do[:, :, q0:q1], out[:, :, q0:q1], lse[:, :, q0:q1],
+                                             0.3, 10000.0, q0, k0, True, rope=rope)
+            got_dq[:, :, q0:q1] += g[0]
+            got_dk[:, :, k0:k1] += g[1]
+            got_dv[:, :, k0:k1] += g[2]
+        assert torch.allclose(merged[0], out[:, :, q0:q1], atol=1e-13)
+        assert torch.allclose(merged[1], lse[:, :, q0:q1], atol=1e-13)
+    for a, b in ((got_dq, dq), (got_dk, dk), (got_dv, dv)):
+        assert torch.allclose(a, b, atol=1e-12)
+
+
+def test_query_block_before_every_key_sees_nothing():
+    """Under the causal mask, queries earlier than the whole key block attend to
+    nothing: lse = -inf, out = 0, and the block contributes no gradient."""
+    B, Hq, Hkv, D = 1, 2, 1, 4
+    q, k, v, do = qkvd(B, Hq, Hkv, 3, D, seed=97)
+    po, pl = O.attention_forward_partial(q, k, v, 0.5, 10000.0, 0, 3, True)
+    assert torch.isneginf(pl).all() and (po == 0).all()
+    g = O.attention_backward_partial(q, k, v, do, torch.zeros_like(po), pl, 0.5, 10000.0, 0, 3,
+                                     True)
+    assert all((t == 0).all() for t in g)
