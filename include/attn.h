@@ -30,8 +30,11 @@
  *   RoPE     half-split: for i < D/2, angle = p * theta^(-2i/D) at position p = 0..S-1;
  *            y_i = x_i cos - x_{i+D/2} sin, y_{i+D/2} = x_{i+D/2} cos + x_i sin.
  *            The rotated q and k are rounded to bf16 before the score product.
- *   Sizes    D in {64, 128}; S a positive multiple of 128; Hq a multiple of Hkv;
- *            B * Hq * S < 2^31.
+ *   Sizes    D in {64, 128}; S > 0 (the kernels work in 128-row tiles: for an S that is
+ *            not a multiple of 128 they run on copies padded to whole tiles, with the
+ *            padding rows contributing nothing, and copy the valid rows out, at the
+ *            cost of those extra passes); Hq a multiple of Hkv;
+ *            B * Hq * S < 2^31 (with S rounded up to a multiple of 128).
  *   Pointers device pointers, 16-byte aligned, not aliasing one another. The caller owns
  *            every buffer; the library never frees or keeps them.
  *   Stream   all work is enqueued on `stream` (a cudaStream_t, or 0); no call
@@ -58,7 +61,8 @@ enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID = 1,     /* null / misaligned pointer, non-positive size, Hq % Hkv != 0,
                                non-finite or non-positive scale or theta, size overflow */
-  ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, S % 128 != 0, or device is not sm_103 */
+  ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, a partial block or position not a multiple
+                               of 128, or device is not sm_103 */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (see attn_sync_status) */
 };
@@ -195,7 +199,8 @@ const char* attn_version(void);
 /* Forward pass that allocates nothing (no counterpart on the source pages: it exists
  * for callers of this library that may not allocate GPU memory, e.g. services that
  * reserve all device memory up front or runtimes that own the allocator).
- * Arguments, layouts, results and argument errors are those of attn_fwd. Instead of
+ * Arguments, layouts, results and argument errors are those of attn_fwd, except that
+ * S must be a multiple of 128 (else ATTN_ERR_UNSUPPORTED). Instead of
  * attn_fwd's pooled workspace and cached RoPE tables it uses one fixed array of
  * ATTN_FWD_NOALLOC_SCRATCH_BYTES in device memory that the CUDA runtime reserves on
  * every GPU where the library's code is loaded and keeps until the process exits.

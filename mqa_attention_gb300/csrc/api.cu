@@ -124,9 +124,10 @@ int validate(const void* const* ptrs, int nptr, int B, int Hq, int Hkv, int S, i
     return ATTN_ERR_INVALID;
   if (static_cast<long long>(B) * Hq * S >= (1LL << 31)) return ATTN_ERR_INVALID;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (S % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
+
+int round_tile(int S) { return (S + kTile - 1) / kTile * kTile; }
 
 // Query / K-V block arguments of the partial entry points: Sq, Skv multiples of
 // 128 (checked with the other sizes by validate), positions non-negative
@@ -227,32 +228,50 @@ const char* attn_status_string(int status) {
 
 // Forward pass of a query block (Sq rows per head at positions q_pos0..) against
 // a K/V block (Skv rows at kv_pos0..); self-attention is Sq = Skv, both 0.
+// A self-attention call (ragged = true: Sq = Skv = S, offsets 0) may have any S:
+// the main kernels then work on copies padded to whole 128-row tiles, and the
+// valid rows of out / lse are copied into the caller's buffers at the end.
 static int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                       int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
                       float rope_theta, int rope_mode, float scale, int causal,
-                      attn_stream_t stream_) {
+                      attn_stream_t stream_, bool ragged) {
   const void* ptrs[] = {q, k, v, out, lse};
   int st = validate(ptrs, 5, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
-  if ((st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
+  if (!ragged && (st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
   if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   float *cs = nullptr, *sn = nullptr;
-  const int npos = q_pos0 + Sq > kv_pos0 + Skv ? q_pos0 + Sq : kv_pos0 + Skv;
+  // Table rows for every position a kernel reads, the padding rows of a ragged
+  // sequence included (they are rotated like any row, and then ignored).
+  const int npos = q_pos0 + round_tile(Sq) > kv_pos0 + round_tile(Skv) ? q_pos0 + round_tile(Sq)
+                                                                        : kv_pos0 + round_tile(Skv);
   if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
 
+  const int Sqp = round_tile(Sq), Skvp = round_tile(Skv);  // rows per head the kernels see
+  const bool padded = Sqp != Sq || Skvp != Skv;
+  if (static_cast<long long>(B) * Hq * Sqp >= (1LL << 31) ||
+      static_cast<long long>(B) * Hkv * Skvp >= (1LL << 31))
+    return ATTN_ERR_INVALID;
   const long long qrows = static_cast<long long>(B) * Hq * Sq;
-  const long long krows = static_cast<long long>(B) * Hkv * Skv;
-  const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
-  const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
+  const long long qrows_p = static_cast<long long>(B) * Hq * Sqp;
+  const long long krows_p = static_cast<long long>(B) * Hkv * Skvp;
+  const size_t qbytes = round256(static_cast<size_t>(qrows_p) * D * 2);
+  const size_t kbytes = round256(static_cast<size_t>(krows_p) * D * 2);
+  const size_t lbytes = padded ? round256(static_cast<size_t>(qrows_p) * 4) : 0;
   uint8_t* ws = nullptr;
-  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), qbytes + kbytes, d->pool, stream) !=
-      cudaSuccess)
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
+                              qbytes + kbytes + (padded ? kbytes + qbytes : 0) + lbytes, d->pool,
+                              stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   void* qr = ws;
   void* kr = ws + qbytes;
+  // padded: v, out and lse in whole tiles
+  void* vk = padded ? static_cast<void*>(ws + qbytes + kbytes) : const_cast<void*>(v);
+  void* ok_out = padded ? static_cast<void*>(ws + qbytes + 2 * kbytes) : out;
+  float* ok_lse = padded ? reinterpret_cast<float*>(ws + 2 * qbytes + 2 * kbytes) : lse;
 
   bool ok = true;
   {
@@ -262,20 +281,22 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
-    rp.seg[0] = {q, qr, nullptr, nullptr, qrows, Sq, q_pos0};
-    rp.seg[1] = {k, kr, nullptr, nullptr, krows, Skv, kv_pos0};
+    rp.seg[0] = {q, qr, nullptr, nullptr, qrows_p, Sq, Sqp, q_pos0};
+    rp.seg[1] = {k, kr, padded ? v : nullptr, padded ? vk : nullptr, krows_p, Skv, Skvp, kv_pos0};
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
     ok = gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
   }
   gbattn::FwdParams fp{};
-  ok = ok && make_map(&fp.map_q, qr, qrows, D, kTile) && make_map(&fp.map_k, kr, krows, D, kTile) &&
-       make_map(&fp.map_v, v, krows, D, kTile) && make_map(&fp.map_out, out, qrows, D, kTile);
+  ok = ok && make_map(&fp.map_q, qr, qrows_p, D, kTile) &&
+       make_map(&fp.map_k, kr, krows_p, D, kTile) && make_map(&fp.map_v, vk, krows_p, D, kTile) &&
+       make_map(&fp.map_out, ok_out, qrows_p, D, kTile);
   if (ok) {
-    fp.out = out;
-    fp.lse = lse;
+    fp.out = ok_out;
+    fp.lse = ok_lse;
     fp.status = d->status;
-    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.Sq = Sq; fp.Skv = Skv; fp.D = D;
+    fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.Sq = Sqp; fp.Skv = Skvp; fp.D = D;
+    fp.kv_valid = Skv;
     fp.q_tile0 = q_pos0 / kTile;
     fp.kv_tile0 = kv_pos0 / kTile;
     fp.scale_log2 = scale * 1.4426950408889634f;
@@ -285,6 +306,10 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     ok = gbattn::launch_fwd(fp, stream) == cudaSuccess;
     tm.done();
   }
+  if (ok && padded)
+    ok = gbattn::launch_unpad_rows(ok_out, out, qrows, Sq, Sqp, D / 2, false, stream) ==
+             cudaSuccess &&
+         gbattn::launch_unpad_rows(ok_lse, lse, qrows, Sq, Sqp, 1, false, stream) == cudaSuccess;
   cudaFreeAsync(ws, stream);
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -293,7 +318,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* l
                 int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
                 int causal, attn_stream_t stream) {
   return fwd_common(q, k, v, out, lse, B, Hq, Hkv, S, S, D, 0, 0, rope_theta, rope_mode, scale,
-                    causal, stream);
+                    causal, stream, true);
 }
 
 int attn_fwd_partial(const void* q, const void* k, const void* v, void* out, float* lse, int B,
@@ -301,7 +326,7 @@ int attn_fwd_partial(const void* q, const void* k, const void* v, void* out, flo
                      float rope_theta, int rope_mode, float scale, int causal,
                      attn_stream_t stream) {
   return fwd_common(q, k, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0, rope_theta,
-                    rope_mode, scale, causal, stream);
+                    rope_mode, scale, causal, stream, false);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -319,28 +344,49 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
                       const float* lse, const void* dout, void* dq_out, void* dk_out, void* dv_out,
                       int B, int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, int kv_pos0,
                       float rope_theta, int rope_mode, float scale, int causal,
-                      attn_stream_t stream_, bool bf16_grads) {
+                      attn_stream_t stream_, bool bf16_grads, bool ragged) {
   const void* ptrs[] = {q, k, v, out, lse, dout, dq_out, dk_out, dv_out};
   int st = validate(ptrs, 9, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
-  if ((st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
+  if (!ragged && (st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
   if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
   const int inter = rope_mode == ATTN_ROPE_INTERLEAVED;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   float *cs = nullptr, *sn = nullptr;
-  const int npos = q_pos0 + Sq > kv_pos0 + Skv ? q_pos0 + Sq : kv_pos0 + Skv;
+  // Table rows for every position a kernel reads, the padding rows of a ragged
+  // sequence included (they are rotated like any row, and then ignored).
+  const int npos = q_pos0 + round_tile(Sq) > kv_pos0 + round_tile(Skv) ? q_pos0 + round_tile(Sq)
+                                                                        : kv_pos0 + round_tile(Skv);
   if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
 
+  // Two CTAs per (KV head, key tile), each with half of the group's query heads,
+  // when one CTA per key tile would not fill the GPU (and the group splits
+  // evenly); otherwise one CTA per key tile, with no dK/dV zeroing.
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  // rows per head the kernels see (padded to whole tiles for a ragged S)
+  const int Sqp = round_tile(Sq), Skvp = round_tile(Skv);
+  const bool padded = Sqp != Sq || Skvp != Skv;
+  if (static_cast<long long>(B) * Hq * Sqp >= (1LL << 31) ||
+      static_cast<long long>(B) * Hkv * Skvp >= (1LL << 31))
+    return ATTN_ERR_INVALID;
   const long long qrows = static_cast<long long>(B) * Hq * Sq;
   const long long krows = static_cast<long long>(B) * Hkv * Skv;
-  const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
-  const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
-  const size_t accbytes = round256(static_cast<size_t>(qrows) * D * 4);
-  const size_t rowbytes = round256(static_cast<size_t>(qrows) * 4);
+  const long long qrows_p = static_cast<long long>(B) * Hq * Sqp;
+  const long long krows_p = static_cast<long long>(B) * Hkv * Skvp;
+  const long long key_tiles = static_cast<long long>(B) * Hkv * (Skvp / kTile);
+  const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
+  const size_t qbytes = round256(static_cast<size_t>(qrows_p) * D * 2);
+  const size_t kbytes = round256(static_cast<size_t>(krows_p) * D * 2);
+  const size_t accbytes = round256(static_cast<size_t>(qrows_p) * D * 4);
+  const size_t rowbytes = round256(static_cast<size_t>(qrows_p) * 4);
   const size_t maxbytes = 256;
-  const size_t gradbytes = bf16_grads ? round256(static_cast<size_t>(krows) * D * 4) : 0;
+  const bool own_dkdv = bf16_grads || padded;  // dk, dv go through workspace copies
+  const size_t gradbytes = own_dkdv ? round256(static_cast<size_t>(krows_p) * D * 4) : 0;
   uint8_t* ws = nullptr;
   if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
                               2 * qbytes + 2 * kbytes + accbytes + 2 * rowbytes + maxbytes +
@@ -357,19 +403,10 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   float* delta = reinterpret_cast<float*>(w); w += rowbytes;
   float* lse2 = reinterpret_cast<float*>(w); w += rowbytes;
   float* maxes = reinterpret_cast<float*>(w); w += maxbytes;
-  // fp32 dk, dv: the caller's buffers, or workspace copies rounded to bf16 at the end
-  float* dk = bf16_grads ? reinterpret_cast<float*>(w) : static_cast<float*>(dk_out);
-  float* dv = bf16_grads ? reinterpret_cast<float*>(w + gradbytes) : static_cast<float*>(dv_out);
-
-  // Two CTAs per (KV head, key tile), each with half of the group's query heads,
-  // when one CTA per key tile would not fill the GPU (and the group splits
-  // evenly); otherwise one CTA per key tile, with no dK/dV zeroing.
-  int dev = 0, nsm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  const long long key_tiles = static_cast<long long>(B) * Hkv * (Skv / kTile);
-  const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
+  // fp32 dk, dv: the caller's buffers, or workspace copies (padded rows, and/or
+  // rounded to bf16) copied into the caller's buffers at the end
+  float* dk = own_dkdv ? reinterpret_cast<float*>(w) : static_cast<float*>(dk_out);
+  float* dv = own_dkdv ? reinterpret_cast<float*>(w + gradbytes) : static_cast<float*>(dv_out);
   bool ok = true;
   {
     LaunchTimer tm(ATTN_KERNEL_BWD_PREP, stream);
@@ -388,8 +425,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     rp.cos_tab = cs;
     rp.sin_tab = sn;
     rp.maxes = maxes;
-    rp.seg[0] = {q, qr, dout, dos, qrows, Sq, q_pos0};
-    rp.seg[1] = {k, kr, v, vs, krows, Skv, kv_pos0};
+    rp.seg[0] = {q, qr, dout, dos, qrows_p, Sq, Sqp, q_pos0};
+    rp.seg[1] = {k, kr, v, vs, krows_p, Skv, Skvp, kv_pos0};
     rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
     if (hsplit > 1) {  // the main kernel adds dK/dV partials of two CTAs
       rp.dk_zero = dk;
@@ -400,10 +437,10 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   }
   gbattn::BwdParams bp{};
   const int bq = gbattn::bwd_query_tile(D);
-  ok = ok && make_map(&bp.map_q, qr, qrows, D, bq, true) &&
-       make_map(&bp.map_do, dos, qrows, D, bq, true) &&
-       make_map(&bp.map_k, kr, krows, D, kTile, true) &&
-       make_map(&bp.map_v, vs, krows, D, kTile, true);
+  ok = ok && make_map(&bp.map_q, qr, qrows_p, D, bq, true) &&
+       make_map(&bp.map_do, dos, qrows_p, D, bq, true) &&
+       make_map(&bp.map_k, kr, krows_p, D, kTile, true) &&
+       make_map(&bp.map_v, vs, krows_p, D, kTile, true);
   if (ok) {
     bp.lse2 = lse2;
     bp.delta = delta;
@@ -414,7 +451,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     bp.cos_tab = cs;
     bp.sin_tab = sn;
     bp.status = d->status;
-    bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.Sq = Sq; bp.Skv = Skv; bp.D = D;
+    bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.Sq = Sqp; bp.Skv = Skvp; bp.D = D;
     bp.q_tile0 = q_pos0 / kTile;
     bp.kv_tile0 = kv_pos0 / kTile;
     bp.scale = scale;
@@ -429,10 +466,16 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   }
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
-    ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, Sq, q_pos0, D, scale, maxes,
-                                    cs, sn,
+    ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, Sq, Sqp, q_pos0, D, scale,
+                                    maxes, cs, sn,
                                     inter, stream) == cudaSuccess;
-    if (bf16_grads)
+    if (padded)
+      ok = ok &&
+           gbattn::launch_unpad_rows(dk, dk_out, krows, Skv, Skvp, D, bf16_grads, stream) ==
+               cudaSuccess &&
+           gbattn::launch_unpad_rows(dv, dv_out, krows, Skv, Skvp, D, bf16_grads, stream) ==
+               cudaSuccess;
+    else if (bf16_grads)
       ok = ok && gbattn::launch_f32_to_bf16(dk, dk_out, krows * D, stream) == cudaSuccess &&
            gbattn::launch_f32_to_bf16(dv, dv_out, krows * D, stream) == cudaSuccess;
     tm.done();
@@ -446,7 +489,7 @@ int attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, co
                 int D, float rope_theta, int rope_mode, float scale, int causal,
                 attn_stream_t stream) {
   return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, S, D, 0, 0, rope_theta,
-                    rope_mode, scale, causal, stream, false);
+                    rope_mode, scale, causal, stream, false, true);
 }
 
 int attn_bwd_partial(const void* q, const void* k, const void* v, const void* out,
@@ -455,7 +498,7 @@ int attn_bwd_partial(const void* q, const void* k, const void* v, const void* ou
                      float rope_theta, int rope_mode, float scale, int causal,
                      attn_stream_t stream) {
   return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0,
-                    rope_theta, rope_mode, scale, causal, stream, false);
+                    rope_theta, rope_mode, scale, causal, stream, false, false);
 }
 
 int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, const float* lse,
@@ -463,7 +506,7 @@ int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, 
                   int D, float rope_theta, int rope_mode, float scale, int causal,
                   attn_stream_t stream) {
   return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, S, D, 0, 0, rope_theta,
-                    rope_mode, scale, causal, stream, true);
+                    rope_mode, scale, causal, stream, true, true);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,

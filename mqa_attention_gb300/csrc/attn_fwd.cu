@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int n_0 = tiles_of(0);
   const int n_1 = tiles_of(1);
   const int n = n_0 > n_1 ? n_0 : n_1;
+  const int kv_valid = p.kv_valid > 0 ? p.kv_valid : p.Skv;  // keys that exist per head
   const int q_row0 = bh * p.Sq;
   const int kv_row0 = (b * p.Hkv + hkv) * p.Skv;
 
@@ -272,6 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (p.causal && p.kv_tile0 + j == p.q_tile0 + qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = i > r ? -INFINITY : s[i];
+      }
+      if (!p.causal && (j + 1) * kTile > kv_valid) {  // padding keys of the last tile
+        const int lim = kv_valid - j * kTile;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = i >= lim ? -INFINITY : s[i];
       }
       // Row maximum as 8 independent partial chains (latency, not issue, bound).
       float mp[8];

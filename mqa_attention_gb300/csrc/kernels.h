@@ -79,8 +79,9 @@ struct RowSegment {
   void* y;
   const void* x2;  // backward: dout (query rows) or v (key rows)
   void* y2;
-  long long rows;
-  int S;     // rows per head; row r sits at position pos0 + r % S
+  long long rows;  // output rows (Sp per head)
+  int S;     // input rows per head; input row h*S + i sits at position pos0 + i
+  int Sp;    // output rows per head (S, or S rounded up to whole tiles)
   int pos0;
 };
 struct RowPrepParams {
@@ -104,12 +105,16 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 // dq = scale * 2^-(edo+ev+ek) * R_iᵀ dqacc (fp32 in; fp32 out, or bf16 rounded to
 // nearest even when dq_bf16); row r sits at position pos0 + r % S.
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
-                               int pos0, int D, float scale, const float* maxes, const float* cos_tab,
+                               int Sp, int pos0, int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream);
 // Merge of two partial attention results of the same rows (bf16 out, fp32 lse);
 // o / l may be oa / la.
 cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb, void* o,
                          float* l, long long rows, int D, cudaStream_t stream);
+// dst[h*S + i] = src[h*Sp + i] for rows of `words` 4-byte words (rows = heads * S);
+// to_bf16: fp32 source rows written as bf16 rows.
+cudaError_t launch_unpad_rows(const void* src, void* dst, long long rows, int S, int Sp, int words,
+                              bool to_bf16, cudaStream_t stream);
 // y = bf16(x) (nearest even), n a multiple of 8.
 cudaError_t launch_f32_to_bf16(const float* x, void* y, long long n, cudaStream_t stream);
 
@@ -126,6 +131,7 @@ struct FwdParams {
   // rows at 128*kv_tile0 + j (self-attention: Sq = Skv = S, both tiles 0).
   int B, Hq, Hkv, Sq, Skv, D;
   int q_tile0, kv_tile0;
+  int kv_valid;      // keys per head that exist (< Skv when the block is padded)
   float scale_log2;  // scale * log2(e)
   int causal;
   int inject_timeout;

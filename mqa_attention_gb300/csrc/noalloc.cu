@@ -132,8 +132,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   rp.D = D;
   rp.cos_tab = cs;
   rp.sin_tab = sn;
-  rp.seg[0] = {q, qr, nullptr, nullptr, qrows, S, 0};
-  rp.seg[1] = {k, kr, nullptr, nullptr, krows, S, 0};
+  rp.seg[0] = {q, qr, nullptr, nullptr, qrows, S, S, 0};
+  rp.seg[1] = {k, kr, nullptr, nullptr, krows, S, S, 0};
   ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
   gbattn::FwdParams fp{};
   ok = ok && map_bf16(&fp.map_q, qr, qrows, D) && map_bf16(&fp.map_k, kr, krows, D) &&
@@ -143,6 +143,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   fp.status = status;
   fp.B = B; fp.Hq = Hq; fp.Hkv = Hkv; fp.Sq = S; fp.Skv = S; fp.D = D;
   fp.out = out;
+  fp.kv_valid = S;
   fp.scale_log2 = scale * 1.4426950408889634f;
   fp.causal = causal ? 1 : 0;
   fp.inject_timeout = 0;

@@ -159,10 +159,13 @@ __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
   }
 }
 
-// One thread per (row, c) with c < D/16 and the two element groups of
+// One thread per (output row, c) with c < D/16 and the two element groups of
 // rope_off_a / rope_off_b. Rows [0, seg[0].rows) are query rows, the next
-// seg[1].rows are key rows.
-template <int D, bool kBwd>
+// seg[1].rows are key rows; a segment's outputs hold Sp rows per head, of which
+// the first S are its input rows (the rest, when the sequence is padded to whole
+// tiles, are written as rows that contribute nothing: zero operands, delta 0 and,
+// in the backward, lse * log2 e = +inf so that their probabilities are 0).
+template <int D, bool kBwd, bool kPad>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
@@ -175,21 +178,45 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   // Threads past the last row read row 0 of the segment (a valid address), take
   // part in the shuffles below and write nothing.
   const bool live = row0 < sg.rows;
-  const long long r = live ? row0 : 0;
-  const int pos = sg.pos0 + static_cast<int>(r % sg.S);
+  // output row, its head and row within the head (rows < 2^31: 32-bit division)
+  const unsigned ro32 = live ? static_cast<unsigned>(row0) : 0u;
+  const unsigned head = ro32 / static_cast<unsigned>(sg.Sp);
+  const int i = static_cast<int>(ro32 - head * static_cast<unsigned>(sg.Sp));
+  const long long ro = ro32;
+  const bool real = !kPad || i < sg.S;  // kPad = false: every output row is an input row
+  const long long ri =  // input row
+      !kPad ? ro : (real ? static_cast<long long>(head) * sg.S + i : 0);
+  const int pos = sg.pos0 + (real ? i : 0);
   const bool inter = p.rope_interleaved != 0;
-  const long long e1 = r * D + rope_off_a(c, inter);
-  const long long e2 = r * D + rope_off_b(c, D, inter);
+  const int oa = rope_off_a(c, inter), ob = rope_off_b(c, D, inter);
+  const long long e1 = ri * D + oa, e2 = ri * D + ob;  // input elements
+  const long long f1 = ro * D + oa, f2 = ro * D + ob;  // output elements
+  const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
   load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e1, x1);
   load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
   load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
   load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
   rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
+  if (!real) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) y1[k] = y2[k] = 0.f;
+  }
   if constexpr (!kBwd) {
     if (live) {
-      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + e1, y1);
-      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + e2, y2);
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
+      if (sg.y2 != nullptr) {  // padded copy of v (key rows)
+        float a1[8], a2[8];
+        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
+        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
+        if (!real) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
+        }
+        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
+        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
+      }
     }
   } else {
     const BwdExponents ex = bwd_exponents(p.maxes);
@@ -198,40 +225,42 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
     float a1[8], a2[8];
     load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
     load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
+    if (!real) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
+    }
     if (live) {
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + e1, y1, s_rot);
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + e2, y2, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f1, y1, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f2, y2, s_rot);
       // x2 is already bf16: scaling by a power of two and storing fp16 is exact
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + e1, a1, s_x2);
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + e2, a2, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
     }
     // delta for query rows. Every thread computes it and takes part in the
     // shuffle (a warp may straddle the query/key boundary); key rows read row 0
     // of `out` and write nothing.
     float o1[8], o2[8];
-    const long long eo = is_q ? 0 : r * D;
+    const long long eo = is_q ? 0 : ri * D;
     load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e1 - eo), o1);
     load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e2 - eo), o2);
     float dot = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dot += a1[i] * o1[i] + a2[i] * o2[i];
+    for (int k = 0; k < 8; ++k) dot += a1[k] * o1[k] + a2[k] * o2[k];
 #pragma unroll
     for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     if (!is_q && live && p.dk_zero != nullptr) {
-      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      store8(p.dk_zero + e1, z);
-      store8(p.dk_zero + e2, z);
-      store8(p.dv_zero + e1, z);
-      store8(p.dv_zero + e2, z);
+      store8(p.dk_zero + f1, z);
+      store8(p.dk_zero + f2, z);
+      store8(p.dv_zero + f1, z);
+      store8(p.dv_zero + f2, z);
     }
     if (is_q && live) {
       if (c == 0) {
-        p.delta[r] = dot * exp2i(ex.dout + ex.v);
-        p.lse2[r] = p.lse[r] * kLog2e;
+        p.delta[ro] = real ? dot * exp2i(ex.dout + ex.v) : 0.f;
+        p.lse2[ro] = real ? p.lse[ri] * kLog2e : INFINITY;
       }
-      const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      store8(p.dqacc + e1, z);
-      store8(p.dqacc + e2, z);
+      store8(p.dqacc + f1, z);
+      store8(p.dqacc + f2, z);
     }
   }
 }
@@ -240,7 +269,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
     dq_finalize_kernel(const float* __restrict__ dqacc, void* __restrict__ dq, long long rows,
-                       int S, int pos0, float scale, const float* __restrict__ maxes,
+                       int S, int Sp, int pos0, float scale, const float* __restrict__ maxes,
                        const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
                        int rope_interleaved) {
   constexpr int T = D / 16;
@@ -249,15 +278,22 @@ __global__ void __launch_bounds__(256)
   const long long row = t / T;
   if (row >= rows) return;
   const int c = static_cast<int>(t % T);
-  const int pos = pos0 + static_cast<int>(row % S);
+  // dq row `row` (S rows per head); its accumulator row has Sp rows per head
+  // (rows < 2^31: 32-bit division)
+  const unsigned head = static_cast<unsigned>(row) / static_cast<unsigned>(S);
+  const int i = static_cast<int>(static_cast<unsigned>(row) - head * static_cast<unsigned>(S));
+  const int pos = pos0 + i;
   const bool inter = rope_interleaved != 0;
+  const long long racc = static_cast<long long>(head) * Sp + i;
   const long long e1 = row * D + rope_off_a(c, inter);
   const long long e2 = row * D + rope_off_b(c, D, inter);
+  const long long a1 = racc * D + rope_off_a(c, inter);
+  const long long a2 = racc * D + rope_off_b(c, D, inter);
   const BwdExponents ex = bwd_exponents(maxes);
   const float f = scale * exp2i(-(ex.dout + ex.v + ex.k));
   float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
-  load8(dqacc + e1, x1);
-  load8(dqacc + e2, x2);
+  load8(dqacc + a1, x1);
+  load8(dqacc + a2, x2);
   load8(cos_tab + (long long)pos * H + 8 * c, cs);
   load8(sin_tab + (long long)pos * H + 8 * c, sn);
   rotate16(x1, x2, cs, sn, inter, -1.f, y1, y2);  // transpose: rotation by -angle
@@ -313,6 +349,28 @@ __global__ void __launch_bounds__(256)
   if (c == 0) l[row] = lse;
 }
 
+// Rows of a padded layout (Sp rows per head) to the unpadded one (S rows per
+// head): dst[h*S + i] = src[h*Sp + i], i < S, rows of `words` 4-byte words; with
+// to_bf16, fp32 rows become bf16 rows (nearest even) of words/2 words.
+__global__ void __launch_bounds__(256)
+    unpad_rows_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst, long long rows,
+                      int S, int Sp, int words, int to_bf16) {
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const int per_row = to_bf16 ? words / 2 : words;
+  const long long row = t / per_row;
+  if (row >= rows) return;
+  const int w = static_cast<int>(t % per_row);
+  const long long srow = (row / S) * Sp + row % S;
+  if (to_bf16) {
+    const float a = __uint_as_float(src[srow * words + 2 * w]);
+    const float b = __uint_as_float(src[srow * words + 2 * w + 1]);
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    dst[row * per_row + w] = *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    dst[row * per_row + w] = src[srow * words + w];
+  }
+}
+
 // y = bf16(x), nearest even; n a multiple of 8.
 __global__ void __launch_bounds__(256)
     f32_to_bf16_kernel(const float* __restrict__ x, void* __restrict__ y, long long n8) {
@@ -342,24 +400,27 @@ cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
   const long long threads = (p.seg[0].rows + p.seg[1].rows) * (p.D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
+  const bool pad = p.seg[0].S != p.seg[0].Sp || p.seg[1].S != p.seg[1].Sp;
+#define GB_PREP(DD, BW, PD) row_prep_kernel<DD, BW, PD><<<grid, 256, 0, stream>>>(p)
   if (p.D == 128) {
-    if (p.bwd) row_prep_kernel<128, true><<<grid, 256, 0, stream>>>(p);
-    else row_prep_kernel<128, false><<<grid, 256, 0, stream>>>(p);
+    if (p.bwd) { if (pad) GB_PREP(128, true, true); else GB_PREP(128, true, false); }
+    else { if (pad) GB_PREP(128, false, true); else GB_PREP(128, false, false); }
   } else {
-    if (p.bwd) row_prep_kernel<64, true><<<grid, 256, 0, stream>>>(p);
-    else row_prep_kernel<64, false><<<grid, 256, 0, stream>>>(p);
+    if (p.bwd) { if (pad) GB_PREP(64, true, true); else GB_PREP(64, true, false); }
+    else { if (pad) GB_PREP(64, false, true); else GB_PREP(64, false, false); }
   }
+#undef GB_PREP
   return cudaGetLastError();
 }
 
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
-                               int pos0, int D, float scale, const float* maxes, const float* cos_tab,
+                               int Sp, int pos0, int D, float scale, const float* maxes, const float* cos_tab,
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
 #define GB_FIN(DD, BF)                                                                   \
-  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, pos0, scale, maxes, \
-                                                       cos_tab, sin_tab, rope_interleaved)
+  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, Sp, pos0, scale,   \
+                                                       maxes, cos_tab, sin_tab, rope_interleaved)
   if (D == 128) {
     if (dq_bf16) GB_FIN(128, true);
     else GB_FIN(128, false);
@@ -376,6 +437,16 @@ cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const 
   const unsigned grid = (unsigned)blocks_for(rows * (D / 8));
   if (D == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
   else merge_kernel<64><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpad_rows(const void* src, void* dst, long long rows, int S, int Sp, int words,
+                              bool to_bf16, cudaStream_t stream) {
+  const long long n = rows * (to_bf16 ? words / 2 : words);
+  if (n == 0) return cudaSuccess;
+  unpad_rows_kernel<<<(unsigned)blocks_for(n), 256, 0, stream>>>(
+      static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, S, Sp, words,
+      to_bf16 ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -184,6 +184,45 @@ def test_bf16_gradients(B, Hq, Hkv, S, D, causal, rope):
         assert e.mean().item() <= gmean + half_ulp.mean().item(), name
 
 
+RAGGED = [
+    # (B, Hq, Hkv, S, D, causal): sequence lengths that are not whole 128-row tiles,
+    # from one row to several tiles plus a tail, causal and not, both head sizes
+    (1, 4, 1, 1, 64, True),
+    (1, 2, 1, 100, 128, True),
+    (2, 4, 2, 300, 64, True),
+    (1, 8, 2, 1000, 128, True),
+    (1, 4, 4, 200, 128, False),
+    (2, 2, 1, 77, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", RAGGED)
+def test_ragged_sequence_lengths(B, Hq, Hkv, S, D, causal):
+    """S not a multiple of 128: the library pads to whole tiles internally; every
+    output row is checked against the oracle, and no padding row may leak into
+    another head's rows."""
+    wl = Workload(270 + S % 97 + D, "ragged", B, Hq, Hkv, S, D,
+                  10000.0 if D == 64 else 500000.0, True, causal)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev)
+    check_all(wl, g, f)
+
+
+def test_ragged_bf16_gradients():
+    """attn_bwd_bf16 with a ragged S: padded fp32 copies, rounded as they are unpadded."""
+    wl = Workload(290, "ragged", 1, 4, 2, 300, 128, 500000.0, True, True)
+    dev, _ = gen(wl)
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+    g32 = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                     wl.causal)
+    g16 = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                     wl.causal, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert M.sync_status() == 0
+    for name, a, b in (("dk", g16[1], g32[1]), ("dv", g16[2], g32[2])):
+        assert torch.equal(a, b.to(torch.bfloat16)), name
+
+
 def test_tiny_mqa_forward_workload():
     wl = by_index(1)
     dev, f = gen(wl)
