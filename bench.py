@@ -62,6 +62,9 @@ def parse():
                     help="RoPE pair layout (interleaved runs attn_fwd_ex / attn_bwd_ex)")
     ap.add_argument("--grads", choices=["fp32", "bf16"], default="fp32",
                     help="gradient dtype (bf16 runs attn_bwd_bf16)")
+    ap.add_argument("--decode", type=int, default=0, metavar="SQ",
+                    help="SQ > 0: time attn_decode, SQ new tokens per sequence against a "
+                         "cache of the workload's S keys (HBM-bound: reported in GB/s)")
     ap.add_argument("--blocks", type=int, default=1,
                     help="N > 1: run the step as N x N query / key-value blocks through "
                          "attn_fwd_partial, attn_merge and attn_bwd_partial")
@@ -595,11 +598,109 @@ def run_blocks(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args, rank, world, local):
+    """Decode shape: SQ new query rows per head (at the cache's last SQ positions)
+    against a rotated key / value cache of the workload's S rows. The work is one
+    read of the cache, so the metric is bytes moved (caches, q, out, lse) per second
+    against the measured HBM copy bandwidth. Device time only."""
+    import mqa_attention_gb300 as M
+    from mqa_attention_gb300 import build as B
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (GB300)")
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    barrier(world)
+    M.lib()
+    wl = by_name(args.workload)
+    sq = args.decode
+    host = host_inputs(wl, rank)
+    dev = {n: to_bf16_tensor(h, "cuda") for n, h in host.items()}
+    q = dev["q"][:, :, :sq].contiguous()
+    mode = M.ROPE_MODES[args.rope]
+    cache = 2 * wl.B * wl.Hkv * wl.S * wl.D * 2
+    # Enough copies of the cache (>= 256 MiB in all) that each call reads its own
+    # copy cold from HBM; one graph launches one call per copy.
+    ncopy = max(1, -(-L2_FLUSH_BYTES // cache))
+    k_rot = M.rope(dev["k"], wl.theta, rope=args.rope)
+    caches = [(k_rot, dev["v"])] + [(k_rot.clone(), dev["v"].clone()) for _ in range(ncopy - 1)]
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, sq), dtype=torch.float32, device="cuda")
+    qpos = wl.S - sq
+
+    def calls(st):
+        for kc, vc in caches:
+            M.attn_decode(q, kc, vc, out, lse, wl.B, wl.Hq, wl.Hkv, sq, wl.S, wl.D, qpos,
+                          wl.theta, mode, wl.scale, st)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(max(3, args.warmup)):
+            calls(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    if M.sync_status() != 0:
+        raise SystemExit("device status error during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls(torch.cuda.current_stream())
+    stream = torch.cuda.current_stream()
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // ncopy)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    status = M.sync_status()
+    ms = max_over_ranks(e0.elapsed_time(e1) / (reps * ncopy), world)
+    sampler.stop()
+    if rank != 0:
+        return
+    _, peak_hbm, peak_src = peaks()
+    moved = cache + 2 * q.numel() * 2 + lse.numel() * 4
+    gbs = moved * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"decode attention GB/s ({sq} new tokens per sequence, cache S={wl.S})",
+        "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic N(0,1) bf16 q/k/v, seeded (splitmix64 + Box-Muller)",
+        "config": dict(config_of(wl, world, l2=f"each call reads its own cache copy ({ncopy} "
+                                                   "copies, >= 256 MiB)", rope=args.rope),
+                       passes="decode fwd", new_tokens=sq, bytes_per_step=moved),
+        "e2e": None,
+        "note": "decode entry point, calls replayed from a CUDA graph; device time only",
+        "steps": reps * ncopy,
+        "gpu_launches": 2 * reps * ncopy,  # chunk kernel and merge per call
+        "roofline": {"bound": "hbm", "kernel": "attn_decode", "achieved": gbs / world,
+                     "peak": peak_hbm, "unit": "GB/s", "frac": gbs / world / peak_hbm,
+                     "traffic": None, "peak_source": f"{peak_src} HBM copy"},
+        "cpu_baseline": None,
+        "clocks": sampler.summary(t0, t1),
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.decode > 0:
+        run_decode(args, rank, world, local)
     elif args.blocks > 1:
         run_blocks(args, rank, world, local)
     else:

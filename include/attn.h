@@ -147,6 +147,26 @@ int attn_bwd_partial(const void* q, const void* k, const void* v, const void* ou
 int attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
                void* out, float* lse, long long rows, int D, attn_stream_t stream);
 
+/* y = RoPE(x) rounded to bf16: x, y [heads, S, D] bf16 (may be the same buffer), row i
+ * of every head rotated by the angle of position pos0 + i in the layout rope_mode (the
+ * rotation attn_fwd applies to q and k). Fills the rotated key cache attn_decode
+ * reads. */
+int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D,
+              float rope_theta, int rope_mode, attn_stream_t stream);
+
+/* Decode-shape forward: Sq new query rows per head (q [B,Hq,Sq,D] bf16, not rotated;
+ * row i at position q_pos0 + i) against a cache of Skv keys and values:
+ * k_rot [B,Hkv,Skv,D] bf16 holding the keys already rotated by their positions
+ * 0..Skv-1 (as attn_rope writes them), v [B,Hkv,Skv,D] bf16. Key j is seen by query i
+ * when j <= q_pos0 + i (and j < Skv); out [B,Hq,Sq,D] bf16, lse [B,Hq,Sq] fp32 as in
+ * attn_fwd (a row that sees no key: out = 0, lse = -inf). The Hq/Hkv query heads of a
+ * K/V head share each pass over its cache (PaLM §2.5: one shared K/V head is what
+ * makes decoding cheap), so (Hq/Hkv) * Sq <= 128 (else ATTN_ERR_UNSUPPORTED). Any
+ * Skv >= 1. */
+int attn_decode(const void* q, const void* k_rot, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, float rope_theta,
+                int rope_mode, float scale, attn_stream_t stream);
+
 /* attn_bwd_ex writing bf16 gradients: dq [B,Hq,S,D], dk, dv [B,Hkv,S,D] bf16, each the
  * value attn_bwd_ex writes in fp32 rounded to nearest even (dk and dv bit for bit;
  * dq's fp32 value sums its partial products in a run-dependent order, so it may

@@ -26,6 +26,10 @@ __all__ = [
     "attn_fwd_partial",
     "attn_bwd_partial",
     "attn_merge",
+    "attn_rope",
+    "attn_decode",
+    "rope",
+    "decode",
     "forward",
     "forward_partial",
     "backward_partial",
@@ -61,6 +65,8 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_partial",
     "attn_bwd_partial",
     "attn_merge",
+    "attn_rope",
+    "attn_decode",
     "attn_sync_status",
     "attn_status_string",
     "attn_profile_begin",
@@ -133,6 +139,11 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_partial.restype = _I
             L.attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_longlong, _I, _P]
             L.attn_merge.restype = _I
+            L.attn_rope.argtypes = [_P, _P, ctypes.c_longlong, _I, _I, _I, _F, _I, _P]
+            L.attn_rope.restype = _I
+            L.attn_decode.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _F,
+                                      _P]
+            L.attn_decode.restype = _I
             _lib = L
         return _lib
 
@@ -241,6 +252,47 @@ def attn_merge(out_a, lse_a, out_b, lse_b, out, lse, rows, D, stream=None):
     """C ABI attn_merge: combine two partial results of the same query rows."""
     _check(lib().attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
                             _ptr(lse), int(rows), int(D), _stream(stream)), "attn_merge")
+
+
+def attn_rope(x, y, heads, S, pos0, D, rope_theta, rope_mode, stream=None):
+    """C ABI attn_rope: y = bf16(RoPE(x)) for rows at positions pos0 + i."""
+    _check(lib().attn_rope(_ptr(x), _ptr(y), int(heads), int(S), int(pos0), int(D),
+                           float(rope_theta), int(rope_mode), _stream(stream)), "attn_rope")
+
+
+def attn_decode(q, k_rot, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, rope_theta, rope_mode,
+                scale, stream=None):
+    """C ABI attn_decode: Sq new queries per head against a rotated K/V cache."""
+    _check(lib().attn_decode(_ptr(q), _ptr(k_rot), _ptr(v), _ptr(out), _ptr(lse), int(B),
+                             int(Hq), int(Hkv), int(Sq), int(Skv), int(D), int(q_pos0),
+                             float(rope_theta), int(rope_mode), float(scale), _stream(stream)),
+           "attn_decode")
+
+
+def rope(x, rope_theta, pos0=0, out=None, stream=None, rope="half"):
+    """bf16 RoPE(x) of x [..., S, D] (rows at positions pos0..pos0+S-1)."""
+    import torch
+
+    S, D = x.shape[-2], x.shape[-1]
+    y = torch.empty_like(x) if out is None else out
+    attn_rope(x, y, x.numel() // (S * D), S, pos0, D, rope_theta, ROPE_MODES[rope], stream)
+    return y
+
+
+def decode(q, k_rot, v, rope_theta, q_pos0=None, scale=None, stream=None, rope="half"):
+    """Allocates out / lse and runs attn_decode; q: [B,Hq,Sq,D], caches [B,Hkv,Skv,D].
+    q_pos0 defaults to Skv - Sq (the new tokens are the cache's last positions)."""
+    import torch
+
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k_rot.shape[1], k_rot.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    q_pos0 = Skv - Sq if q_pos0 is None else q_pos0
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    attn_decode(q, k_rot, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, rope_theta,
+                ROPE_MODES[rope], scale, stream)
+    return out, lse
 
 
 def forward_partial(q, k, v, rope_theta, q_pos0, kv_pos0, scale=None, causal=True, stream=None,

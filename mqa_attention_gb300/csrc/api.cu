@@ -516,6 +516,97 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
                      ATTN_ROPE_HALF, scale, causal, stream);
 }
 
+int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D, float rope_theta,
+              int rope_mode, attn_stream_t stream_) {
+  if (!aligned16(x) || !aligned16(y)) return ATTN_ERR_INVALID;
+  if (heads <= 0 || S <= 0 || pos0 < 0 || heads * S >= (1LL << 31) ||
+      static_cast<long long>(pos0) + S > (1LL << 30))
+    return ATTN_ERR_INVALID;
+  if (!std::isfinite(rope_theta) || rope_theta <= 0.f) return ATTN_ERR_INVALID;
+  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  int st = device_state(&d);
+  if (st != ATTN_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  float *cs = nullptr, *sn = nullptr;
+  if ((st = rope_table(d, pos0 + S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  gbattn::RowPrepParams rp{};
+  rp.bwd = 0;
+  rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
+  rp.D = D;
+  rp.cos_tab = cs;
+  rp.sin_tab = sn;
+  rp.seg[0] = {x, y, nullptr, nullptr, heads * S, S, S, pos0};
+  rp.seg[1] = {x, y, nullptr, nullptr, 0, S, S, pos0};
+  return gbattn::launch_row_prep(rp, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode(const void* q, const void* k_rot, const void* v, void* out, float* lse, int B,
+                int Hq, int Hkv, int Sq, int Skv, int D, int q_pos0, float rope_theta,
+                int rope_mode, float scale, attn_stream_t stream_) {
+  const void* ptrs[] = {q, k_rot, v, out, lse};
+  int st = validate(ptrs, 5, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
+  if (st != ATTN_OK) return st;
+  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  if (q_pos0 < 0 || static_cast<long long>(q_pos0) + Sq > (1LL << 30) ||
+      static_cast<long long>(B) * Hkv * Skv >= (1LL << 31))
+    return ATTN_ERR_INVALID;
+  if ((Hq / Hkv) * Sq > kTile) return ATTN_ERR_UNSUPPORTED;  // one tile holds a group's rows
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != ATTN_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  float *cs = nullptr, *sn = nullptr;
+  if ((st = rope_table(d, q_pos0 + Sq, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+
+  // Chunks: about one CTA per SM over all (batch, KV head) caches (a CTA holds a
+  // whole SM's shared memory, so more would run in a second wave).
+  gbattn::DecParams dp{};
+  const long long nu = static_cast<long long>(B) * Hkv;
+  const int last_q = q_pos0 + Sq - 1;
+  const int ntiles_all = (Skv + kTile - 1) / kTile;
+  const int vis = last_q / kTile + 1;
+  const int ntiles = vis < ntiles_all ? vis : ntiles_all;  // tiles with a visible key
+  long long tpc = (static_cast<long long>(ntiles) * nu + nsm - 1) / nsm;
+  tpc = tpc < 1 ? 1 : tpc;
+  dp.tiles_per_chunk = static_cast<int>(tpc);
+  dp.nchunks = static_cast<int>((ntiles + tpc - 1) / tpc);
+  if (dp.nchunks < 1) dp.nchunks = 1;
+  dp.rows = static_cast<long long>(B) * Hq * Sq;
+
+  const size_t obytes = round256(static_cast<size_t>(dp.nchunks) * dp.rows * D * 4);
+  const size_t lbytes = round256(static_cast<size_t>(dp.nchunks) * dp.rows * 4);
+  uint8_t* ws = nullptr;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), obytes + lbytes, d->pool, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  dp.part_out = reinterpret_cast<float*>(ws);
+  dp.part_lse = reinterpret_cast<float*>(ws + obytes);
+  const long long krows = static_cast<long long>(B) * Hkv * Skv;
+  bool ok = make_map(&dp.map_q, q, dp.rows, D, kTile) &&
+            make_map(&dp.map_k, k_rot, krows, D, kTile) && make_map(&dp.map_v, v, krows, D, kTile);
+  if (ok) {
+    dp.out = out;
+    dp.lse = lse;
+    dp.cos_tab = cs;
+    dp.sin_tab = sn;
+    dp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
+    dp.status = d->status;
+    dp.B = B; dp.Hq = Hq; dp.Hkv = Hkv; dp.Sq = Sq; dp.Skv = Skv; dp.D = D;
+    dp.q_pos0 = q_pos0;
+    dp.scale_log2 = scale * 1.4426950408889634f;
+    LaunchTimer tm(ATTN_KERNEL_FWD, stream);
+    ok = gbattn::launch_decode(dp, stream) == cudaSuccess;
+    tm.done();
+  }
+  cudaFreeAsync(ws, stream);
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_merge(const void* out_a, const float* lse_a, const void* out_b, const float* lse_b,
                void* out, float* lse, long long rows, int D, attn_stream_t stream_) {
   const void* ptrs[] = {out_a, lse_a, out_b, lse_b, out, lse};

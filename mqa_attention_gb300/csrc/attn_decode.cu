@@ -1,0 +1,451 @@
+// Decode-shape attention for sm_103a: a few new queries per sequence (Sq rows
+// per query head) against a long key/value cache.
+//
+// What it computes is the forward of attn_fwd restricted to those rows: query i
+// of a head sits at position q_pos0 + i and sees the cached keys at positions
+// j <= q_pos0 + i (j < Skv); scores q~.k~ scale, softmax with the row maximum
+// subtracted, P v ("ColossalAI 中的 PaLM 教学实现…", §2.5 Attention, where one
+// shared K/V head is what makes such decoding cheap; "深度学习系统设计llama3-
+// from-scratch：并行计算架构", §键值（Key-Value）共享机制).
+//
+// GB300 design. The work is bound by reading the cache once, so the G query
+// heads that share a K/V head are packed into the rows of one 128-row MMA tile
+// (G * Sq <= 128 real rows: one CTA serves the whole group and each K/V tile is
+// read once), and the cache of each (batch, KV head) is split into chunks of
+// key tiles spread over the SMs. Per chunk a CTA loads the group's query rows,
+// rotates them in shared memory (RoPE at their positions, rounded to bf16 as the
+// pre-pass of attn_fwd does), streams K~/V tiles through a TMA ring; S = Q~ K~ᵀ
+// (tcgen05, two TMEM buffers so that the next score MMA runs while the softmax
+// works), P (bf16, over S) and O += P V (TS MMA) as in the forward kernel, and
+// writes its rows' partial out (fp32, already divided by the chunk's row sum) and
+// lse. decode_merge_kernel then combines the chunks of each row by their
+// log-sum-exp weights, spread over the whole GPU (merging in the last CTA of a
+// K/V head instead put up to a megabyte of partial rows on one SM).
+// Warp roles: 0-3 softmax (thread = tile row), 4 TMA producer, 5 MMA issuer (whole
+// warp, one elected lane issues) and TMEM owner.
+// TMEM: S_0 [0,128), S_1 [128,256), O [256, 256 + D).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+using namespace gb;
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kThreads = 192;
+constexpr int kWarpLoad = 4;
+constexpr int kWarpMma = 5;
+
+enum : int {
+  kSiteQ = 41, kSiteKvFull = 42, kSiteKvEmpty = 43, kSiteSFull = 44, kSitePFull = 45,
+  kSiteODone = 46, kSiteQRot = 47
+};
+
+template <int D>
+struct DecCfg {
+  static constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16)
+  static constexpr int kRegions = D / 64;
+  static constexpr int kTileBytes = kRegions * kRegionBytes;
+  static constexpr int kSlots = D == 128 ? 6 : 12;  // K/V ring depth (tiles)
+  static constexpr int kKvOff = kTileBytes;         // after the Q tile
+  static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
+  static_assert(kSmemBytes + 1024 <= 232448, "shared memory budget");
+  static constexpr uint32_t kColO = 256;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs / 4) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecParams p) {
+  using C = DecCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_q_rot, bar_drain, bar_o_done;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kSlots], bar_kv_empty[C::kSlots];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  // ---- work item: chunk c of the cache of (batch, KV head) bhk
+  const int nu = p.B * p.Hkv;
+  const int c = static_cast<int>(blockIdx.x) / nu;
+  const int bhk = static_cast<int>(blockIdx.x) % nu;
+  const int b = bhk / p.Hkv;
+  const int hkv = bhk % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int m_real = G * p.Sq;                               // real rows of the tile
+  const int q_row0 = (b * p.Hq + hkv * G) * p.Sq;            // first row of the group
+  const int kv_row0 = bhk * p.Skv;
+  const int ntiles = (p.Skv + kTile - 1) / kTile;
+  const int last_q = p.q_pos0 + p.Sq - 1;                    // largest query position
+  int kt0 = c * p.tiles_per_chunk;
+  int kt1 = kt0 + p.tiles_per_chunk;
+  kt1 = kt1 < ntiles ? kt1 : ntiles;
+  const int kt_vis = last_q / kTile + 1;                     // tiles with a visible key
+  kt1 = kt1 < kt_vis ? kt1 : kt_vis;
+  const int n = kt1 > kt0 ? kt1 - kt0 : 0;
+
+  // ---- setup
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_q_rot), 128);
+    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_o_done), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_s_full[t]), 1);
+      mbar_init(smem_u32(&bar_p_full[t]), 128);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == kWarpLoad) {
+    // ================================================================ producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&p.map_q);
+      tma_prefetch_desc(&p.map_k);
+      tma_prefetch_desc(&p.map_v);
+      mbar_arrive_expect_tx(smem_u32(&bar_q), C::kTileBytes);
+      for (int r = 0; r < C::kRegions; ++r)
+        tma_load_2d(sbase + r * C::kRegionBytes, &p.map_q, r * 64, q_row0, smem_u32(&bar_q));
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        for (int w = 0; w < 2; ++w) {  // K_j, then V_j
+          const int slot = issued % C::kSlots;
+          const uint32_t ph = ((issued / C::kSlots) & 1) ^ 1;
+          if (!bounded_wait(smem_u32(&bar_kv_empty[slot]), ph, abort_ptr, p.status, kSiteKvEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&bar_kv_full[slot]);
+          mbar_arrive_expect_tx(full, C::kTileBytes);
+          const CUtensorMap* map = w == 0 ? &p.map_k : &p.map_v;
+          const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (kt0 + j) * kTile, full);
+          ++issued;
+        }
+      }
+      // Loads already issued land before the CTA releases its shared memory.
+      drain_wait(smem_u32(&bar_q), 0);
+      for (int i = issued - C::kSlots > 0 ? issued - C::kSlots : 0; i < issued; ++i)
+        drain_wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);
+    constexpr uint64_t kMnV = sdesc_hi(C::kRegionBytes, 1024);
+    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
+    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
+    };
+    auto slot_addr = [&](int i) { return sbase + C::kKvOff + (i % C::kSlots) * C::kTileBytes; };
+    auto wait_kv = [&](int i) {
+      return wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1, kSiteKvFull);
+    };
+    // S_(j&1) = Q~ K_jᵀ (K_j at ring index 2j)
+    auto issue_qk = [&](int j) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+        mma_ss_w(tmem + (j & 1) * 128, desc(kKmaj, sbase + off), desc(kKmaj, slot_addr(2 * j) + off),
+                 idesc_qk, kk > 0);
+      }
+      mma_commit_w(smem_u32(&bar_s_full[j & 1]));
+      mma_commit_w(smem_u32(&bar_kv_empty[(2 * j) % C::kSlots]));
+    };
+    bool ok = n > 0;
+    ok = ok && wait(smem_u32(&bar_q_rot), 0, kSiteQRot);  // loaded and rotated
+    for (int j = 0; j < 2 && j < n && ok; ++j) {
+      ok = wait_kv(2 * j);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk(j);
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      ok = wait(smem_u32(&bar_p_full[j & 1]), (j >> 1) & 1, kSitePFull) && wait_kv(2 * j + 1);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t vaddr = slot_addr(2 * j + 1);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)  // O += P_j V_j, P packed over S_(j&1)
+        mma_ts_w(tmem + C::kColO, tmem + (j & 1) * 128 + kk * 8,
+                 desc(kMnV, vaddr + kk * 16 * 128), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_w(smem_u32(&bar_o_done));
+      mma_commit_w(smem_u32(&bar_kv_empty[(2 * j + 1) % C::kSlots]));
+      if (j + 2 < n) {  // after P V(j) in issue order: P_j is read before S_(j&1) is rewritten
+        ok = wait_kv(2 * (j + 2));
+        if (!ok) break;
+        issue_qk(j + 2);
+      }
+    }
+    // Every MMA issued above completes before the tensor memory is released.
+    mma_commit_w(smem_u32(&bar_drain));
+    drain_wait(smem_u32(&bar_drain), 0);
+    __syncwarp();
+  } else {
+    // ================================================================ softmax (rows)
+    const int r = tid;  // tile row == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const bool row_real = r < m_real;
+    const int qpos = p.q_pos0 + (row_real ? r % p.Sq : 0);  // this row's query position
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running maximum (base 2); -inf while no key was seen
+    float l = 0.f;
+    bool ok = true;
+    if (n > 0) {
+      // ---- RoPE of this row of the Q tile, in place (128-byte swizzled rows)
+      ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ));
+      if (ok && row_real) {
+        const float* cs = p.cos_tab + static_cast<long long>(qpos) * (D / 2);
+        const float* sn = p.sin_tab + static_cast<long long>(qpos) * (D / 2);
+        uint8_t* qs = smem_raw + (sbase - smem_u32(smem_raw));
+        auto chunk = [&](int col) {  // 16-byte chunk holding columns col..col+7 of row r
+          return reinterpret_cast<uint4*>(qs + (col / 64) * C::kRegionBytes +
+                                          sw128_offset(r, (col % 64) / 8));
+        };
+        auto unpack = [](uint4 v, float (&f)[8]) {
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+          }
+        };
+        auto pack = [](const float (&f)[8]) {
+          return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                            pack_bf16(f[6], f[7]));
+        };
+#pragma unroll 1
+        for (int g = 0; g < D / 16; ++g) {
+          // half-split: columns [8g, +8) pair with [D/2 + 8g, +8), frequencies 8g + k;
+          // interleaved: columns [16g, +16) hold the pairs of frequencies 8g + k
+          uint4* pa = chunk(p.rope_interleaved ? 16 * g : 8 * g);
+          uint4* pb = chunk(p.rope_interleaved ? 16 * g + 8 : D / 2 + 8 * g);
+          float a[8], bb[8], c8[8], s8[8];
+          unpack(*pa, a);
+          unpack(*pb, bb);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            c8[k] = cs[8 * g + k];
+            s8[k] = sn[8 * g + k];
+          }
+          float ya[8], yb[8];
+          if (!p.rope_interleaved) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              ya[k] = a[k] * c8[k] - bb[k] * s8[k];
+              yb[k] = bb[k] * c8[k] + a[k] * s8[k];
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              ya[2 * k] = a[2 * k] * c8[k] - a[2 * k + 1] * s8[k];
+              ya[2 * k + 1] = a[2 * k + 1] * c8[k] + a[2 * k] * s8[k];
+              yb[2 * k] = bb[2 * k] * c8[4 + k] - bb[2 * k + 1] * s8[4 + k];
+              yb[2 * k + 1] = bb[2 * k + 1] * c8[4 + k] + bb[2 * k] * s8[4 + k];
+            }
+          }
+          *pa = pack(ya);
+          *pb = pack(yb);
+        }
+      }
+      fence_async_smem();  // the rotated rows are read by the tensor core
+      mbar_arrive(smem_u32(&bar_q_rot));
+    }
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t tS = tmem + lane_base + (j & 1) * 128;
+      ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_s_full[j & 1]), (j >> 1) & 1,
+                                                abort_ptr, p.status, kSiteSFull));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t u[32], w[32];
+        tmem_ld32x2(tS + cc * 64, tS + cc * 64 + 32, u, w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[cc * 64 + i] = __uint_as_float(u[i]);
+          s[cc * 64 + 32 + i] = __uint_as_float(w[i]);
+        }
+      }
+      // keys after the row's position, or past the end of the cache, are masked
+      const int k0 = (kt0 + j) * kTile;
+      const int lim_c = qpos - k0 + 1;   // keys k0 + i with i < lim_c are visible
+      const int lim_e = p.Skv - k0;      // ... and exist
+      const int lim = lim_c < lim_e ? lim_c : lim_e;
+      if (lim < 128) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = i >= lim ? -INFINITY : s[i];
+      }
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+      for (int i = 8; i < 128; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[i + k]);
+      const float mx2 = sl2 * fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      float alpha = 1.f;
+      bool grew = false;
+      if (mx2 > m + 8.f) {  // lazy rescaling, as in the forward kernel
+        alpha = m == -INFINITY ? 0.f : ex2(m - mx2);
+        grew = true;
+        m = mx2;
+      }
+      const float msub = m == -INFINITY ? 0.f : m;  // a row with no key yet: P = 0
+      float rp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a0 = ex2(fmaf(s[hh * 64 + 2 * i], sl2, -msub));
+          const float a1 = ex2(fmaf(s[hh * 64 + 2 * i + 1], sl2, -msub));
+          rp[i & 7] += a0 + a1;
+          pk[i] = pack_bf16(a0, a1);
+        }
+        tmem_st32(tS + hh * 32, pk);
+      }
+      l = l * alpha + (((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7])));
+      // O of the previous step is complete before it is rescaled (and the softmax
+      // stays in step with the barrier's phases)
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_o_done), (j - 1) & 1, abort_ptr,
+                                                  p.status, kSiteODone));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grew)) {
+          const float f = grew ? alpha : 1.f;
+          const uint32_t tO = tmem + lane_base + C::kColO;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t u[32];
+            tmem_ld32(tO + cc * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
+            tmem_st32(tO + cc * 32, u);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p_full[j & 1]));
+    }
+    // ------------------------------------------------------------ partial result
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_o_done), (n - 1) & 1, abort_ptr,
+                                                p.status, kSiteODone));
+    const long long grow = q_row0 + r;  // the row's index among the B*Hq*Sq rows
+    if (ok) {
+      tc_fence_after();
+      const long long prow = static_cast<long long>(c) * p.rows + grow;
+      float* dst = p.part_out + prow * D;
+      const bool seen = n > 0 && l > 0.f;
+      const float inv_l = seen ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (n > 0) tmem_ld32(tmem + lane_base + C::kColO + cc * 32, u);
+        if (row_real) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dst + cc * 32)[i] =
+                n > 0 ? make_float4(__uint_as_float(u[4 * i]) * inv_l,
+                                    __uint_as_float(u[4 * i + 1]) * inv_l,
+                                    __uint_as_float(u[4 * i + 2]) * inv_l,
+                                    __uint_as_float(u[4 * i + 3]) * inv_l)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (row_real) p.part_lse[prow] = seen ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// out_i = sum_c exp(lse_c - lse) out_c, lse = ln sum_c exp(lse_c) over the chunks c;
+// one thread per 8 elements of a row.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecParams p) {
+  constexpr int T = D / 8;
+  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = t / T;
+  if (row >= p.rows) return;
+  const int e = static_cast<int>(t % T) * 8;
+  float mx = -INFINITY;
+  for (int c = 0; c < p.nchunks; ++c) mx = fmaxf(mx, p.part_lse[c * p.rows + row]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int c = 0; c < p.nchunks; ++c) {
+      const float w = expf(p.part_lse[c * p.rows + row] - mx);  // 0: a chunk without keys
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(p.part_out + (c * p.rows + row) * D + e);
+      const float4 a = src[0], bq = src[1];
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * bq.x; acc[5] += w * bq.y; acc[6] += w * bq.z; acc[7] += w * bq.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * D + e) =
+      make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+  if (e == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecParams& p, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_decode_kernel<D><<<p.nchunks * p.B * p.Hkv, kThreads, C::kSmemBytes, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>((p.rows * (D / 8) + 255) / 256);
+  decode_merge_kernel<D><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecParams& p, cudaStream_t stream) {
+  return p.D == 128 ? launch_decode_d<128>(p, stream) : launch_decode_d<64>(p, stream);
+}
+
+}  // namespace gbattn

@@ -165,4 +165,27 @@ struct BwdParams {
 inline int bwd_query_tile(int) { return 64; }
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
 
+// Decode-shape forward: Sq query rows per head at positions q_pos0 + i against a
+// cache of Skv rotated keys / values; chunks of tiles_per_chunk key tiles per CTA.
+struct DecParams {
+  CUtensorMap map_q;  // q (bf16, rotated in the kernel) rows [B*Hq*Sq, D], box {64, 128}
+  CUtensorMap map_k;  // rotated key cache (bf16) rows [B*Hkv*Skv, D], box {64, 128}
+  CUtensorMap map_v;  // value cache (bf16), same rows
+  float* part_out;    // [nchunks][rows][D] fp32: each chunk's out (divided by its row sum)
+  float* part_lse;    // [nchunks][rows]: each chunk's lse (-inf: no key seen)
+  void* out;          // [rows][D] bf16
+  float* lse;         // [rows]
+  const float* cos_tab;
+  const float* sin_tab;
+  int rope_interleaved;
+  int* status;
+  int B, Hq, Hkv, Sq, Skv, D;
+  int q_pos0;
+  int tiles_per_chunk, nchunks;
+  long long rows;     // B * Hq * Sq
+  float scale_log2;
+};
+// The chunk kernel and the merge of the chunks into out / lse.
+cudaError_t launch_decode(const DecParams& p, cudaStream_t stream);
+
 }  // namespace gbattn

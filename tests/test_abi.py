@@ -117,3 +117,13 @@ def test_partial_entry_points_reject_unaligned_blocks(built_lib):
     assert lib.attn_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 64, None) == M.ATTN_ERR_INVALID
     assert lib.attn_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 96, None) == \
         M.ATTN_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_groups_beyond_one_tile(built_lib):
+    """A K/V head's query rows (Hq/Hkv * Sq) must fit one 128-row tile."""
+    lib = built_lib
+    assert lib.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 1, 17, 256, 64, 239, 10000.0, 0,
+                           0.125, None) == M.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 1, 1, 256, 64, -1, 10000.0, 0,
+                           0.125, None) == M.ATTN_ERR_INVALID
+    assert lib.attn_rope(FAKE, FAKE, 4, 100, 0, 96, 10000.0, 0, None) == M.ATTN_ERR_UNSUPPORTED
