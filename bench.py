@@ -342,7 +342,6 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    M.profile_begin(max(4096, 2 * args.steps))
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
@@ -354,11 +353,19 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
-    M.profile_end()
-    status = M.sync_status()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = sum(step_ms) / len(step_ms)
     ms = max_over_ranks(ms_local, world)
+    # Per-kernel durations: the library's events around each launch, over a second
+    # run of the same steps (an event between two launches would hold back the
+    # programmatic early start of the second, so the timed run above records none).
+    M.profile_begin(max(4096, 2 * args.steps))
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    M.profile_end()
+    status = M.sync_status()
     kern = {}
     for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
                        (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
@@ -545,7 +552,6 @@ def run_blocks(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
-    M.profile_begin(max(4096, 16 * len(pairs) * args.steps))
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
@@ -557,9 +563,14 @@ def run_blocks(args, rank, world, local):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
+    M.profile_begin(max(4096, 16 * len(pairs) * args.steps))  # per-kernel times: a second run
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
     M.profile_end()
     status = M.sync_status()
-    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
     kern = {}
     for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
                        (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
@@ -649,7 +660,17 @@ def run_decode(args, rank, world, local):
     stream = torch.cuda.current_stream()
     graph.replay()
     torch.cuda.synchronize()
-    reps = max(1, args.steps // ncopy)
+    # A replay lasts microseconds: replay enough (>= 0.5 s) that the clock sampler
+    # sees the timed region.
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(10):
+        graph.replay()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    per_replay_s = p0.elapsed_time(p1) / 10 * 1e-3
+    reps = max(1, args.steps // ncopy, int(0.5 / max(per_replay_s, 1e-9)) + 1)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)

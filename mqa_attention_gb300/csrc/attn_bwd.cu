@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   qt_begin = qt_begin < 0 ? 0 : (qt_begin > nqt ? nqt : qt_begin);
   const int per_head = nqt - qt_begin;  // even: Sq and the offsets are multiples of 128
   const int n = Gc * per_head;          // 0: no query of the block sees these keys
-  const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   auto step_qt = [&](int s) { return qt_begin + s % per_head; };
   auto step_row = [&](int s) {
     const int h = h_first + s / per_head;
@@ -174,6 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
+  // Nothing above touched global memory: this prologue may overlap the kernel before
+  // it in the stream.
+  pdl_wait();
+  pdl_launch_dependents();
+  const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
   auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
   auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s % C::kDsBufs) * C::kDsBytes; };
 
@@ -565,8 +569,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>((p.Skv / kTile) * p.B * p.Hkv * p.hsplit);
-  attn_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p);
 }
 
 }  // namespace

@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
+  // Up to here nothing touched global memory, so this prologue may overlap the grid
+  // before it in the stream; the merge of this call may be scheduled from now on (it
+  // waits for this grid to complete before it reads the partial results).
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
@@ -221,11 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
     float l = 0.f;
     bool ok = true;
     if (n > 0) {
-      // ---- RoPE of this row of the Q tile, in place (128-byte swizzled rows)
+      // ---- RoPE of this row of the Q tile, in place (128-byte swizzled rows). The
+      // row's cos / sin values are loaded while the tile is in flight.
+      float cv[D / 2], sv[D / 2];
+      if (row_real) {
+        const float4* cs = reinterpret_cast<const float4*>(p.cos_tab + static_cast<long long>(qpos) * (D / 2));
+        const float4* sn = reinterpret_cast<const float4*>(p.sin_tab + static_cast<long long>(qpos) * (D / 2));
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          const float4 a = __ldg(cs + i), bq = __ldg(sn + i);
+          cv[4 * i] = a.x; cv[4 * i + 1] = a.y; cv[4 * i + 2] = a.z; cv[4 * i + 3] = a.w;
+          sv[4 * i] = bq.x; sv[4 * i + 1] = bq.y; sv[4 * i + 2] = bq.z; sv[4 * i + 3] = bq.w;
+        }
+      }
       ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ));
       if (ok && row_real) {
-        const float* cs = p.cos_tab + static_cast<long long>(qpos) * (D / 2);
-        const float* sn = p.sin_tab + static_cast<long long>(qpos) * (D / 2);
         uint8_t* qs = smem_raw + (sbase - smem_u32(smem_raw));
         auto chunk = [&](int col) {  // 16-byte chunk holding columns col..col+7 of row r
           return reinterpret_cast<uint4*>(qs + (col / 64) * C::kRegionBytes +
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                             pack_bf16(f[6], f[7]));
         };
-#pragma unroll 1
+#pragma unroll
         for (int g = 0; g < D / 16; ++g) {
           // half-split: columns [8g, +8) pair with [D/2 + 8g, +8), frequencies 8g + k;
           // interleaved: columns [16g, +16) hold the pairs of frequencies 8g + k
@@ -254,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           unpack(*pb, bb);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            c8[k] = cs[8 * g + k];
-            s8[k] = sn[8 * g + k];
+            c8[k] = cv[8 * g + k];
+            s8[k] = sv[8 * g + k];
           }
           float ya[8], yb[8];
           if (!p.rope_interleaved) {
@@ -399,34 +414,91 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
   }
 }
 
-// out_i = sum_c exp(lse_c - lse) out_c, lse = ln sum_c exp(lse_c) over the chunks c;
-// one thread per 8 elements of a row.
+// out_i = sum_c exp(lse_c - lse) out_c, lse = ln sum_c exp(lse_c) over the chunks c.
+// A row is served by T = D/8 element lanes (8 elements each) times L chunk lanes;
+// chunk lane l takes the chunks l, l + L, ... four at a time (their loads in flight
+// together), keeping a running maximum, weight sum and weighted sum, and the L lanes
+// of an element lane (adjacent lanes of a warp) combine theirs with shuffles.
+constexpr int kMergeL = 8;
+constexpr int kMergeThreads = 256;
+
+struct MergeAcc {
+  float m, ws, acc[8];
+};
+
+// Combines (m2, ws2, acc2) into a: both rescaled to the larger maximum.
+__device__ __forceinline__ void merge_combine(MergeAcc& a, float m2, float ws2, const float (&acc2)[8]) {
+  const float M = fmaxf(a.m, m2);
+  if (M == -INFINITY) return;  // neither side has seen a key
+  const float s1 = a.m == -INFINITY ? 0.f : expf(a.m - M);
+  const float s2 = m2 == -INFINITY ? 0.f : expf(m2 - M);
+  a.ws = a.ws * s1 + ws2 * s2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a.acc[i] = a.acc[i] * s1 + acc2[i] * s2;
+  a.m = M;
+}
+
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecParams p) {
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecParams p) {
   constexpr int T = D / 8;
-  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long row = t / T;
-  if (row >= p.rows) return;
-  const int e = static_cast<int>(t % T) * 8;
-  float mx = -INFINITY;
-  for (int c = 0; c < p.nchunks; ++c) mx = fmaxf(mx, p.part_lse[c * p.rows + row]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int c = 0; c < p.nchunks; ++c) {
-      const float w = expf(p.part_lse[c * p.rows + row] - mx);  // 0: a chunk without keys
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(p.part_out + (c * p.rows + row) * D + e);
-      const float4 a = src[0], bq = src[1];
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * bq.x; acc[5] += w * bq.y; acc[6] += w * bq.z; acc[7] += w * bq.w;
+  constexpr int L = kMergeL;
+  constexpr int U = 4;
+  static_assert((T * L) % 32 == 0, "the lanes of a row fill whole warps");
+  pdl_wait();  // the chunk grid has completed and its partial results are visible
+  const long long t = blockIdx.x * static_cast<long long>(kMergeThreads) + threadIdx.x;
+  const long long row = t / (T * L);
+  if (row >= p.rows) return;  // a row's T * L lanes fill whole warps: a warp leaves together
+  const int e = static_cast<int>(t / L % T) * 8;
+  const int l = static_cast<int>(t % L);
+  const float* lse_c = p.part_lse + row;
+  const float* out_c = p.part_out + row * D + e;
+  const long long ostride = p.rows * D;
+  MergeAcc a{-INFINITY, 0.f, {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}};
+  for (int c0 = l; c0 < p.nchunks; c0 += U * L) {
+    float lv[U];
+    float4 x[U], y[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * L;
+      lv[u] = -INFINITY;
+      x[u] = y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < p.nchunks) {
+        lv[u] = __ldcg(lse_c + c * p.rows);
+        const float4* src = reinterpret_cast<const float4*>(out_c + c * ostride);
+        x[u] = __ldcg(src);
+        y[u] = __ldcg(src + 1);
+      }
     }
+    float acc2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float m2 = -INFINITY, ws2 = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) m2 = fmaxf(m2, lv[u]);
+    if (m2 != -INFINITY) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float w = expf(lv[u] - m2);  // 0: a chunk without keys, or past the last
+        ws2 += w;
+        acc2[0] += w * x[u].x; acc2[1] += w * x[u].y; acc2[2] += w * x[u].z; acc2[3] += w * x[u].w;
+        acc2[4] += w * y[u].x; acc2[5] += w * y[u].y; acc2[6] += w * y[u].z; acc2[7] += w * y[u].w;
+      }
+    }
+    merge_combine(a, m2, ws2, acc2);
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int off = 1; off < L; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, a.m, off);
+    const float ws2 = __shfl_xor_sync(0xffffffffu, a.ws, off);
+    float acc2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc2[i] = __shfl_xor_sync(0xffffffffu, a.acc[i], off);
+    merge_combine(a, m2, ws2, acc2);
+  }
+  if (l != 0) return;
+  const float inv = a.ws > 0.f ? 1.f / a.ws : 0.f;
   *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * D + e) =
-      make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                 pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-  if (e == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+      make_uint4(pack_bf16(a.acc[0] * inv, a.acc[1] * inv), pack_bf16(a.acc[2] * inv, a.acc[3] * inv),
+                 pack_bf16(a.acc[4] * inv, a.acc[5] * inv), pack_bf16(a.acc[6] * inv, a.acc[7] * inv));
+  if (e == 0) p.lse[row] = a.ws > 0.f ? a.m + logf(a.ws) : -INFINITY;
 }
 
 template <int D>
@@ -435,11 +507,13 @@ cudaError_t launch_decode_d(const DecParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_decode_kernel<D><<<p.nchunks * p.B * p.Hkv, kThreads, C::kSmemBytes, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((p.rows * (D / 8) + 255) / 256);
-  decode_merge_kernel<D><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(attn_decode_kernel<D>, dim3(static_cast<unsigned>(p.nchunks * p.B * p.Hkv)),
+                 dim3(kThreads), C::kSmemBytes, stream, p);
+  if (e != cudaSuccess) return e;
+  const long long mthreads = p.rows * (D / 8) * kMergeL;
+  return launch_pdl(decode_merge_kernel<D>,
+                    dim3(static_cast<unsigned>((mthreads + kMergeThreads - 1) / kMergeThreads)),
+                    dim3(kMergeThreads), 0, stream, p);
 }
 
 }  // namespace

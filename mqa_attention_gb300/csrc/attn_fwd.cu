@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
+  // Nothing above touched global memory: this prologue may overlap the kernel before
+  // it in the stream.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
@@ -387,8 +391,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int nq = p.Sq / kTile;
   const unsigned grid = static_cast<unsigned>(((nq + 1) / 2) * p.B * p.Hq);
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p);
 }
 
 }  // namespace

@@ -28,6 +28,14 @@ GB_DEV uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A grid launched with programmatic stream serialisation may start while the grid
+// before it in the stream is still running; pdl_wait blocks until that grid has
+// completed and its memory writes are visible (it returns at once otherwise), and
+// pdl_launch_dependents lets the next grid in the stream start early.
+GB_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+GB_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 GB_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

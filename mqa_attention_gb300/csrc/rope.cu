@@ -16,6 +16,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace gbattn {
 namespace {
@@ -24,6 +25,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict__ sin_tab, int S,
                                   int D, double theta) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   const int half = D / 2;
   const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= (long long)S * half) return;
@@ -116,6 +119,8 @@ __device__ __forceinline__ void store8_bf16_scaled_f16(void* p, const float (&o)
 // orders like the value, so the maximum is taken on the 15-bit magnitudes of
 // packed pairs (__vmaxu2) and converted back to float once per thread.
 __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   __shared__ uint32_t red[4][8];
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -167,6 +172,8 @@ __global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
 // in the backward, lse * log2 e = +inf so that their probabilities are 0).
 template <int D, bool kBwd, bool kPad>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -272,6 +279,8 @@ __global__ void __launch_bounds__(256)
                        int S, int Sp, int pos0, float scale, const float* __restrict__ maxes,
                        const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
                        int rope_interleaved) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   constexpr int T = D / 16;
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -320,6 +329,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
     merge_kernel(const void* oa, const float* la, const void* ob, const float* lb, void* o,
                  float* l, long long rows) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   constexpr int T = D / 8;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row = t / T;
@@ -355,6 +366,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     unpad_rows_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst, long long rows,
                       int S, int Sp, int words, int to_bf16) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const int per_row = to_bf16 ? words / 2 : words;
   const long long row = t / per_row;
@@ -374,6 +387,8 @@ __global__ void __launch_bounds__(256)
 // y = bf16(x), nearest even; n a multiple of 8.
 __global__ void __launch_bounds__(256)
     f32_to_bf16_kernel(const float* __restrict__ x, void* __restrict__ y, long long n8) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (t >= n8) return;
   float v[8];
@@ -388,20 +403,20 @@ long long blocks_for(long long threads) { return (threads + 255) / 256; }
 cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
                               cudaStream_t stream) {
   const long long n = (long long)S * (D / 2);
-  rope_table_kernel<<<(unsigned)blocks_for(n), 256, 0, stream>>>(cos_tab, sin_tab, S, D, theta);
-  return cudaGetLastError();
+  return launch_pdl(rope_table_kernel, dim3((unsigned)blocks_for(n)), dim3(256), 0, stream, cos_tab,
+                    sin_tab, S, D, theta);
 }
 
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
-  absmax_kernel<<<152 * 8, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(absmax_kernel, dim3(152 * 8), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
   const long long threads = (p.seg[0].rows + p.seg[1].rows) * (p.D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
   const bool pad = p.seg[0].S != p.seg[0].Sp || p.seg[1].S != p.seg[1].Sp;
-#define GB_PREP(DD, BW, PD) row_prep_kernel<DD, BW, PD><<<grid, 256, 0, stream>>>(p)
+#define GB_PREP(DD, BW, PD) \
+  return launch_pdl(row_prep_kernel<DD, BW, PD>, dim3(grid), dim3(256), 0, stream, p)
   if (p.D == 128) {
     if (p.bwd) { if (pad) GB_PREP(128, true, true); else GB_PREP(128, true, false); }
     else { if (pad) GB_PREP(128, false, true); else GB_PREP(128, false, false); }
@@ -410,7 +425,6 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
     else { if (pad) GB_PREP(64, false, true); else GB_PREP(64, false, false); }
   }
 #undef GB_PREP
-  return cudaGetLastError();
 }
 
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
@@ -418,9 +432,9 @@ cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long 
                                const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
-#define GB_FIN(DD, BF)                                                                   \
-  dq_finalize_kernel<DD, BF><<<grid, 256, 0, stream>>>(dqacc, dq, rows, S, Sp, pos0, scale,   \
-                                                       maxes, cos_tab, sin_tab, rope_interleaved)
+#define GB_FIN(DD, BF)                                                                       \
+  return launch_pdl(dq_finalize_kernel<DD, BF>, dim3(grid), dim3(256), 0, stream, dqacc, dq, rows, \
+                    S, Sp, pos0, scale, maxes, cos_tab, sin_tab, rope_interleaved)
   if (D == 128) {
     if (dq_bf16) GB_FIN(128, true);
     else GB_FIN(128, false);
@@ -429,32 +443,29 @@ cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long 
     else GB_FIN(64, false);
   }
 #undef GB_FIN
-  return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb, void* o,
                          float* l, long long rows, int D, cudaStream_t stream) {
   const unsigned grid = (unsigned)blocks_for(rows * (D / 8));
-  if (D == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
-  else merge_kernel<64><<<grid, 256, 0, stream>>>(oa, la, ob, lb, o, l, rows);
-  return cudaGetLastError();
+  if (D == 128) return launch_pdl(merge_kernel<128>, dim3(grid), dim3(256), 0, stream, oa, la, ob, lb, o, l, rows);
+  return launch_pdl(merge_kernel<64>, dim3(grid), dim3(256), 0, stream, oa, la, ob, lb, o, l, rows);
 }
 
 cudaError_t launch_unpad_rows(const void* src, void* dst, long long rows, int S, int Sp, int words,
                               bool to_bf16, cudaStream_t stream) {
   const long long n = rows * (to_bf16 ? words / 2 : words);
   if (n == 0) return cudaSuccess;
-  unpad_rows_kernel<<<(unsigned)blocks_for(n), 256, 0, stream>>>(
-      static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, S, Sp, words,
-      to_bf16 ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(unpad_rows_kernel, dim3((unsigned)blocks_for(n)), dim3(256), 0, stream,
+                    static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, S, Sp,
+                    words, to_bf16 ? 1 : 0);
 }
 
 cudaError_t launch_f32_to_bf16(const float* x, void* y, long long n, cudaStream_t stream) {
   const long long n8 = n / 8;
   if (n8 == 0) return cudaSuccess;
-  f32_to_bf16_kernel<<<(unsigned)blocks_for(n8), 256, 0, stream>>>(x, y, n8);
-  return cudaGetLastError();
+  return launch_pdl(f32_to_bf16_kernel, dim3((unsigned)blocks_for(n8)), dim3(256), 0, stream, x, y,
+                    n8);
 }
 
 }  // namespace gbattn

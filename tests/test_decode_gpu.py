@@ -50,6 +50,10 @@ DECODE = [
     (1, 4, 4, 2, 300, 64, 298, "half"),        # MHA
     (1, 8, 2, 3, 777, 128, 500, "interleaved"),  # queries mid-cache: later keys masked
     (1, 2, 1, 1, 1, 64, 0, "half"),            # a single cached key
+    (1, 8, 1, 8, 256, 64, 124, "half"),        # rows 124..127 see no key of the second chunk
+    (1, 8, 1, 1, 65536, 64, 65535, "half"),    # one cache over 128 chunks: a long merge
+    (1, 32, 8, 4, 32768, 128, 32764, "half"),  # the S = 32768 decode line, four new tokens
+    (8, 8, 1, 16, 2048, 64, 2032, "half"),     # PaLM MQA, 16 new tokens: 128 rows per tile
 ]
 
 
