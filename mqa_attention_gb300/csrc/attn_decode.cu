@@ -26,6 +26,7 @@
 // TMEM: S_0 [0,128), S_1 [128,256), O [256, 256 + D).
 #include "kernels.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace gbattn {
 namespace {
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
         for (int g = 0; g < D / 16; ++g) {
           // half-split: columns [8g, +8) pair with [D/2 + 8g, +8), frequencies 8g + k;
           // interleaved: columns [16g, +16) hold the pairs of frequencies 8g + k
-          uint4* pa = chunk(p.rope_interleaved ? 16 * g : 8 * g);
-          uint4* pb = chunk(p.rope_interleaved ? 16 * g + 8 : D / 2 + 8 * g);
+          uint4* pa = chunk(rope_off_a(g, p.rope_interleaved != 0));
+          uint4* pb = chunk(rope_off_b(g, D, p.rope_interleaved != 0));
           float a[8], bb[8], c8[8], s8[8];
           unpack(*pa, a);
           unpack(*pb, bb);
@@ -273,21 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
             s8[k] = sv[8 * g + k];
           }
           float ya[8], yb[8];
-          if (!p.rope_interleaved) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              ya[k] = a[k] * c8[k] - bb[k] * s8[k];
-              yb[k] = bb[k] * c8[k] + a[k] * s8[k];
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              ya[2 * k] = a[2 * k] * c8[k] - a[2 * k + 1] * s8[k];
-              ya[2 * k + 1] = a[2 * k + 1] * c8[k] + a[2 * k] * s8[k];
-              yb[2 * k] = bb[2 * k] * c8[4 + k] - bb[2 * k + 1] * s8[4 + k];
-              yb[2 * k + 1] = bb[2 * k + 1] * c8[4 + k] + bb[2 * k] * s8[4 + k];
-            }
-          }
+          rope_rotate16(a, bb, c8, s8, p.rope_interleaved != 0, 1.f, ya, yb);
           *pa = pack(ya);
           *pb = pack(yb);
         }

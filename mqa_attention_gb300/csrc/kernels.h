@@ -87,6 +87,7 @@ struct AbsMaxParams {
   const void* x[4];
   long long n[4];  // element counts, multiples of 8
   float* maxes;
+  int blk0[5];     // CTAs [blk0[t], blk0[t+1]) read tensor t (set by launch_absmax)
 };
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream);
 

@@ -17,6 +17,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace gbattn {
 namespace {
@@ -37,36 +38,6 @@ __global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict
   sincos(static_cast<double>(p) * inv_freq, &s, &c);
   cos_tab[idx] = static_cast<float>(c);
   sin_tab[idx] = static_cast<float>(s);
-}
-
-// Element offsets (within a row) of the two 8-element groups a thread holds
-// for its chunk c < D/16, and their rotation. Half-split: elements [8c, 8c+8)
-// and [D/2 + 8c, +8), pairs (a_i, b_i) at frequency 8c + i. Interleaved:
-// elements [16c, 16c+16), pairs (a_2j, a_2j+1) at frequency 8c + j and
-// (b_2j, b_2j+1) at 8c + 4 + j. Both use the table entries [8c, 8c+8) of the
-// row's position; sgn = 1 rotates by +angle, -1 by -angle (the transpose).
-__device__ __forceinline__ int rope_off_a(int c, bool inter) { return inter ? 16 * c : 8 * c; }
-__device__ __forceinline__ int rope_off_b(int c, int D, bool inter) {
-  return inter ? 16 * c + 8 : D / 2 + 8 * c;
-}
-__device__ __forceinline__ void rotate16(const float (&a)[8], const float (&b)[8],
-                                         const float (&cs)[8], const float (&sn)[8], bool inter,
-                                         float sgn, float (&ya)[8], float (&yb)[8]) {
-  if (!inter) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      ya[i] = a[i] * cs[i] - sgn * (b[i] * sn[i]);
-      yb[i] = b[i] * cs[i] + sgn * (a[i] * sn[i]);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      ya[2 * j] = a[2 * j] * cs[j] - sgn * (a[2 * j + 1] * sn[j]);
-      ya[2 * j + 1] = a[2 * j + 1] * cs[j] + sgn * (a[2 * j] * sn[j]);
-      yb[2 * j] = b[2 * j] * cs[4 + j] - sgn * (b[2 * j + 1] * sn[4 + j]);
-      yb[2 * j + 1] = b[2 * j + 1] * cs[4 + j] + sgn * (b[2 * j] * sn[4 + j]);
-    }
-  }
 }
 
 struct alignas(16) Vec8x16 {
@@ -117,50 +88,52 @@ __device__ __forceinline__ void store8_bf16_scaled_f16(void* p, const float (&o)
 
 // Largest |x| of bf16 tensors. For a non-negative bf16 value the bit pattern
 // orders like the value, so the maximum is taken on the 15-bit magnitudes of
-// packed pairs (__vmaxu2) and converted back to float once per thread.
-__global__ void __launch_bounds__(256) absmax_kernel(const AbsMaxParams p) {
+// packed pairs (__vmaxu2) and converted back to float once per CTA. The CTAs are
+// shared out among the tensors in proportion to their sizes; each reads one
+// contiguous slab of its tensor, eight 16-byte loads in flight per thread.
+constexpr int kAbsMaxThreads = 256;
+constexpr int kAbsMaxUnroll = 8;
+
+__global__ void __launch_bounds__(kAbsMaxThreads) absmax_kernel(const AbsMaxParams p) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
-  __shared__ uint32_t red[4][8];
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long t0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  uint32_t m[4] = {0u, 0u, 0u, 0u};
-#pragma unroll 1
-  for (int t = 0; t < 4; ++t) {
-    if (p.x[t] == nullptr) continue;
-    const uint4* src = static_cast<const uint4*>(p.x[t]);
-    const long long chunks = p.n[t] / 8;
-    uint32_t acc = 0u;
-    long long c = t0;
-    for (; c + 3 * stride < chunks; c += 4 * stride) {
-      const uint4 a = __ldg(src + c), b = __ldg(src + c + stride);
-      const uint4 d = __ldg(src + c + 2 * stride), g = __ldg(src + c + 3 * stride);
-      const uint4 v[4] = {a, b, d, g};
+  __shared__ uint32_t red[kAbsMaxThreads / 32];
+  const int blk = static_cast<int>(blockIdx.x);
+  // the CTA's tensor t (selected without indexing the parameter arrays at run time)
+  const int t = blk >= p.blk0[3] ? 3 : blk >= p.blk0[2] ? 2 : blk >= p.blk0[1] ? 1 : 0;
+  auto pick = [t](auto a0, auto a1, auto a2, auto a3) {
+    return t == 0 ? a0 : t == 1 ? a1 : t == 2 ? a2 : a3;
+  };
+  const long long chunks = pick(p.n[0], p.n[1], p.n[2], p.n[3]) / 8;
+  const int b0 = pick(p.blk0[0], p.blk0[1], p.blk0[2], p.blk0[3]);
+  const int b1 = pick(p.blk0[1], p.blk0[2], p.blk0[3], p.blk0[4]);
+  const long long per = (chunks + (b1 - b0) - 1) / (b1 - b0);
+  const long long lo = (blk - b0) * per;
+  const long long hi = lo + per < chunks ? lo + per : chunks;
+  const uint4* src = static_cast<const uint4*>(pick(p.x[0], p.x[1], p.x[2], p.x[3]));
+  uint32_t acc = 0u;
+  for (long long c0 = lo + threadIdx.x; c0 < hi; c0 += kAbsMaxThreads * kAbsMaxUnroll) {
+    uint4 v[kAbsMaxUnroll];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu),
-                                     __vmaxu2(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu)));
+    for (int u = 0; u < kAbsMaxUnroll; ++u) {
+      const long long c = c0 + u * kAbsMaxThreads;
+      v[u] = c < hi ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; c < chunks; c += stride) {
-      const uint4 a = __ldg(src + c);
-      acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(a.x & 0x7fff7fffu, a.y & 0x7fff7fffu),
-                                   __vmaxu2(a.z & 0x7fff7fffu, a.w & 0x7fff7fffu)));
-    }
-    m[t] = max(acc & 0xffffu, acc >> 16);
-  }
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m[t] = max(m[t], __shfl_xor_sync(0xffffffffu, m[t], o));
-    if ((threadIdx.x & 31) == 0) red[t][threadIdx.x >> 5] = m[t];
+    for (int u = 0; u < kAbsMaxUnroll; ++u)
+      acc = __vmaxu2(acc, __vmaxu2(__vmaxu2(v[u].x & 0x7fff7fffu, v[u].y & 0x7fff7fffu),
+                                   __vmaxu2(v[u].z & 0x7fff7fffu, v[u].w & 0x7fff7fffu)));
   }
+  uint32_t m = max(acc & 0xffffu, acc >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
-  if (threadIdx.x < 4) {
-    const int t = threadIdx.x;
+  if (threadIdx.x == 0) {
     uint32_t b = 0u;
-    for (int w = 0; w < 8; ++w) b = max(b, red[t][w]);
+    for (int w = 0; w < kAbsMaxThreads / 32; ++w) b = max(b, red[w]);
     // bf16 magnitude bits -> float bits; non-negative floats order like their bits
-    if (p.x[t] != nullptr) atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), b << 16);
+    atomicMax(reinterpret_cast<unsigned int*>(p.maxes + t), b << 16);
   }
 }
 
@@ -204,7 +177,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
   load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
   load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
-  rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
+  rope_rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
   if (!real) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) y1[k] = y2[k] = 0.f;
@@ -305,7 +278,7 @@ __global__ void __launch_bounds__(256)
   load8(dqacc + a2, x2);
   load8(cos_tab + (long long)pos * H + 8 * c, cs);
   load8(sin_tab + (long long)pos * H + 8 * c, sn);
-  rotate16(x1, x2, cs, sn, inter, -1.f, y1, y2);  // transpose: rotation by -angle
+  rope_rotate16(x1, x2, cs, sn, inter, -1.f, y1, y2);  // transpose: rotation by -angle
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     y1[i] *= f;
@@ -407,8 +380,25 @@ cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, doub
                     sin_tab, S, D, theta);
 }
 
-cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream) {
-  return launch_pdl(absmax_kernel, dim3(152 * 8), dim3(256), 0, stream, p);
+cudaError_t launch_absmax(const AbsMaxParams& p_in, cudaStream_t stream) {
+  // About 8 CTAs per SM over all tensors, at least one per present tensor and
+  // none for an absent one (its slab is empty).
+  AbsMaxParams p = p_in;
+  long long total = 0;
+  for (int t = 0; t < 4; ++t) total += p.x[t] ? p.n[t] : 0;
+  const long long want = 152 * 8;
+  p.blk0[0] = 0;
+  for (int t = 0; t < 4; ++t) {
+    long long nb = 0;
+    if (p.x[t] && p.n[t] > 0) {
+      nb = total > 0 ? (want * p.n[t] + total - 1) / total : 1;
+      nb = nb < 1 ? 1 : nb;
+    }
+    p.blk0[t + 1] = p.blk0[t] + static_cast<int>(nb);
+  }
+  if (p.blk0[4] == 0) return cudaSuccess;
+  return launch_pdl(absmax_kernel, dim3(static_cast<unsigned>(p.blk0[4])), dim3(kAbsMaxThreads),
+                    0, stream, p);
 }
 
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {

@@ -318,3 +318,26 @@ def test_gpu_rejects_unsupported():
     with pytest.raises(M.AttnError) as e:
         M.attn_fwd(dev["q"], dev["k"], dev["v"], out, lse, 1, 2, 1, 128, 96, 1e4, 0.125, True)
     assert e.value.code == M.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("D,hkv", [(128, 2), (64, 1)])
+def test_power_of_two_input_scales_are_exact(D, hkv):
+    """The backward's fp16 operands carry per-tensor power-of-two scales chosen
+    from the inputs' abs-maxima. Scaling q by 2^4, k by 2^-4 (scores unchanged),
+    v by 2^6 and dO by 2^-10 must then scale every result by an exact power of
+    two: out 2^6, lse 1, dv 2^-10, dk 2^(-4+4), dq 2^(-4-4). out, lse, dk and dv
+    are compared bit for bit (they are summed in a fixed order); dq, whose
+    partial sums land in a run-dependent order, to fp32 rounding."""
+    B, Hq, S, theta = 1, 8, 512, 500000.0 if D == 128 else 10000.0
+    wl = Workload(300 + D, "scaled", B, Hq, hkv, S, D, theta, True)
+    dev, _ = gen(wl)
+    base = run_gpu(wl, dev)
+    sc = {"q": 2.0 ** 4, "k": 2.0 ** -4, "v": 2.0 ** 6, "dout": 2.0 ** -10}
+    dev2 = {n: (t.float() * sc[n]).to(torch.bfloat16) for n, t in dev.items()}
+    got = run_gpu(wl, dev2)
+    assert torch.equal(got["out"], base["out"] * 2.0 ** 6)
+    assert torch.equal(got["lse"], base["lse"])
+    assert torch.equal(got["dv"], base["dv"] * 2.0 ** -10)
+    assert torch.equal(got["dk"], base["dk"])
+    want = base["dq"] * 2.0 ** -8
+    assert ((got["dq"] - want).abs() <= want.abs() * 2.0 ** -20 + 1e-12).all()
