@@ -298,6 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       ok = wait(smem_u32(&bar_ds_full[buf]), (s >> 1) & 1, kSiteDsFull);
       if (!ok) break;
       tc_fence_after();
+      if constexpr (!C::kDqPair) {
+        // dQᵀ(s) first: its drain then overlaps dV/dK(s) and Sᵀ(s+2), and is done
+        // before dPᵀ(s+2) needs the columns (dPᵀ(s) was consumed by the softmax)
+        issue_dq(s);
+        mma_commit_w(smem_u32(&bar_dq_full[buf]));
+      }
       issue_dvdk(s, s == 0);
       mma_commit_w(smem_u32(&bar_stage_empty[s % C::kStages]));
       if constexpr (C::kDqPair) {
@@ -309,9 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           issue_dq(s);
           mma_commit_w(smem_u32(&bar_dq_full[0]));
         }
-      } else {
-        issue_dq(s);
-        mma_commit_w(smem_u32(&bar_dq_full[buf]));
       }
       if (s + 2 < n) {
         ok = wait(smem_u32(&bar_stage_full[(s + 2) % C::kStages]), ((s + 2) / C::kStages) & 1,
