@@ -457,6 +457,26 @@ def run_ours(args, rank, world, local):
                 "traffic": ncu_traffic(dom[0], wl.name),
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "step_frac_of_peak": value / world / peak_tf}
+    # the backward prologue (abs-max pass + row pass) is HBM-bound: its algorithmic bytes
+    # against the measured copy bandwidth
+    prologue = None
+    if "bwd_prep" in kern:
+        qb = wl.B * wl.Hq * wl.S * wl.D * 2       # one bf16 / fp16 [B,Hq,S,D] tensor
+        kb = wl.B * wl.Hkv * wl.S * wl.D * 2      # one bf16 / fp16 [B,Hkv,S,D] tensor
+        rb = wl.B * wl.Hq * wl.S * 4              # one fp32 [B,Hq,S] row vector
+        nbytes = (2 * qb + 2 * kb) + (3 * qb + 2 * kb + rb) + (2 * qb + 2 * kb + 2 * qb + 2 * rb)
+        gbs = nbytes / (kern["bwd_prep"]["avg_ms"] * 1e-3) / 1e9
+        prologue = {"kernel": "bwd_prep (abs-max pass + row pass)", "bound": "hbm",
+                    "bytes": nbytes, "achieved": gbs, "peak": peak_hbm, "unit": "GB/s",
+                    "frac": gbs / peak_hbm,
+                    "reads": "abs-max: q, k, v, dO; row pass: q, k, v, dO, out, lse",
+                    "writes": "fp16 q~, k~, v, dO; zeroed fp32 dQ accumulator; delta; lse*log2e"}
+    passes = {}
+    if "attn_fwd" in kern:
+        passes["fwd"] = kern["attn_fwd"]["avg_ms"] + kern.get("rope", {"avg_ms": 0.0})["avg_ms"]
+    if "attn_bwd_main" in kern:
+        passes["bwd"] = sum(kern[k]["avg_ms"] for k in ("bwd_prep", "attn_bwd_main", "dq_finalize")
+                            if k in kern)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         tf, heads, secs = oracle_sample_heads(wl, host)
@@ -477,6 +497,8 @@ def run_ours(args, rank, world, local):
                           "copy streams, overlapped with the neighbouring steps' compute"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
+        "prologue_roofline": prologue,
+        "passes_ms": {k: round(v, 5) for k, v in passes.items()},
         "kernels_ms": {n: round(d["avg_ms"], 5) for n, d in kern.items()},
         "cpu_baseline": cpu,
         "clocks": clocks,
