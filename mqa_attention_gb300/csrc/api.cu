@@ -111,6 +111,20 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, int D, int box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 matrix [rows][cols], 128-byte swizzled boxes of {32 columns, 128 rows}.
+bool make_map_f32(CUtensorMap* m, const void* ptr, long long rows, int cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -440,7 +454,9 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   ok = ok && make_map(&bp.map_q, qr, qrows_p, D, bq, true) &&
        make_map(&bp.map_do, dos, qrows_p, D, bq, true) &&
        make_map(&bp.map_k, kr, krows_p, D, kTile, true) &&
-       make_map(&bp.map_v, vs, krows_p, D, kTile, true);
+       make_map(&bp.map_v, vs, krows_p, D, kTile, true) &&
+       make_map_f32(&bp.map_dk, dk, krows_p, D) && make_map_f32(&bp.map_dv, dv, krows_p, D) &&
+       make_map_f32(&bp.map_cos, cs, npos, D / 2) && make_map_f32(&bp.map_sin, sn, npos, D / 2);
   if (ok) {
     bp.lse2 = lse2;
     bp.delta = delta;

@@ -56,7 +56,7 @@ constexpr int kWarpMma = 13;
 
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
-  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25
+  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteTab = 26
 };
 
 template <int D>
@@ -84,6 +84,16 @@ struct BwdCfg {
   static constexpr uint32_t kColDK = 384;
   static_assert(kColDK + D <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // Epilogue staging, in the shared memory the main loop used: the cos and sin rows
+  // of the tile's keys, then dV and dK, as 128-byte swizzled boxes of 32 fp32
+  // columns x 128 rows (the TMA layout).
+  static constexpr int kBoxBytes = 128 * 128;
+  static constexpr int kTabBoxes = D / 64;  // boxes per table row set (D/2 floats)
+  static constexpr int kEpiCos = 0;
+  static constexpr int kEpiSin = kTabBoxes * kBoxBytes;
+  static constexpr int kEpiDv = 2 * kTabBoxes * kBoxBytes;
+  static constexpr int kEpiDk = kEpiDv + (D / 32) * kBoxBytes;
+  static_assert(kEpiDk + (D / 32) * kBoxBytes <= kDsOff + kDsBufs * kDsBytes, "epilogue staging");
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -93,19 +103,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Writes 4 consecutive floats, or adds them (fp32 reduction) when several CTAs
-// contribute to the same row.
-__device__ __forceinline__ void put4(float* dst, float a, float b, float c, float d, bool add) {
-  if (add) red_add_v4_f32(dst, a, b, c, d);
-  else *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never, bar_tab;
   __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
   __shared__ uint32_t tmem_slot;
@@ -156,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(smem_u32(&bar_done), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     mbar_init(smem_u32(&bar_never), 1);
+    mbar_init(smem_u32(&bar_tab), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_stage_full[s]), 1);
       mbar_init(smem_u32(&bar_stage_empty[s]), 1);
@@ -481,78 +486,116 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    } else if (half == 0) {
-      // dV accumulated Pᵀ (dO 2^edo)
-      const float f = exp2i(-ex.dout);
-      float* dst = p.dv + grow * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          put4(dst + cc * 32 + 4 * i, f * __uint_as_float(u[4 * i]),
-               f * __uint_as_float(u[4 * i + 1]), f * __uint_as_float(u[4 * i + 2]),
-               f * __uint_as_float(u[4 * i + 3]), sum_parts);
-      }
     } else {
-      // dk = scale * R_keyᵀ dk~ (rotation by -angle); dK
-      // accumulated (dS 2^(edo+ev)) (q~ 2^eq)
-      const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
-      float* dst = p.dk + grow * D;
-      const float* cs = p.cos_tab + (long long)key * (D / 2);
-      const float* sn = p.sin_tab + (long long)key * (D / 2);
-      if (p.rope_interleaved) {
-        // complex pairs (2j, 2j+1) at frequency j: columns [64 ch, 64 ch + 64) hold
-        // the frequencies [32 ch, 32 ch + 32)
+      // Rows go to shared memory (conflict-free swizzled 16-byte chunks) and leave in
+      // 128-row TMA tiles (added into the rows when two CTAs share the key tile), so
+      // that no warp issues scattered row-per-thread stores.
+      auto at = [&](uint32_t base, int col) {  // fp32 column col of this thread's row
+        return base + static_cast<uint32_t>((col / 32) * C::kBoxBytes + r * 128 +
+                                            ((((col % 32) / 4) ^ (r & 7)) << 4));
+      };
+      const uint32_t tcos = sbase + C::kEpiCos, tsin = sbase + C::kEpiSin;
+      const uint32_t stage = sbase + (half == 0 ? C::kEpiDv : C::kEpiDk);
+      if (half == 0) {
+        // dV accumulated Pᵀ (dO 2^edo)
+        const float f = exp2i(-ex.dout);
 #pragma unroll 1
-        for (int ch = 0; ch < D / 64; ++ch) {
-          uint32_t x1[32], x2[32];
-          tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 64,
-                      tmem + lane_base + C::kColDK + ch * 64 + 32, x1, x2);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + C::kColDV + cc * 32, u);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
-            const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
-            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = 8 * (i & 3) + 2 * e;
-              const float xe = __uint_as_float(i < 4 ? x1[k] : x2[k]);
-              const float xo = __uint_as_float(i < 4 ? x1[k + 1] : x2[k + 1]);
-              y[2 * e] = f * (xe * cc[e] + xo * ss[e]);
-              y[2 * e + 1] = f * (xo * cc[e] - xe * ss[e]);
-            }
-            put4(dst + ch * 64 + 8 * i, y[0], y[1], y[2], y[3], sum_parts);
-            put4(dst + ch * 64 + 8 * i + 4, y[4], y[5], y[6], y[7], sum_parts);
-          }
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(at(stage, cc * 32 + 4 * i), __float_as_uint(f * __uint_as_float(u[4 * i])),
+                         __float_as_uint(f * __uint_as_float(u[4 * i + 1])),
+                         __float_as_uint(f * __uint_as_float(u[4 * i + 2])),
+                         __float_as_uint(f * __uint_as_float(u[4 * i + 3])));
         }
       } else {
-#pragma unroll 1
-        for (int ch = 0; ch < D / 64; ++ch) {
-          uint32_t x1[32], x2[32];
-          tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 32,
-                      tmem + lane_base + C::kColDK + D / 2 + ch * 32, x1, x2);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 c4 = reinterpret_cast<const float4*>(cs + ch * 32)[i];
-            const float4 s4 = reinterpret_cast<const float4*>(sn + ch * 32)[i];
-            const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-            const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
-            float y1[4], y2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a = __uint_as_float(x1[4 * i + e]);
-              const float bb = __uint_as_float(x2[4 * i + e]);
-              y1[e] = f * (a * cc[e] + bb * ss[e]);
-              y2[e] = f * (bb * cc[e] - a * ss[e]);
-            }
-            put4(dst + ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3], sum_parts);
-            put4(dst + D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3], sum_parts);
+        // dk = scale * R_keyᵀ dk~ (rotation by -angle); dK accumulated
+        // (dS 2^(edo+ev)) (q~ 2^eq). The cos / sin rows of the tile's keys arrive by TMA.
+        if (r == 0) {
+          mbar_arrive_expect_tx(smem_u32(&bar_tab), 2 * C::kTabBoxes * C::kBoxBytes);
+          for (int bx = 0; bx < C::kTabBoxes; ++bx) {
+            tma_load_2d(tcos + bx * C::kBoxBytes, &p.map_cos, bx * 32, k0p, smem_u32(&bar_tab));
+            tma_load_2d(tsin + bx * C::kBoxBytes, &p.map_sin, bx * 32, k0p, smem_u32(&bar_tab));
           }
         }
+        const float f = p.scale * exp2i(-(ex.dout + ex.v + ex.q));
+        const bool got = bounded_wait(smem_u32(&bar_tab), 0, abort_ptr, p.status, kSiteTab);
+        if (got) {
+          auto tab4 = [&](uint32_t base, int fq, float (&o)[4]) {  // frequencies fq..fq+3
+            uint32_t w0, w1, w2, w3;
+            ld_shared_v4(at(base, fq), w0, w1, w2, w3);
+            o[0] = __uint_as_float(w0); o[1] = __uint_as_float(w1);
+            o[2] = __uint_as_float(w2); o[3] = __uint_as_float(w3);
+          };
+          auto put = [&](int col, float a, float b, float c, float d) {
+            st_shared_v4(at(stage, col), __float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
+                         __float_as_uint(d));
+          };
+          if (p.rope_interleaved) {
+            // complex pairs (2j, 2j+1) at frequency j: columns [64 ch, 64 ch + 64) hold
+            // the frequencies [32 ch, 32 ch + 32)
+#pragma unroll 1
+            for (int ch = 0; ch < D / 64; ++ch) {
+              uint32_t x1[32], x2[32];
+              tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 64,
+                          tmem + lane_base + C::kColDK + ch * 64 + 32, x1, x2);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float cc[4], ss[4];
+                tab4(tcos, ch * 32 + 4 * i, cc);
+                tab4(tsin, ch * 32 + 4 * i, ss);
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int k = 8 * (i & 3) + 2 * e;
+                  const float xe = __uint_as_float(i < 4 ? x1[k] : x2[k]);
+                  const float xo = __uint_as_float(i < 4 ? x1[k + 1] : x2[k + 1]);
+                  y[2 * e] = f * (xe * cc[e] + xo * ss[e]);
+                  y[2 * e + 1] = f * (xo * cc[e] - xe * ss[e]);
+                }
+                put(ch * 64 + 8 * i, y[0], y[1], y[2], y[3]);
+                put(ch * 64 + 8 * i + 4, y[4], y[5], y[6], y[7]);
+              }
+            }
+          } else {
+#pragma unroll 1
+            for (int ch = 0; ch < D / 64; ++ch) {
+              uint32_t x1[32], x2[32];
+              tmem_ld32x2(tmem + lane_base + C::kColDK + ch * 32,
+                          tmem + lane_base + C::kColDK + D / 2 + ch * 32, x1, x2);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float cc[4], ss[4];
+                tab4(tcos, ch * 32 + 4 * i, cc);
+                tab4(tsin, ch * 32 + 4 * i, ss);
+                float y1[4], y2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float a = __uint_as_float(x1[4 * i + e]);
+                  const float bb = __uint_as_float(x2[4 * i + e]);
+                  y1[e] = f * (a * cc[e] + bb * ss[e]);
+                  y2[e] = f * (bb * cc[e] - a * ss[e]);
+                }
+                put(ch * 32 + 4 * i, y1[0], y1[1], y1[2], y1[3]);
+                put(D / 2 + ch * 32 + 4 * i, y2[0], y2[1], y2[2], y2[3]);
+              }
+            }
+          }
+        }
+      }
+      // this half's 128 rows are staged: one thread stores (or adds) the tiles
+      fence_async_smem();
+      named_bar_sync(1 + half, 128);
+      if (r == 0) {
+        const CUtensorMap* map = half == 0 ? &p.map_dv : &p.map_dk;
+        for (int bx = 0; bx < D / 32; ++bx) {
+          if (sum_parts) tma_reduce_add_2d(map, bx * 32, kv_row, stage + bx * C::kBoxBytes);
+          else tma_store_2d(map, bx * 32, kv_row, stage + bx * C::kBoxBytes);
+        }
+        bulk_commit();
+        bulk_wait_read_all();  // the tiles have left shared memory before the CTA ends
       }
     }
   }

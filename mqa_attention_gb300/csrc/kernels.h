@@ -166,6 +166,10 @@ struct BwdParams {
   CUtensorMap map_do;  // scaled dout (fp16), box {64, BQ}
   CUtensorMap map_k;   // scaled rotated k (fp16), box {64, 128}
   CUtensorMap map_v;   // scaled v (fp16), box {64, 128}
+  CUtensorMap map_dk;  // dk (fp32) [B*Hkv*S, D], box {32, 128}
+  CUtensorMap map_dv;  // dv (fp32) [B*Hkv*S, D], box {32, 128}
+  CUtensorMap map_cos; // RoPE cos table (fp32) [positions, D/2], box {32, 128}
+  CUtensorMap map_sin; // RoPE sin table, the same
   const float* lse2;   // lse * log2(e), [B*Hq*S]
   const float* delta;  // scaled delta, [B*Hq*S]
   const float* maxes;  // the abs-max pass's four maxima

@@ -129,6 +129,14 @@ GB_DEV void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
                "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// 2-D tiled reduction shared -> global: adds the fp32 tile into the global rows.
+GB_DEV void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
 // Plain (untiled) bulk copy global -> shared; addresses and size 16-byte aligned.
 GB_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
@@ -386,6 +394,12 @@ GB_DEV uint32_t pack_fp16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+GB_DEV void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr)
+               : "memory");
+}
 GB_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
