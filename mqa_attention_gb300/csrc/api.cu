@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/attn.h: argument validation,
 // per-device state (status word, workspace pool, RoPE table cache), TMA tensor
 // maps, kernel launches and optional per-kernel event timing.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <functional>
+#include <queue>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -350,6 +353,100 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                      causal, stream);
 }
 
+// Work order of the backward main kernel. A CTA owns one key tile of one (batch, KV
+// head) and walks the group's query heads over the query tiles that see it, so
+// under causal masking the first key tiles carry the most steps. The CTAs run
+// heaviest first; when that leaves a few long CTAs finishing last, the heaviest
+// key tiles are split between two CTAs (half of the group's query heads each, dK/dV
+// added). The number of tiles to split is chosen by simulating the greedy schedule
+// on the SMs (about three steps of start-up per CTA), once per shape.
+struct BwdPlan {
+  int nplan = 0;  // 0: no table (one CTA per key tile, or `uniform` each)
+  int uniform = 1;
+  int split = 0;  // key tiles [0, split) have two CTAs
+  short kt[gbattn::kMaxBwdPlan];
+  signed char parts[gbattn::kMaxBwdPlan];
+};
+
+static BwdPlan choose_bwd_plan(int nkt, int per, int G, int causal, int q_tile0, int kv_tile0,
+                               int nqt, int nsm) {
+  BwdPlan pl;
+  const long long key_tiles = static_cast<long long>(per) * nkt;
+  const bool even = G % 2 == 0;
+  // Many waves (or nothing to split): the greedy schedule is already balanced.
+  if (!even || nkt > gbattn::kMaxBwdPlan || key_tiles > 4LL * nsm) {
+    pl.uniform = (even && key_tiles < nsm) ? 2 : 1;
+    pl.split = pl.uniform == 2 ? nkt : 0;
+    return pl;
+  }
+  std::vector<int> sph(nkt);  // steps per query head of each key tile
+  for (int kt = 0; kt < nkt; ++kt) {
+    int begin = 0;
+    if (causal) {
+      const int d = ((kv_tile0 + kt) * kTile - q_tile0 * kTile) / 64;
+      begin = d < 0 ? 0 : (d > nqt ? nqt : d);
+    }
+    sph[kt] = nqt - begin;
+  }
+  const double ovh = 3.0;
+  auto makespan = [&](int split) {
+    std::vector<double> u;
+    u.reserve(static_cast<size_t>(2 * key_tiles));
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int parts = kt < split ? 2 : 1;
+      const double size = static_cast<double>(G / parts) * sph[kt] + ovh;
+      for (int i = 0; i < parts * per; ++i) u.push_back(size);
+    }
+    std::sort(u.begin(), u.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+    for (int i = 0; i < nsm; ++i) sm.push(0.0);
+    for (double x : u) {
+      const double l = sm.top();
+      sm.pop();
+      sm.push(l + x);
+    }
+    double m = 0.0;
+    while (!sm.empty()) {
+      m = std::max(m, sm.top());
+      sm.pop();
+    }
+    return m;
+  };
+  double best = makespan(0);
+  for (int split = 1; split <= nkt; ++split) {
+    const double m = makespan(split);
+    if (m < best - 1e-9) {
+      best = m;
+      pl.split = split;
+    }
+  }
+  // the table: key tiles by unit size, heaviest first (ties by key tile)
+  std::vector<int> order(nkt);
+  for (int kt = 0; kt < nkt; ++kt) order[kt] = kt;
+  auto unit = [&](int kt) { return (kt < pl.split ? G / 2 : G) * sph[kt]; };
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return unit(a) > unit(b); });
+  pl.nplan = nkt;
+  for (int e = 0; e < nkt; ++e) {
+    pl.kt[e] = static_cast<short>(order[e]);
+    pl.parts[e] = static_cast<signed char>(order[e] < pl.split ? 2 : 1);
+  }
+  return pl;
+}
+
+static const BwdPlan& bwd_plan_cached(int nkt, int per, int G, int causal, int q_tile0,
+                                      int kv_tile0, int nqt, int nsm) {
+  static std::map<std::tuple<int, int, int, int, int, int, int, int>, BwdPlan> cache;
+  const auto key = std::make_tuple(nkt, per, G, causal, q_tile0, kv_tile0, nqt, nsm);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  BwdPlan pl = choose_bwd_plan(nkt, per, G, causal, q_tile0, kv_tile0, nqt, nsm);
+  std::lock_guard<std::mutex> lk(g_mu);
+  return cache.emplace(key, pl).first->second;  // std::map references stay valid
+}
+
 // The backward pass with fp32 gradients, or (bf16_grads) with gradients rounded
 // to bf16 at the end: dq by the finalisation, dk and dv by a conversion pass over
 // fp32 copies kept in the workspace, so that every gradient is the fp32 result
@@ -392,8 +489,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   const long long krows = static_cast<long long>(B) * Hkv * Skv;
   const long long qrows_p = static_cast<long long>(B) * Hq * Sqp;
   const long long krows_p = static_cast<long long>(B) * Hkv * Skvp;
-  const long long key_tiles = static_cast<long long>(B) * Hkv * (Skvp / kTile);
-  const int hsplit = ((Hq / Hkv) % 2 == 0 && key_tiles < nsm) ? 2 : 1;
+  const BwdPlan& plan = bwd_plan_cached(Skvp / kTile, B * Hkv, Hq / Hkv, causal ? 1 : 0,
+                                        q_pos0 / kTile, kv_pos0 / kTile, Sqp / 64, nsm);
   const size_t qbytes = round256(static_cast<size_t>(qrows_p) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows_p) * D * 2);
   const size_t accbytes = round256(static_cast<size_t>(qrows_p) * D * 4);
@@ -442,9 +539,10 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     rp.seg[0] = {q, qr, dout, dos, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, v, vs, krows_p, Skv, Skvp, kv_pos0};
     rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
-    if (hsplit > 1) {  // the main kernel adds dK/dV partials of two CTAs
+    if (plan.split > 0) {  // the main kernel adds dK/dV partials of two CTAs there
       rp.dk_zero = dk;
       rp.dv_zero = dv;
+      rp.dk_zero_rows = plan.split * kTile;
     }
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
@@ -474,7 +572,12 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     bp.scale_log2 = scale * 1.4426950408889634f;
     bp.causal = causal ? 1 : 0;
     bp.inject_timeout = g_inject_timeout ? 1 : 0;
-    bp.hsplit = hsplit;
+    bp.hsplit = plan.uniform;
+    bp.nplan = plan.nplan;
+    for (int e = 0; e < plan.nplan; ++e) {
+      bp.plan_kt[e] = plan.kt[e];
+      bp.plan_parts[e] = plan.parts[e];
+    }
     bp.rope_interleaved = inter;
     LaunchTimer tm(ATTN_KERNEL_BWD_MAIN, stream);
     ok = gbattn::launch_bwd_main(bp, stream) == cudaSuccess;

@@ -14,10 +14,12 @@
 //
 // GB300 design: one CTA per (batch, KV head, 128-key tile) keeps K~ and V in
 // shared memory and walks the (query head, 64-query tile) steps that see its
-// keys (only tiles on or below the diagonal when causal). When one CTA per key
-// tile would not fill the GPU and the group has an even number of query heads,
-// two CTAs share a key tile, each taking half of the heads, and add their dK/dV
-// partials into zeroed outputs.
+// keys (only tiles on or below the diagonal when causal). The CTAs run heaviest
+// first, from a work-order table the host fills: when a few long CTAs would finish
+// last (or one CTA per key tile would leave SMs idle) and the group has an even
+// number of query heads, the heaviest key tiles get two CTAs, each taking half of
+// the heads and adding its dK/dV partials into zeroed rows. The epilogue stages
+// dK / dV in shared memory and writes (or adds) them as TMA tiles.
 //
 // Per step s (buffer b = s & 1), in TMEM:
 //   Sᵀ_b  = K~ Q~ᵀ  [128 keys x 64 queries]   (SS MMA)
@@ -122,16 +124,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   uint8_t* const sgen = smem_raw + (sbase - smem_u32(smem_raw));
 
   // ---- work item: key tile kt of KV head (b, hkv), query heads of part `part`
-  // of the group (hsplit parts); heaviest (kt = 0) first
-  const int units = p.B * p.Hkv * p.hsplit;
-  const int kt = static_cast<int>(blockIdx.x) / units;
-  const int unit = static_cast<int>(blockIdx.x) % units;
-  const int bhk = unit / p.hsplit;
-  const int part = unit % p.hsplit;
+  // of the group (nparts parts), heaviest first
+  int kt, nparts, idx;
+  if (p.nplan > 0) {
+    const int per = p.B * p.Hkv;
+    int start = 0, e = 0;
+    for (; e < p.nplan - 1; ++e) {
+      const int cnt = p.plan_parts[e] * per;
+      if (static_cast<int>(blockIdx.x) < start + cnt) break;
+      start += cnt;
+    }
+    kt = p.plan_kt[e];
+    nparts = p.plan_parts[e];
+    idx = static_cast<int>(blockIdx.x) - start;
+  } else {
+    const int units = p.B * p.Hkv * p.hsplit;
+    kt = static_cast<int>(blockIdx.x) / units;
+    nparts = p.hsplit;
+    idx = static_cast<int>(blockIdx.x) % units;
+  }
+  const int bhk = idx / nparts;
+  const int part = idx % nparts;
   const int b = bhk / p.Hkv;
   const int hkv = bhk % p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int Gc = G / p.hsplit;  // query heads of this CTA
+  const int Gc = G / nparts;  // query heads of this CTA
   const int h_first = hkv * G + part * Gc;
   const int k0 = kt * kTile;                  // first key row of the tile in the block
   const int k0p = (p.kv_tile0 + kt) * kTile;  // its position
@@ -478,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     __syncwarp();
     tc_fence_after();
     const long long grow = kv_row + r;
-    const bool sum_parts = p.hsplit > 1;  // other CTAs add into the same dk/dv rows
+    const bool sum_parts = nparts > 1;  // another CTA adds into the same dk/dv rows
     if (n == 0) {
       // no query of the block sees these keys: dk = dv = 0 (summed rows start at 0)
       if (!sum_parts) {
@@ -614,7 +631,14 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((p.Skv / kTile) * p.B * p.Hkv * p.hsplit);
+  long long ctas = 0;
+  if (p.nplan > 0) {
+    for (int e = 0; e < p.nplan; ++e) ctas += p.plan_parts[e];
+    ctas *= static_cast<long long>(p.B) * p.Hkv;
+  } else {
+    ctas = static_cast<long long>(p.Skv / kTile) * p.B * p.Hkv * p.hsplit;
+  }
+  const unsigned grid = static_cast<unsigned>(ctas);
   return launch_pdl(attn_bwd_kernel<D>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p);
 }
 

@@ -122,6 +122,7 @@ struct RowPrepParams {
   float* dqacc;
   float* dk_zero;  // backward, key rows: zeroed when the main kernel sums dK/dV partials
   float* dv_zero;
+  int dk_zero_rows;  // with dk_zero: rows [0, dk_zero_rows) of each head are zeroed
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
@@ -161,6 +162,7 @@ struct FwdParams {
 };
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 
+constexpr int kMaxBwdPlan = 64;  // key tiles a work-order table can hold
 struct BwdParams {
   CUtensorMap map_q;   // scaled rotated q (fp16), box {64, BQ}
   CUtensorMap map_do;  // scaled dout (fp16), box {64, BQ}
@@ -187,6 +189,13 @@ struct BwdParams {
   int inject_timeout;
   int hsplit;  // CTAs sharing one (KV head, key tile): 1, or 2 (dK/dV summed with reductions)
   int rope_interleaved;  // rotation pairs of the dk epilogue (see RowPrepParams)
+  // Work order, heaviest unit first. nplan > 0: entry e is key tile plan_kt[e] with
+  // plan_parts[e] CTAs per (batch, KV head) — 1, or 2 each taking half of the group's
+  // query heads and adding its dK/dV partials — and hsplit is unused. nplan = 0: key
+  // tile blockIdx / (B*Hkv*hsplit), hsplit CTAs each.
+  int nplan;
+  short plan_kt[kMaxBwdPlan];
+  signed char plan_parts[kMaxBwdPlan];
 };
 // Query-tile rows used by the backward main kernel for head dimension D.
 inline int bwd_query_tile(int) { return 64; }

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
     for (int k = 0; k < 8; ++k) dot += a1[k] * o1[k] + a2[k] * o2[k];
 #pragma unroll
     for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (!is_q && live && p.dk_zero != nullptr) {
+    if (!is_q && live && p.dk_zero != nullptr && i < p.dk_zero_rows) {
       store8(p.dk_zero + f1, z);
       store8(p.dk_zero + f2, z);
       store8(p.dv_zero + f1, z);

@@ -172,8 +172,11 @@ def test_bf16_gradients(B, Hq, Hkv, S, D, causal, rope):
     assert all(t.dtype == torch.bfloat16 for t in g16)
     for name, a, b in (("dk", g16[1], g32[1]), ("dv", g16[2], g32[2])):
         assert torch.equal(a, b.to(torch.bfloat16)), name
+    # one bf16 ulp, plus the two runs' fp32 rounding of dq's sums (relative to the
+    # largest |dq|: an element whose terms cancel can differ by more than its own ulp)
     a, b = g16[0].double(), g32[0].to(torch.bfloat16).double()
-    assert ((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + 1e-12).all(), "dq"
+    slack = 2.0 ** -20 * b.abs().max().item()
+    assert ((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + slack).all(), "dq"
     want = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta, wl.causal,
                                 rope=rope, round_rotated=True)
     gmax, gmean = grad_bounds(wl)
@@ -326,8 +329,9 @@ def test_power_of_two_input_scales_are_exact(D, hkv):
     from the inputs' abs-maxima. Scaling q by 2^4, k by 2^-4 (scores unchanged),
     v by 2^6 and dO by 2^-10 must then scale every result by an exact power of
     two: out 2^6, lse 1, dv 2^-10, dk 2^(-4+4), dq 2^(-4-4). out, lse, dk and dv
-    are compared bit for bit (they are summed in a fixed order); dq, whose
-    partial sums land in a run-dependent order, to fp32 rounding."""
+    are compared bit for bit (each is summed in a fixed order: the two CTAs that may
+    share a key tile add into zero, which commutes); dq, whose partial sums land in a
+    run-dependent order, to fp32 rounding of those sums."""
     B, Hq, S, theta = 1, 8, 512, 500000.0 if D == 128 else 10000.0
     wl = Workload(300 + D, "scaled", B, Hq, hkv, S, D, theta, True)
     dev, _ = gen(wl)
@@ -339,5 +343,7 @@ def test_power_of_two_input_scales_are_exact(D, hkv):
     assert torch.equal(got["lse"], base["lse"])
     assert torch.equal(got["dv"], base["dv"] * 2.0 ** -10)
     assert torch.equal(got["dk"], base["dk"])
+    # dq sums its key tiles' partial products in a run-dependent order: the two runs
+    # differ by fp32 rounding of those sums, bounded here against the largest |dq|
     want = base["dq"] * 2.0 ** -8
-    assert ((got["dq"] - want).abs() <= want.abs() * 2.0 ** -20 + 1e-12).all()
+    assert (got["dq"] - want).abs().max().item() <= 2.0 ** -16 * want.abs().max().item()
