@@ -709,6 +709,25 @@ def run_decode(args, rank, world, local):
     status = M.sync_status()
     ms = max_over_ranks(e0.elapsed_time(e1) / (reps * ncopy), world)
     sampler.stop()
+    # End to end: each call takes its new query rows from pinned host memory and
+    # returns out and lse to it (the cache stays resident, as in serving).
+    hq = q.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    n_e2e = 200
+    for i in range(n_e2e + 10):
+        if i == 10:
+            torch.cuda.synchronize()
+            e0.record(stream)
+        kc, vc = caches[i % ncopy]
+        q.copy_(hq, non_blocking=True)
+        M.attn_decode(q, kc, vc, out, lse, wl.B, wl.Hq, wl.Hkv, sq, wl.S, wl.D, qpos, wl.theta,
+                      mode, wl.scale, stream)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
     if rank != 0:
         return
     _, peak_hbm, peak_src = peaks()
@@ -723,13 +742,19 @@ def run_decode(args, rank, world, local):
         "config": dict(config_of(wl, world, l2=f"each call reads its own cache copy ({ncopy} "
                                                    "copies, >= 256 MiB)", rope=args.rope),
                        passes="decode fwd", new_tokens=sq, bytes_per_step=moved),
-        "e2e": None,
-        "note": "decode entry point, calls replayed from a CUDA graph; device time only",
+        "e2e": {"value": moved * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
+                "copies": "pinned host q in, out and lse out, every call; calls issued "
+                          "one after another on the stream (no graph)"},
+        "note": "value: decode entry point replayed from a CUDA graph, device time",
         "steps": reps * ncopy,
         "gpu_launches": 2 * reps * ncopy,  # chunk kernel and merge per call
         "roofline": {"bound": "hbm", "kernel": "attn_decode", "achieved": gbs / world,
                      "peak": peak_hbm, "unit": "GB/s", "frac": gbs / world / peak_hbm,
-                     "traffic": None, "peak_source": f"{peak_src} HBM copy"},
+                     # the committed ncu record is for one new token per sequence
+                     "traffic": ncu_traffic("attn_decode", wl.name) if sq == 1 else None,
+                     "peak_source": f"{peak_src} HBM copy"},
         "cpu_baseline": None,
         "clocks": sampler.summary(t0, t1),
         "device_status": status,
