@@ -166,12 +166,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     return (b * p.Hq + h) * p.Sq + step_qt(s) * BQ;
   };
 
-  // ---- setup
+  // ---- setup. The producer's lane initialises the barriers and, as soon as the
+  // previous kernel's writes are visible, starts the K~/V and first Q~/dO loads while
+  // the MMA warp allocates tensor memory.
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  const bool producer = warp == kWarpLoad && lane == 0;
+  auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
+  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s % C::kDsBufs) * C::kDsBytes; };
+  int issued = 0;  // Q~/dO stage loads issued (producer lane)
+  // stage load of step s, once the stage is free
+  auto issue_stage = [&](int s) {
+    const int st = s % C::kStages;
+    if (!bounded_wait(smem_u32(&bar_stage_empty[st]), ((s / C::kStages) & 1) ^ 1, &abort_flag,
+                      p.status, kSiteStageEmpty))
+      return false;
+    const uint32_t full = smem_u32(&bar_stage_full[st]);
+    const uint32_t dst = stage_addr(s);
+    const int row = step_row(s);
+    mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
+    for (int r = 0; r < C::kRegions; ++r) {
+      tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
+      tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
+    }
+    bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
+    bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
+    return true;
+  };
+  if (producer) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_kv), 1);
     mbar_init(smem_u32(&bar_done), 1);
@@ -189,52 +213,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(smem_u32(&bar_dq_free[i]), 128);
     }
     fence_mbar_init();
+    pdl_wait();  // the operands come from the pre-pass before this kernel
+    tma_prefetch_desc(&p.map_q);
+    tma_prefetch_desc(&p.map_do);
+    const uint32_t kvb = smem_u32(&bar_kv);
+    mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
+    for (int r = 0; r < C::kRegions; ++r) {
+      tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
+      tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
+    }
+    while (issued < n && issued < C::kStages && issue_stage(issued)) ++issued;  // free stages
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
-  // Nothing above touched global memory: this prologue may overlap the kernel before
-  // it in the stream.
+  // Nothing above except the producer's loads (after its own wait) touched global
+  // memory: this prologue may overlap the kernel before it in the stream.
   pdl_wait();
   pdl_launch_dependents();
   const BwdExponents ex = bwd_exponents(p.maxes);  // fp16 operand scales
-  auto stage_addr = [&](int s) { return sbase + C::kStageOff + (s % C::kStages) * C::kStageBytes; };
-  auto ds_addr = [&](int s) { return sbase + C::kDsOff + (s % C::kDsBufs) * C::kDsBytes; };
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.map_q);
-      tma_prefetch_desc(&p.map_do);
-      const uint32_t kvb = smem_u32(&bar_kv);
-      mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
-      for (int r = 0; r < C::kRegions; ++r) {
-        tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
-        tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
-      }
-      int issued = 0;
-      for (int s = 0; s < n; ++s) {
-        const int st = s % C::kStages;
-        if (!bounded_wait(smem_u32(&bar_stage_empty[st]), ((s / C::kStages) & 1) ^ 1, abort_ptr,
-                          p.status, kSiteStageEmpty))
-          break;
-        const uint32_t full = smem_u32(&bar_stage_full[st]);
-        const uint32_t dst = stage_addr(s);
-        const int row = step_row(s);
-        mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
-        for (int r = 0; r < C::kRegions; ++r) {
-          tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
-          tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
-        }
-        bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
-        bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
-        ++issued;
-      }
+      while (issued < n && issue_stage(issued)) ++issued;
       // Copies already issued land before the CTA releases its shared memory
       // (at most one in flight per stage: a stage is refilled only once consumed).
-      drain_wait(kvb, 0);
+      drain_wait(smem_u32(&bar_kv), 0);
       for (int i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i)
         drain_wait(smem_u32(&bar_stage_full[i % C::kStages]), (i / C::kStages) & 1);
     }

@@ -102,12 +102,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int q_row0 = bh * p.Sq;
   const int kv_row0 = (b * p.Hkv + hkv) * p.Skv;
 
-  // ---- setup
+  // ---- setup. The producer's lane initialises the barriers and, as soon as the
+  // previous kernel's writes are visible, starts the Q loads and fills the K/V ring
+  // while the MMA warp allocates tensor memory.
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  const bool producer = warp == kWarpLoad && lane == 0;
+  int issued = 0;  // K/V ring loads issued (producer lane)
+  // ring load i: K_(i/2) or V_(i/2) into slot i % kSlots, once that slot is free
+  auto issue_kv = [&](int i) {
+    const int slot = i % C::kSlots;
+    const uint32_t ph = ((i / C::kSlots) & 1) ^ 1;
+    if (!bounded_wait(smem_u32(&bar_kv_empty[slot]), ph, &abort_flag, p.status, kSiteKvEmpty))
+      return false;
+    const uint32_t full = smem_u32(&bar_kv_full[slot]);
+    mbar_arrive_expect_tx(full, C::kTileBytes);
+    const CUtensorMap* map = (i & 1) == 0 ? &p.map_k : &p.map_v;
+    const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
+    for (int r = 0; r < C::kRegions; ++r)
+      tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (i >> 1) * kTile, full);
+    return true;
+  };
+  if (producer) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
     mbar_init(smem_u32(&bar_drain), 1);
@@ -122,50 +140,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(smem_u32(&bar_o_done[t]), 1);
     }
     fence_mbar_init();
+    pdl_wait();  // q~, k~ come from the pre-pass before this kernel
+    tma_prefetch_desc(&p.map_q);
+    tma_prefetch_desc(&p.map_k);
+    tma_prefetch_desc(&p.map_v);
+    const int nvalid = (n_0 > 0) + (n_1 > 0);
+    mbar_arrive_expect_tx(smem_u32(&bar_q), nvalid * C::kTileBytes);
+    for (int t = 0; t < 2; ++t) {
+      if ((t ? n_1 : n_0) == 0) continue;
+      for (int r = 0; r < C::kRegions; ++r)
+        tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
+                    q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
+    }
+    while (issued < 2 * n && issued < C::kSlots && issue_kv(issued)) ++issued;  // free slots
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_ptr = &abort_flag;
-  // Nothing above touched global memory: this prologue may overlap the kernel before
-  // it in the stream.
+  // Nothing above except the producer's loads (after its own wait) touched global
+  // memory: this prologue may overlap the kernel before it in the stream.
   pdl_wait();
   pdl_launch_dependents();
 
   if (warp == kWarpLoad) {
     // ================================================================ producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.map_q);
-      tma_prefetch_desc(&p.map_k);
-      tma_prefetch_desc(&p.map_v);
-      const int nvalid = (n_0 > 0) + (n_1 > 0);
-      mbar_arrive_expect_tx(smem_u32(&bar_q), nvalid * C::kTileBytes);
-      for (int t = 0; t < 2; ++t) {
-        if ((t ? n_1 : n_0) == 0) continue;
-        for (int r = 0; r < C::kRegions; ++r)
-          tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
-                      q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
-      }
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        for (int w = 0; w < 2; ++w) {
-          const int slot = issued % C::kSlots;
-          const uint32_t ph = ((issued / C::kSlots) & 1) ^ 1;
-          if (!bounded_wait(smem_u32(&bar_kv_empty[slot]), ph, abort_ptr, p.status, kSiteKvEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&bar_kv_full[slot]);
-          mbar_arrive_expect_tx(full, C::kTileBytes);
-          const CUtensorMap* map = w == 0 ? &p.map_k : &p.map_v;
-          const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + j * kTile, full);
-          ++issued;
-        }
-      }
+      while (issued < 2 * n && issue_kv(issued)) ++issued;
       // Loads already issued land before the CTA releases its shared memory (a
       // no-op in a healthy run). Each slot has at most one load in flight: a load
       // is issued only after the previous one in its slot was consumed.
