@@ -279,6 +279,20 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def bwd_prologue_bytes(wl):
+    """Algorithmic HBM bytes of the backward prologue (abs-max pass + row pass) for an
+    unpadded self-attention shape: the abs-max pass reads q, k, v, dO; the row pass
+    reads q, dO, out, k, v, lse and writes fp16 q~, dO, k~, v, the zeroed fp32 dQ
+    accumulator (twice a bf16 tensor), delta and lse * log2 e."""
+    qb = wl.B * wl.Hq * wl.S * wl.D * 2       # one bf16 / fp16 [B,Hq,S,D] tensor
+    kb = wl.B * wl.Hkv * wl.S * wl.D * 2      # one bf16 / fp16 [B,Hkv,S,D] tensor
+    rb = wl.B * wl.Hq * wl.S * 4              # one fp32 [B,Hq,S] row vector
+    absmax = 2 * qb + 2 * kb
+    reads = 3 * qb + 2 * kb + rb
+    writes = 2 * qb + 2 * kb + 2 * qb + 2 * rb
+    return absmax + reads + writes
+
+
 def config_of(wl, n, l2, rope="half", grads="fp32"):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
             "rope_theta": wl.theta, "rope": rope, "grads": grads, "causal": wl.causal,
@@ -464,10 +478,7 @@ def run_ours(args, rank, world, local):
     # against the measured copy bandwidth
     prologue = None
     if "bwd_prep" in kern:
-        qb = wl.B * wl.Hq * wl.S * wl.D * 2       # one bf16 / fp16 [B,Hq,S,D] tensor
-        kb = wl.B * wl.Hkv * wl.S * wl.D * 2      # one bf16 / fp16 [B,Hkv,S,D] tensor
-        rb = wl.B * wl.Hq * wl.S * 4              # one fp32 [B,Hq,S] row vector
-        nbytes = (2 * qb + 2 * kb) + (3 * qb + 2 * kb + rb) + (2 * qb + 2 * kb + 2 * qb + 2 * rb)
+        nbytes = bwd_prologue_bytes(wl)
         gbs = nbytes / (kern["bwd_prep"]["avg_ms"] * 1e-3) / 1e9
         prologue = {"kernel": "bwd_prep (abs-max pass + row pass)", "bound": "hbm",
                     "bytes": nbytes, "achieved": gbs, "peak": peak_hbm, "unit": "GB/s",

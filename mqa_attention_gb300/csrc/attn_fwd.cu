@@ -343,20 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float inv_l = 1.f / l;
       const uint32_t obuf = sbase + t * C::kTileBytes;  // Q_t is no longer read
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tO + cc * 32, u);
-        const uint32_t region = obuf + ((cc * 32) / 64) * C::kRegionBytes;
-        const uint32_t chunk0 = ((cc * 32) % 64) / 8;
+      for (int c2 = 0; c2 < D / 64; ++c2) {  // 64 columns (one swizzle region) per wait
+        uint32_t u[2][32];
+        tmem_ld32x2(tO + c2 * 64, tO + c2 * 64 + 32, u[0], u[1]);
+        const uint32_t region = obuf + c2 * C::kRegionBytes;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t w[4];
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__uint_as_float(u[8 * q4 + 2 * e]) * inv_l,
-                             __uint_as_float(u[8 * q4 + 2 * e + 1]) * inv_l);
-          st_shared_v4(region + sw128_offset(r, chunk0 + q4), w[0], w[1], w[2], w[3]);
-        }
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(u[h][8 * q4 + 2 * e]) * inv_l,
+                               __uint_as_float(u[h][8 * q4 + 2 * e + 1]) * inv_l);
+            st_shared_v4(region + sw128_offset(r, 4 * h + q4), w[0], w[1], w[2], w[3]);
+          }
       }
       fence_async_smem();
       named_bar_sync(1 + t, 128);
