@@ -213,6 +213,15 @@ int attn_profile_query(int kernel, int* launches, float* total_ms);
  * call are undefined. Not for production use. */
 int attn_debug_inject_timeout(int enable);
 
+/* The backward main kernel's work plan for these sizes on a GPU with `nsm` SMs, as
+ * attn_bwd / attn_bwd_partial would choose it (host computation only; touches no
+ * device): *split_key_tiles = how many of the heaviest key tiles get two CTAs (each
+ * half of the group's query heads, dK/dV added), *ctas = CTAs launched. Sizes as in
+ * attn_bwd_partial (self-attention: Sq = Skv, positions 0). Returns ATTN_OK, or
+ * ATTN_ERR_INVALID for invalid sizes or null outputs. */
+int attn_debug_bwd_plan(int B, int Hq, int Hkv, int Sq, int Skv, int q_pos0, int kv_pos0,
+                        int causal, int nsm, int* split_key_tiles, int* ctas);
+
 /* Library version string. */
 const char* attn_version(void);
 

@@ -41,6 +41,7 @@ __all__ = [
     "profile_end",
     "profile_query",
     "debug_inject_timeout",
+    "debug_bwd_plan",
     "version",
     "EXPORTED_SYMBOLS",
     "KERNEL_ROPE",
@@ -73,6 +74,7 @@ EXPORTED_SYMBOLS = (
     "attn_profile_end",
     "attn_profile_query",
     "attn_debug_inject_timeout",
+    "attn_debug_bwd_plan",
     "attn_version",
     "attn_fwd_noalloc",
 )
@@ -120,6 +122,9 @@ def lib() -> ctypes.CDLL:
             L.attn_profile_query.restype = _I
             L.attn_debug_inject_timeout.argtypes = [_I]
             L.attn_debug_inject_timeout.restype = _I
+            L.attn_debug_bwd_plan.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                              ctypes.POINTER(_I), ctypes.POINTER(_I)]
+            L.attn_debug_bwd_plan.restype = _I
             L.attn_version.argtypes = []
             L.attn_version.restype = ctypes.c_char_p
             L.attn_fwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P]
@@ -416,6 +421,16 @@ def profile_query(kernel: int):
 
 def debug_inject_timeout(enable: bool):
     _check(lib().attn_debug_inject_timeout(1 if enable else 0), "attn_debug_inject_timeout")
+
+
+def debug_bwd_plan(B, Hq, Hkv, Sq, Skv, nsm, q_pos0=0, kv_pos0=0, causal=True):
+    """The backward main kernel's work plan on a GPU with `nsm` SMs (host only):
+    (number of heaviest key tiles split between two CTAs, CTAs launched)."""
+    split, ctas = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().attn_debug_bwd_plan(B, Hq, Hkv, Sq, Skv, q_pos0, kv_pos0, 1 if causal else 0,
+                                     nsm, ctypes.byref(split), ctypes.byref(ctas)),
+           "attn_debug_bwd_plan")
+    return split.value, ctas.value
 
 
 def version() -> str:

@@ -805,4 +805,24 @@ int attn_debug_inject_timeout(int enable) {
   return ATTN_OK;
 }
 
+int attn_debug_bwd_plan(int B, int Hq, int Hkv, int Sq, int Skv, int q_pos0, int kv_pos0,
+                        int causal, int nsm, int* split_key_tiles, int* ctas) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Sq <= 0 || Skv <= 0 || nsm <= 0 ||
+      q_pos0 < 0 || kv_pos0 < 0 || q_pos0 % kTile != 0 || kv_pos0 % kTile != 0 ||
+      !split_key_tiles || !ctas)
+    return ATTN_ERR_INVALID;
+  const int nkt = round_tile(Skv) / kTile;
+  const BwdPlan& pl = bwd_plan_cached(nkt, B * Hkv, Hq / Hkv, causal ? 1 : 0, q_pos0 / kTile,
+                                      kv_pos0 / kTile, round_tile(Sq) / 64, nsm);
+  *split_key_tiles = pl.split;
+  long long n = 0;
+  if (pl.nplan > 0) {
+    for (int e = 0; e < pl.nplan; ++e) n += pl.parts[e];
+  } else {
+    n = static_cast<long long>(nkt) * pl.uniform;
+  }
+  *ctas = static_cast<int>(n * B * Hkv);
+  return ATTN_OK;
+}
+
 }  // extern "C"

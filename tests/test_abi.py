@@ -127,3 +127,29 @@ def test_decode_rejects_groups_beyond_one_tile(built_lib):
     assert lib.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 1, 1, 256, 64, -1, 10000.0, 0,
                            0.125, None) == M.ATTN_ERR_INVALID
     assert lib.attn_rope(FAKE, FAKE, 4, 100, 0, 96, 10000.0, 0, None) == M.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape,want", [
+    # (B, Hq, Hkv, Sq, Skv, SMs) -> (key tiles split in two, CTAs)
+    ((1, 32, 8, 4096, 4096, 152), (6, 304)),       # Llama-3-8B: the 6 heaviest key tiles
+    ((8, 8, 1, 2048, 2048, 152), (12, 224)),       # PaLM-MQA: 128 key tiles < 152 SMs
+    ((4, 32, 32, 1024, 1024, 152), (0, 1024)),     # SmolLM (MHA): one head per group, no split
+    ((1, 32, 8, 32768, 32768, 152), (0, 2048)),    # 13 waves: balanced as it is
+    ((1, 8, 1, 16384, 16384, 152), (128, 256)),    # beyond the table: every tile split
+])
+def test_backward_work_plan(shape, want):
+    """The host's choice of which heavy key tiles to split (a simulated greedy
+    schedule of the CTAs on the SMs; no GPU needed)."""
+    assert M.debug_bwd_plan(*shape) == want
+
+
+def test_backward_work_plan_counts_ctas():
+    for B, Hq, Hkv, S in [(1, 32, 8, 4096), (2, 16, 4, 2048), (8, 8, 1, 2048), (1, 4, 1, 300)]:
+        nkt = -(-S // 128)
+        split, ctas = M.debug_bwd_plan(B, Hq, Hkv, S, S, 152)
+        assert 0 <= split <= nkt
+        if (Hq // Hkv) % 2:
+            assert split == 0
+        assert ctas == B * Hkv * (nkt + split)
+    with pytest.raises(M.AttnError):
+        M.debug_bwd_plan(1, 6, 4, 128, 128, 152)  # Hq not a multiple of Hkv
