@@ -472,9 +472,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
                                                                         : kv_pos0 + round_tile(Skv);
   if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
 
-  // Two CTAs per (KV head, key tile), each with half of the group's query heads,
-  // when one CTA per key tile would not fill the GPU (and the group splits
-  // evenly); otherwise one CTA per key tile, with no dK/dV zeroing.
+  // The main kernel's work order (bwd_plan_cached) depends on the number of SMs.
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
