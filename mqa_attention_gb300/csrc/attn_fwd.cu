@@ -52,6 +52,34 @@ struct FwdCfg {
   __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? D : 0); }
 };
 
+// Packed fp32 pairs (fma.rn.f32x2 / add.rn.f32x2: one instruction for two lanes'
+// worth of the same operation, each rounded as the scalar form) and the
+// three-input maximum.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Waits for a phase without looking at the abort flag (used to drain copies
 // and MMAs that were already issued before the CTA releases its resources).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -285,16 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = i >= lim ? -INFINITY : s[i];
       }
-      // Row maximum as 8 independent partial chains (latency, not issue, bound).
-      float mp[8];
+      // Row maximum as 4 independent chains of three-input maxima (the softmax warps'
+      // instruction issue, not the tensor core, is what a step waits for).
+      float mp[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+      for (int k = 0; k < 4; ++k) mp[k] = fmaxf(s[k], s[k + 4]);
 #pragma unroll
       for (int i = 8; i < 128; i += 8)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[i + k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int k = 0; k < 4; ++k) mp[k] = fmax3(mp[k], s[i + k], s[i + 4 + k]);
+      const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), mp[3], mp[3]);
       const float mx2 = mx * sl2;
       float alpha = 1.f;
       bool grew = false;
@@ -305,20 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         grew = true;
         m = mx2;
       }
-      float rp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+      // exponent arguments and partial row sums two columns at a time (packed f32x2)
+      float2 rp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m, -m);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a0 = ex2(fmaf(s[hh * 64 + 2 * i], sl2, -m));
-          const float a1 = ex2(fmaf(s[hh * 64 + 2 * i + 1], sl2, -m));
-          rp[i & 7] += a0 + a1;
-          pk[i] = pack_bf16(a0, a1);
+          const float2 x =
+              ffma2(make_float2(s[hh * 64 + 2 * i], s[hh * 64 + 2 * i + 1]), sl2x2, negm);
+          const float2 a = make_float2(ex2(x.x), ex2(x.y));
+          rp[i & 3] = fadd2(rp[i & 3], a);
+          pk[i] = pack_bf16(a.x, a.y);
         }
         tmem_st32(tS + hh * 32, pk);
       }
-      const float rs = ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+      const float2 r2 = fadd2(fadd2(rp[0], rp[1]), fadd2(rp[2], rp[3]));
+      const float rs = r2.x + r2.y;
       l = l * alpha + rs;
       if (j > 0 && __any_sync(0xffffffffu, grew)) {
         const float f = grew ? alpha : 1.f;
