@@ -98,6 +98,34 @@ struct BwdCfg {
   static_assert(kEpiDk + (D / 32) * kBoxBytes <= kDsOff + kDsBufs * kDsBytes, "epilogue staging");
 };
 
+// Packed fp32 pairs: one instruction for two lanes' worth of the same operation,
+// each rounded as the scalar form.
+__device__ __forceinline__ uint64_t pack2(float2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
+  return unpack2(d);
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -470,11 +498,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
         float pr[4], dsv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float pv = ex2(fmaf(__uint_as_float(sv[4 * g + e]), sl2, -lv[e]));
-          pv = (4 * g + e < lim) ? 0.f : pv;
-          pr[e] = pv;
-          dsv[e] = pv * (__uint_as_float(dpv[4 * g + e]) - dl[e]);
+        for (int e = 0; e < 4; e += 2) {  // two query columns per packed f32x2 operation
+          const float2 x = ffma2(make_float2(__uint_as_float(sv[4 * g + e]),
+                                             __uint_as_float(sv[4 * g + e + 1])),
+                                 make_float2(sl2, sl2), make_float2(-lv[e], -lv[e + 1]));
+          float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          pv.x = (4 * g + e < lim) ? 0.f : pv.x;
+          pv.y = (4 * g + e + 1 < lim) ? 0.f : pv.y;
+          const float2 dp = fsub2(make_float2(__uint_as_float(dpv[4 * g + e]),
+                                              __uint_as_float(dpv[4 * g + e + 1])),
+                                  make_float2(dl[e], dl[e + 1]));
+          const float2 ds = fmul2(pv, dp);
+          pr[e] = pv.x;
+          pr[e + 1] = pv.y;
+          dsv[e] = ds.x;
+          dsv[e + 1] = ds.y;
         }
         pk[2 * g] = pack_fp16(pr[0], pr[1]);
         pk[2 * g + 1] = pack_fp16(pr[2], pr[3]);
