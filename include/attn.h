@@ -29,7 +29,8 @@
  *   Heads    query head h reads K/V head h / (Hq / Hkv) (contiguous groups).
  *   RoPE     half-split: for i < D/2, angle = p * theta^(-2i/D) at position p = 0..S-1;
  *            y_i = x_i cos - x_{i+D/2} sin, y_{i+D/2} = x_{i+D/2} cos + x_i sin.
- *            The rotated q and k are rounded to bf16 before the score product.
+ *            The rotated q and k are rounded to bf16 before the score product: to the
+ *            bf16 value nearest the exact rotation (cos/sin evaluated in fp64).
  *   Sizes    D in {64, 128}; S > 0 (the kernels work in 128-row tiles: for an S that is
  *            not a multiple of 128 they run on copies padded to whole tiles, with the
  *            padding rows contributing nothing, and copy the valid rows out, at the
@@ -38,8 +39,20 @@
  *   Pointers device pointers, 16-byte aligned, not aliasing one another. The caller owns
  *            every buffer; the library never frees or keeps them.
  *   Stream   all work is enqueued on `stream` (a cudaStream_t, or 0); no call
- *            synchronises with the host except where stated. Temporary workspace is
- *            taken from a library-owned stream-ordered pool on the current device.
+ *            synchronises with the host except attn_sync_status and
+ *            attn_profile_query. Temporary workspace is taken from a library-owned
+ *            stream-ordered pool on the current device and released in stream order.
+ *   RoPE     the cos/sin table of a (D, rope_theta) is built on the device the first
+ *   table    time a call needs it (and rebuilt, at least twice as long, when a later
+ *            call needs more positions), in stream order on that call's stream: memory
+ *            from the pool, no host synchronisation; a call on another stream waits
+ *            for the build on the device. At most 8 (D, rope_theta) tables are kept per
+ *            device (least recently used dropped first); a dropped table is freed in
+ *            stream order after every use recorded for it, except a table read under
+ *            stream capture, which stays allocated (a graph may still read it). A call
+ *            that needs a table built while `stream` is capturing returns
+ *            ATTN_ERR_UNSUPPORTED: make the first call for a (D, rope_theta, length)
+ *            outside capture.
  *   Device   the current CUDA device must be an sm_103 GPU (GB300).
  *   Errors   every entry point returns ATTN_OK (0) or one of the codes below and writes
  *            nothing when it rejects its arguments. Device-side failures of a launched
@@ -89,7 +102,13 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
  *   dq_i = scale R_iᵀ sum_j dS_ij k~_j,  dk_j = scale R_jᵀ sum_{h,i} dS_ij q~_i,
  *   dv_j = sum_{h,i} P_ij dout_i.
  * lse is treated as an input that is not differentiated. The gradient formulas are the
- * chain rule through the forward definition above (no page writes them out). */
+ * chain rule through the forward definition above (no page writes them out).
+ * delta_i: in exact arithmetic dout_i.out_i = sum_j P_ij dP_ij. The `out` received is
+ * rounded to bf16, and that rounding enters every dS_ij of the row and, summed over a
+ * group's query heads, dk. attn_bwd takes delta from `out` (one read of it) when
+ * Hq/Hkv <= 8, and otherwise runs an extra tensor-core pass over the scores that forms
+ * sum_j P_ij dP_ij itself (about the cost of a forward pass); attn_bwd_ex can choose
+ * either (ATTN_DELTA_* below). */
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
              const void* dout, float* dq, float* dk, float* dv, int B, int Hq, int Hkv, int S,
              int D, float rope_theta, float scale, int causal, attn_stream_t stream);
@@ -104,9 +123,20 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
  *                         (llama3-from-scratch §RoPE). */
 enum { ATTN_ROPE_HALF = 0, ATTN_ROPE_INTERLEAVED = 1 };
 
+/* Delta flags, OR-ed into the rope_mode argument of attn_bwd_ex and attn_bwd_bf16 (not
+ * attn_bwd_partial, whose out is the merged result of every K/V block):
+ *   ATTN_DELTA_EXACT     always form delta_i = sum_j P_ij dP_ij with the extra pass:
+ *                        gradients free of the rounding of `out` (which dominates their
+ *                        error when the softmax rows are sharply peaked or many query
+ *                        heads share a K/V head); `out` is then not read;
+ *   ATTN_DELTA_FROM_OUT  always take delta_i = dout_i.out_i from the bf16 `out`.
+ * Neither: the default of attn_bwd (exact when Hq/Hkv > 8). Both: ATTN_ERR_INVALID. */
+enum { ATTN_DELTA_EXACT = 0x100, ATTN_DELTA_FROM_OUT = 0x200 };
+
 /* attn_fwd / attn_bwd with the RoPE pair layout chosen by rope_mode (one of the
- * ATTN_ROPE_* values; anything else returns ATTN_ERR_INVALID). Arguments, layouts,
- * ownership and errors are otherwise those of attn_fwd / attn_bwd; attn_fwd(...) is
+ * ATTN_ROPE_* values, for attn_bwd_ex optionally OR-ed with one ATTN_DELTA_* flag;
+ * anything else returns ATTN_ERR_INVALID). Arguments, layouts, ownership and errors are
+ * otherwise those of attn_fwd / attn_bwd; attn_fwd(...) is
  * attn_fwd_ex(..., rope_theta, ATTN_ROPE_HALF, scale, ...). */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                 int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,
@@ -193,14 +223,15 @@ const char* attn_status_string(int status);
  * attn_profile_end disables it. attn_profile_query synchronises the recorded events and
  * returns the number of recorded launches of `kernel` and their summed duration in ms.
  * Kernel kinds: 0 rope (forward RoPE pre-pass), 1 forward attention, 2 backward
- * pre-pass, 3 backward dK/dV/dQ main kernel, 4 dQ finalisation. */
+ * pre-pass, 3 backward dK/dV/dQ main kernel, 4 dQ finalisation, 5 the exact delta pass. */
 enum {
   ATTN_KERNEL_ROPE = 0,
   ATTN_KERNEL_FWD = 1,
   ATTN_KERNEL_BWD_PREP = 2,
   ATTN_KERNEL_BWD_MAIN = 3,
   ATTN_KERNEL_DQ_FINAL = 4,
-  ATTN_NUM_KERNELS = 5
+  ATTN_KERNEL_DELTA = 5,
+  ATTN_NUM_KERNELS = 6
 };
 int attn_profile_begin(int max_launches);
 int attn_profile_end(void);
@@ -233,15 +264,18 @@ const char* attn_version(void);
  * attn_fwd's pooled workspace and cached RoPE tables it uses one fixed array of
  * ATTN_FWD_NOALLOC_SCRATCH_BYTES in device memory that the CUDA runtime reserves on
  * every GPU where the library's code is loaded and keeps until the process exits.
- * Limit: 256 + 2*round256(4*S*D/2) + round256(2*B*Hq*S*D) + round256(2*B*Hkv*S*D)
- * bytes must fit in that array (e.g. B=1, Hq=32, Hkv=8, S=4096, D=128 needs 44 MB);
- * larger problems return ATTN_ERR_UNSUPPORTED.
+ * Limit: 16*ceil64(S*D/2) + round256(2*B*Hq*S*D) + round256(2*B*Hkv*S*D) bytes
+ * (ceil64: rounded up to a multiple of 64) must fit in that array (e.g. B=1, Hq=32,
+ * Hkv=8, S=4096, D=128 needs 46 MB); larger problems return ATTN_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address (with that
  * device current); make that first call before any stream capture.
  * All calls on a device share the array and leave their contents in it: calls whose
  * GPU work overlaps (other streams, other host threads) race and give undefined
- * results. A kernel wait that expires here leaves out/lse undefined and is not
- * reported by attn_sync_status. No cudaMalloc, cudaFree or allocating routine. */
+ * results. A kernel wait that expires here leaves out/lse undefined and is reported
+ * by attn_sync_status like any other (the status word is a static device variable, so
+ * finding it allocates nothing). The device address of that array and of the status
+ * word may not outlive the CUDA context they were looked up in: do not keep using the
+ * library across cudaDeviceReset. No cudaMalloc, cudaFree or allocating routine. */
 #define ATTN_FWD_NOALLOC_SCRATCH_BYTES (64u << 20)
 int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                      int Hq, int Hkv, int S, int D, float rope_theta, float scale, int causal,

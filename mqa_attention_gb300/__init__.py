@@ -49,13 +49,17 @@ __all__ = [
     "KERNEL_BWD_PREP",
     "KERNEL_BWD_MAIN",
     "KERNEL_DQ_FINAL",
+    "KERNEL_DELTA",
+    "DELTA_MODES",
 ]
 
 LIB_NAME = "libmqa_attention_gb300.so"
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
-KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL = range(5)
+KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL, KERNEL_DELTA = range(6)
+# delta flags OR-ed into the rope_mode of attn_bwd_ex / attn_bwd_bf16 (ATTN_DELTA_*)
+DELTA_MODES = {"auto": 0, "exact": 0x100, "from_out": 0x200}
 
 EXPORTED_SYMBOLS = (
     "attn_fwd",
@@ -367,9 +371,11 @@ def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None, rope="hal
 
 
 def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None,
-             rope="half", grad_dtype=None):
-    """Allocates dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved",
-    attn_bwd_bf16 for grad_dtype=torch.bfloat16; fp32 gradients otherwise)."""
+             rope="half", grad_dtype=None, delta="auto"):
+    """Allocates dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved" or a
+    delta mode other than "auto", attn_bwd_bf16 for grad_dtype=torch.bfloat16; fp32
+    gradients otherwise). delta: "auto" (attn_bwd's choice), "exact" (the extra pass over
+    the scores) or "from_out" (dout . out)."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
@@ -378,15 +384,16 @@ def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, strea
     dq = torch.empty(q.shape, dtype=gd, device=q.device)
     dk = torch.empty(k.shape, dtype=gd, device=q.device)
     dv = torch.empty(v.shape, dtype=gd, device=q.device)
+    mode = ROPE_MODES[rope] | DELTA_MODES[delta]
     if gd == torch.bfloat16:
-        attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
-                      ROPE_MODES[rope], scale, causal, stream)
-    elif rope == "half":
+        attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, mode,
+                      scale, causal, stream)
+    elif mode == 0:
         attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, scale, causal,
                  stream)
     else:
-        attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta,
-                    ROPE_MODES[rope], scale, causal, stream)
+        attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, mode,
+                    scale, causal, stream)
     return dq, dk, dv
 
 

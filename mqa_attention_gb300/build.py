@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libmqa_attention_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["api.cu", "rope.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "rope.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_decode.cu", "attn_delta.cu",
+           "noalloc.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "rope_math.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

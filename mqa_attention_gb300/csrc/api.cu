@@ -8,6 +8,7 @@
 #include <queue>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <tuple>
 #include <vector>
@@ -24,17 +25,44 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// One RoPE table (see launch_rope_table): positions [0, npos) of one (D, theta), four
+// fp32 arrays n floats apart, built on the stream of the call that first needed it.
+struct RopeTable {
+  float* buf = nullptr;
+  int npos = 0;
+  long long n = 0;
+  cudaEvent_t ready = nullptr;  // recorded after the build
+  // The last use by each stream that read the table outside stream capture: a retired
+  // table is freed once all of them have completed.
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;
+  bool pinned = false;   // read under stream capture: a graph may hold its address
+  bool retired = false;  // replaced or evicted: freed when the last holder releases it
+  int active = 0;        // calls between rope_acquire and rope_release
+  uint64_t tick = 0;     // last acquisition (least recently used is evicted first)
+};
+using RopePtr = std::shared_ptr<RopeTable>;
+
 struct DeviceState {
   bool init = false;
   bool supported = false;
-  int* status = nullptr;            // device status word
+  int* status = nullptr;            // device status word (a static device variable)
   cudaMemPool_t pool = nullptr;     // library-owned stream-ordered pool
-  std::map<std::tuple<int, int, uint64_t>, std::pair<float*, float*>> rope;  // (S, D, theta bits)
+  std::map<std::pair<int, uint32_t>, RopePtr> rope;  // (D, theta bits)
+  std::vector<RopePtr> to_free;     // retired under capture: freed by the next plain call
+  uint64_t tick = 0;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// RoPE tables kept per device (distinct (D, theta) pairs), and streams whose last use
+// of one table is tracked separately.
+constexpr int kRopeKeys = 8;
+constexpr int kRopeStreams = 8;
 bool g_inject_timeout = false;
+
+// Groups larger than this take the exact delta pass by default (see bwd_common).
+constexpr int kExactDeltaGroup = 8;
 
 // ------------------------------------------------------------------ profiling
 struct Profile {
@@ -159,6 +187,24 @@ int validate_blocks(int Sq, int Skv, int q_pos0, int kv_pos0) {
   return ATTN_OK;
 }
 
+// The device status word: a static device variable, zero when the library is loaded
+// on a device, so that no call allocates it. Kernels record an expired wait in it;
+// attn_sync_status reads and clears it.
+__device__ int g_status_word;
+int* g_status_ptr[kMaxDevices] = {};
+
+// Device address of the status word on device `dev` (the current device), looked up
+// once per device. Caller holds g_mu.
+int status_word_locked(int dev, int** out) {
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
 // Current device's state, initialised on first use. Returns an ATTN_* code.
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -172,8 +218,7 @@ int device_state(DeviceState** out) {
       return ATTN_ERR_CUDA;
     d.supported = major == 10 && minor == 3;
     if (d.supported) {
-      if (cudaMalloc(&d.status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-      if (cudaMemset(d.status, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (status_word_locked(dev, &d.status) != ATTN_OK) return ATTN_ERR_CUDA;
       cudaMemPoolProps props;
       std::memset(&props, 0, sizeof(props));
       props.allocType = cudaMemAllocationTypePinned;
@@ -191,38 +236,168 @@ int device_state(DeviceState** out) {
   return ATTN_OK;
 }
 
-// cos/sin table for (S, D, theta); built on first use (the stream is then
-// synchronised once so that the table is complete for every later stream).
-int rope_table(DeviceState* d, int S, int D, float theta, cudaStream_t stream, float** cs,
-               float** sn) {
+}  // namespace
+
+namespace gbattn {
+// The status word of the current device, for entry points that must not create the
+// library's pool (it allocates nothing).
+int device_status_word(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return status_word_locked(dev, out);
+}
+}  // namespace gbattn
+
+namespace {
+
+bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
+
+// Releases a retired table's memory in stream order on `stream` (alive and not capturing):
+// after every recorded use. A table read under capture stays allocated (a graph may
+// still read it). Caller holds g_mu.
+void rope_free_locked(RopeTable& t, cudaStream_t stream) {
+  for (auto& u : t.uses) cudaStreamWaitEvent(stream, u.second, 0);
+  if (!t.pinned && t.buf) cudaFreeAsync(t.buf, stream);
+  for (auto& u : t.uses) cudaEventDestroy(u.second);
+  if (t.ready) cudaEventDestroy(t.ready);
+  t.uses.clear();
+  t.ready = nullptr;
+  t.buf = nullptr;
+}
+
+// Marks a table retired; frees it now when no call holds it. Caller holds g_mu.
+void rope_retire_locked(DeviceState* d, const RopePtr& t, cudaStream_t stream, bool capturing) {
+  t->retired = true;
+  if (t->active > 0) return;  // the last rope_release frees it
+  if (capturing) d->to_free.push_back(t);
+  else rope_free_locked(*t, stream);
+}
+
+// The RoPE table of one call: the four arrays for positions [0, npos).
+struct RopeUse {
+  RopePtr t;
+  const float *ch = nullptr, *sh = nullptr, *cl = nullptr, *sl = nullptr;
+  int npos = 0;  // positions the table holds (>= the ones asked for)
+};
+
+// Table covering positions [0, npos) for (D, theta), built when missing or too short:
+// memory from the library pool and the build kernel, both in stream order on `stream`,
+// with no host synchronisation; another stream that reads the table before the build
+// has completed waits for it on the device. A longer table replaces a shorter one (at
+// least doubling its length); at most kRopeKeys (D, theta) pairs are kept, the least
+// recently used evicted first. A build cannot be recorded into a stream capture
+// (ATTN_ERR_UNSUPPORTED): the first call for a (D, theta), or for a longer sequence than
+// before, belongs outside capture. Pair with rope_release after the call's launches.
+int rope_acquire(DeviceState* d, int npos, int D, float theta, cudaStream_t stream,
+                 bool capturing, RopeUse* out) {
   uint32_t tb;
   std::memcpy(&tb, &theta, 4);
-  const auto key = std::make_tuple(S, D, static_cast<uint64_t>(tb));
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = d->rope.find(key);
-    if (it != d->rope.end()) {
-      *cs = it->second.first;
-      *sn = it->second.second;
-      return ATTN_OK;
-    }
-  }
-  const size_t n = static_cast<size_t>(S) * (D / 2);
-  float* buf = nullptr;
-  if (cudaMalloc(&buf, 2 * n * sizeof(float)) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (gbattn::launch_rope_table(buf, buf + n, S, D, static_cast<double>(theta), stream) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess) {
-    cudaFree(buf);
-    return ATTN_ERR_CUDA;
-  }
+  const auto key = std::make_pair(D, tb);
   std::lock_guard<std::mutex> lk(g_mu);
-  auto ins = d->rope.emplace(key, std::make_pair(buf, buf + n));
-  if (!ins.second) cudaFree(buf);  // another thread built it meanwhile
-  *cs = ins.first->second.first;
-  *sn = ins.first->second.second;
+  if (!capturing && !d->to_free.empty()) {
+    for (auto& t : d->to_free) rope_free_locked(*t, stream);
+    d->to_free.clear();
+  }
+  auto it = d->rope.find(key);
+  RopePtr t = it != d->rope.end() ? it->second : nullptr;
+  if (!t || t->npos < npos) {
+    if (capturing) return ATTN_ERR_UNSUPPORTED;
+    long long want = (static_cast<long long>(npos) + kTile - 1) / kTile * kTile;
+    if (t) want = std::max(want, std::min(2LL * t->npos, 1LL << 30));
+    auto nt = std::make_shared<RopeTable>();
+    nt->npos = static_cast<int>(want);
+    nt->n = (want * (D / 2) + 63) / 64 * 64;  // arrays 256-byte aligned
+    void* buf = nullptr;
+    if (cudaMallocFromPoolAsync(&buf, static_cast<size_t>(4 * nt->n) * sizeof(float), d->pool,
+                                stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    nt->buf = static_cast<float*>(buf);
+    if (gbattn::launch_rope_table(nt->buf, nt->n, nt->npos, D, static_cast<double>(theta),
+                                  stream) != cudaSuccess ||
+        cudaEventCreateWithFlags(&nt->ready, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(nt->ready, stream) != cudaSuccess) {
+      if (nt->ready) cudaEventDestroy(nt->ready);
+      cudaFreeAsync(nt->buf, stream);
+      return ATTN_ERR_CUDA;
+    }
+    if (t) {
+      rope_retire_locked(d, t, stream, false);
+    } else if (static_cast<int>(d->rope.size()) >= kRopeKeys) {
+      auto lru = d->rope.begin();
+      for (auto i = d->rope.begin(); i != d->rope.end(); ++i)
+        if (i->second->tick < lru->second->tick) lru = i;
+      rope_retire_locked(d, lru->second, stream, false);
+      d->rope.erase(lru);
+    }
+    d->rope[key] = nt;
+    t = nt;
+  } else if (cudaEventQuery(t->ready) != cudaSuccess) {
+    // built by another call whose stream may not have finished the build yet
+    if (cudaStreamWaitEvent(stream, t->ready, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  t->active += 1;
+  t->tick = ++d->tick;
+  if (capturing) t->pinned = true;
+  out->t = t;
+  out->ch = t->buf;
+  out->sh = t->buf + t->n;
+  out->cl = t->buf + 2 * t->n;
+  out->sl = t->buf + 3 * t->n;
+  out->npos = t->npos;
   return ATTN_OK;
 }
+
+// Ends a call's use of its table: records the stream's last use (outside capture) and
+// frees the table if it was retired meanwhile and nothing else holds it.
+void rope_release(DeviceState* d, RopeUse& u, cudaStream_t stream, bool capturing) {
+  if (!u.t) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  RopeTable& t = *u.t;
+  t.active -= 1;
+  if (!capturing) {
+    cudaEvent_t ev = nullptr;
+    for (auto& su : t.uses)
+      if (su.first == stream) ev = su.second;
+    if (!ev) {
+      if (static_cast<int>(t.uses.size()) >= kRopeStreams) {
+        // too many streams to track one by one: this stream takes over their uses
+        for (auto& su : t.uses) {
+          cudaStreamWaitEvent(stream, su.second, 0);
+          cudaEventDestroy(su.second);
+        }
+        t.uses.clear();
+      }
+      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess)
+        t.uses.emplace_back(stream, ev);
+      else
+        ev = nullptr;
+    }
+    if (ev) cudaEventRecord(ev, stream);
+  }
+  if (t.retired && t.active == 0) {
+    if (capturing) d->to_free.push_back(u.t);
+    else rope_free_locked(t, stream);
+  }
+  u.t.reset();
+}
+
+// Holds a call's RoPE table from acquisition to the end of the call (every launch that
+// reads it has been enqueued by then).
+struct RopeGuard {
+  DeviceState* d;
+  cudaStream_t stream;
+  bool capturing;
+  RopeUse u;
+  RopeGuard(DeviceState* d_, cudaStream_t s_) : d(d_), stream(s_), capturing(stream_capturing(s_)) {}
+  int acquire(int npos, int D, float theta) {
+    return rope_acquire(d, npos, D, theta, stream, capturing, &u);
+  }
+  ~RopeGuard() { rope_release(d, u, stream, capturing); }
+};
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -260,12 +435,12 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  float *cs = nullptr, *sn = nullptr;
   // Table rows for every position a kernel reads, the padding rows of a ragged
   // sequence included (they are rotated like any row, and then ignored).
   const int npos = q_pos0 + round_tile(Sq) > kv_pos0 + round_tile(Skv) ? q_pos0 + round_tile(Sq)
                                                                         : kv_pos0 + round_tile(Skv);
-  if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  RopeGuard rope(d, stream);
+  if ((st = rope.acquire(npos, D, rope_theta)) != ATTN_OK) return st;
 
   const int Sqp = round_tile(Sq), Skvp = round_tile(Skv);  // rows per head the kernels see
   const bool padded = Sqp != Sq || Skvp != Skv;
@@ -296,8 +471,10 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     rp.bwd = 0;
     rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
     rp.D = D;
-    rp.cos_tab = cs;
-    rp.sin_tab = sn;
+    rp.cos_tab = rope.u.ch;
+    rp.sin_tab = rope.u.sh;
+    rp.cos_lo = rope.u.cl;
+    rp.sin_lo = rope.u.sl;
     rp.seg[0] = {q, qr, nullptr, nullptr, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, padded ? v : nullptr, padded ? vk : nullptr, krows_p, Skv, Skvp, kv_pos0};
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
@@ -460,17 +637,30 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   int st = validate(ptrs, 9, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
   if (!ragged && (st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
-  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
-  const int inter = rope_mode == ATTN_ROPE_INTERLEAVED;
+  // rope_mode: the RoPE pair layout, optionally with one delta flag (self-attention only)
+  const int layout = rope_mode & 0xff;
+  const int dflags = rope_mode & ~0xff;
+  if (layout != ATTN_ROPE_HALF && layout != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  if (dflags != 0 && dflags != ATTN_DELTA_EXACT && dflags != ATTN_DELTA_FROM_OUT)
+    return ATTN_ERR_INVALID;
+  if (!ragged && dflags == ATTN_DELTA_EXACT) return ATTN_ERR_INVALID;
+  const int inter = layout == ATTN_ROPE_INTERLEAVED;
+  // delta from the scores (the exact pass) or from the bf16 `out` (one HBM read): by
+  // default exact when more than 8 query heads share a K/V head, whose dk sums the
+  // rounding of out over the whole group
+  const bool exact_delta =
+      ragged && (dflags == ATTN_DELTA_EXACT || (dflags == 0 && Hq / Hkv > kExactDeltaGroup));
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  float *cs = nullptr, *sn = nullptr;
   // Table rows for every position a kernel reads, the padding rows of a ragged
   // sequence included (they are rotated like any row, and then ignored).
   const int npos = q_pos0 + round_tile(Sq) > kv_pos0 + round_tile(Skv) ? q_pos0 + round_tile(Sq)
                                                                         : kv_pos0 + round_tile(Skv);
-  if ((st = rope_table(d, npos, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  RopeGuard rope(d, stream);
+  if ((st = rope.acquire(npos, D, rope_theta)) != ATTN_OK) return st;
+  const float* cs = rope.u.ch;
+  const float* sn = rope.u.sh;
 
   // The main kernel's work order (bwd_plan_cached) depends on the number of SMs.
   int dev = 0, nsm = 0;
@@ -533,10 +723,13 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
+    rp.cos_lo = rope.u.cl;
+    rp.sin_lo = rope.u.sl;
     rp.maxes = maxes;
     rp.seg[0] = {q, qr, dout, dos, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, v, vs, krows_p, Skv, Skvp, kv_pos0};
-    rp.out = out; rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
+    rp.out = exact_delta ? nullptr : out;
+    rp.delta = delta; rp.lse = lse; rp.lse2 = lse2; rp.dqacc = dqacc;
     if (plan.split > 0) {  // the main kernel adds dK/dV partials of two CTAs there
       rp.dk_zero = dk;
       rp.dv_zero = dv;
@@ -545,6 +738,26 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
   }
+  if (ok && exact_delta) {
+    gbattn::DeltaParams xp{};
+    ok = make_map(&xp.map_q, qr, qrows_p, D, kTile, true) &&
+         make_map(&xp.map_do, dos, qrows_p, D, kTile, true) &&
+         make_map(&xp.map_k, kr, krows_p, D, kTile, true) &&
+         make_map(&xp.map_v, vs, krows_p, D, kTile, true);
+    if (ok) {
+      xp.lse2 = lse2;
+      xp.maxes = maxes;
+      xp.delta = delta;
+      xp.status = d->status;
+      xp.B = B; xp.Hq = Hq; xp.Hkv = Hkv; xp.S = Sqp; xp.D = D;
+      xp.scale_log2 = scale * 1.4426950408889634f;
+      xp.causal = causal ? 1 : 0;
+      xp.inject_timeout = g_inject_timeout ? 1 : 0;
+      LaunchTimer tm(ATTN_KERNEL_DELTA, stream);
+      ok = gbattn::launch_delta(xp, stream) == cudaSuccess;
+      tm.done();
+    }
+  }
   gbattn::BwdParams bp{};
   const int bq = gbattn::bwd_query_tile(D);
   ok = ok && make_map(&bp.map_q, qr, qrows_p, D, bq, true) &&
@@ -552,7 +765,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
        make_map(&bp.map_k, kr, krows_p, D, kTile, true) &&
        make_map(&bp.map_v, vs, krows_p, D, kTile, true) &&
        make_map_f32(&bp.map_dk, dk, krows_p, D) && make_map_f32(&bp.map_dv, dv, krows_p, D) &&
-       make_map_f32(&bp.map_cos, cs, npos, D / 2) && make_map_f32(&bp.map_sin, sn, npos, D / 2);
+       make_map_f32(&bp.map_cos, cs, rope.u.npos, D / 2) &&
+       make_map_f32(&bp.map_sin, sn, rope.u.npos, D / 2);
   if (ok) {
     bp.lse2 = lse2;
     bp.delta = delta;
@@ -646,14 +860,16 @@ int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D, f
   int st = device_state(&d);
   if (st != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  float *cs = nullptr, *sn = nullptr;
-  if ((st = rope_table(d, pos0 + S, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  RopeGuard rope(d, stream);
+  if ((st = rope.acquire(pos0 + S, D, rope_theta)) != ATTN_OK) return st;
   gbattn::RowPrepParams rp{};
   rp.bwd = 0;
   rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
   rp.D = D;
-  rp.cos_tab = cs;
-  rp.sin_tab = sn;
+  rp.cos_tab = rope.u.ch;
+  rp.sin_tab = rope.u.sh;
+  rp.cos_lo = rope.u.cl;
+  rp.sin_lo = rope.u.sl;
   rp.seg[0] = {x, y, nullptr, nullptr, heads * S, S, S, pos0};
   rp.seg[1] = {x, y, nullptr, nullptr, 0, S, S, pos0};
   return gbattn::launch_row_prep(rp, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -673,8 +889,8 @@ int attn_decode(const void* q, const void* k_rot, const void* v, void* out, floa
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  float *cs = nullptr, *sn = nullptr;
-  if ((st = rope_table(d, q_pos0 + Sq, D, rope_theta, stream, &cs, &sn)) != ATTN_OK) return st;
+  RopeGuard rope(d, stream);
+  if ((st = rope.acquire(q_pos0 + Sq, D, rope_theta)) != ATTN_OK) return st;
   int dev = 0, nsm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -709,8 +925,10 @@ int attn_decode(const void* q, const void* k_rot, const void* v, void* out, floa
   if (ok) {
     dp.out = out;
     dp.lse = lse;
-    dp.cos_tab = cs;
-    dp.sin_tab = sn;
+    dp.cos_tab = rope.u.ch;
+    dp.sin_tab = rope.u.sh;
+    dp.cos_lo = rope.u.cl;
+    dp.sin_lo = rope.u.sl;
     dp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
     dp.status = d->status;
     dp.B = B; dp.Hq = Hq; dp.Hkv = Hkv; dp.Sq = Sq; dp.Skv = Skv; dp.D = D;

@@ -230,14 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       // ---- RoPE of this row of the Q tile, in place (128-byte swizzled rows). The
       // row's cos / sin values are loaded while the tile is in flight.
       float cv[D / 2], sv[D / 2];
+      const long long trow = static_cast<long long>(qpos) * (D / 2);
       if (row_real) {
-        const float4* cs = reinterpret_cast<const float4*>(p.cos_tab + static_cast<long long>(qpos) * (D / 2));
-        const float4* sn = reinterpret_cast<const float4*>(p.sin_tab + static_cast<long long>(qpos) * (D / 2));
+        const float4* cs = reinterpret_cast<const float4*>(p.cos_tab + trow);
+        const float4* sn = reinterpret_cast<const float4*>(p.sin_tab + trow);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) {
           const float4 a = __ldg(cs + i), bq = __ldg(sn + i);
           cv[4 * i] = a.x; cv[4 * i + 1] = a.y; cv[4 * i + 2] = a.z; cv[4 * i + 3] = a.w;
           sv[4 * i] = bq.x; sv[4 * i + 1] = bq.y; sv[4 * i + 2] = bq.z; sv[4 * i + 3] = bq.w;
+        }
+        // the lo parts are read group by group below: bring their lines to L1 now
+#pragma unroll
+        for (int i = 0; i < D / 2; i += 32) {
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(p.cos_lo + trow + i));
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(p.sin_lo + trow + i));
         }
       }
       ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ));
@@ -265,16 +272,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           // interleaved: columns [16g, +16) hold the pairs of frequencies 8g + k
           uint4* pa = chunk(rope_off_a(g, p.rope_interleaved != 0));
           uint4* pb = chunk(rope_off_b(g, D, p.rope_interleaved != 0));
-          float a[8], bb[8], c8[8], s8[8];
+          float a[8], bb[8], c8[8], s8[8], cl8[8], sl8[8];
           unpack(*pa, a);
           unpack(*pb, bb);
+          const float4* clo = reinterpret_cast<const float4*>(p.cos_lo + trow + 8 * g);
+          const float4* slo = reinterpret_cast<const float4*>(p.sin_lo + trow + 8 * g);
+          const float4 c0 = __ldg(clo), c1 = __ldg(clo + 1), s0 = __ldg(slo), s1 = __ldg(slo + 1);
+          cl8[0] = c0.x; cl8[1] = c0.y; cl8[2] = c0.z; cl8[3] = c0.w;
+          cl8[4] = c1.x; cl8[5] = c1.y; cl8[6] = c1.z; cl8[7] = c1.w;
+          sl8[0] = s0.x; sl8[1] = s0.y; sl8[2] = s0.z; sl8[3] = s0.w;
+          sl8[4] = s1.x; sl8[5] = s1.y; sl8[6] = s1.z; sl8[7] = s1.w;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             c8[k] = cv[8 * g + k];
             s8[k] = sv[8 * g + k];
           }
           float ya[8], yb[8];
-          rope_rotate16(a, bb, c8, s8, p.rope_interleaved != 0, 1.f, ya, yb);
+          rope_rotate16_exact(a, bb, c8, cl8, s8, sl8, p.rope_interleaved != 0, ya, yb);
           *pa = pack(ya);
           *pb = pack(yb);
         }

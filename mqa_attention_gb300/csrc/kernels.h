@@ -76,9 +76,15 @@ __host__ __device__ inline BwdExponents bwd_exponents(const float* maxes) {
   return x;
 }
 
+// Device address of the library's status word on the current device (a static device
+// variable: looking it up allocates nothing). Returns an ATTN_* code.
+int device_status_word(int** out);
+
 // ---------------------------------------------------------------- row kernels
-// RoPE cos/sin table, [S][D/2] fp32 each, built in fp64.
-cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
+// RoPE table for positions 0..S-1: four fp32 arrays [S][D/2], n floats apart (n >=
+// S*D/2): cos hi, sin hi, cos lo, sin lo, where hi + lo is the fp64 value to about
+// 48 significant bits (hi alone: the fp64 value rounded to fp32).
+cudaError_t launch_rope_table(float* tab, long long n, int S, int D, double theta,
                               cudaStream_t stream);
 
 // Largest |value| of up to four bf16 tensors, atomically max-ed into maxes[i]
@@ -112,10 +118,12 @@ struct RowPrepParams {
   int rope_interleaved;  // 0: half-split pairs (i, i + D/2); 1: pairs (2i, 2i + 1)
   RowSegment seg[2];
   int D;
-  const float* cos_tab;
+  const float* cos_tab;  // table hi parts
   const float* sin_tab;
+  const float* cos_lo;   // table lo parts
+  const float* sin_lo;
   const float* maxes;  // backward
-  const void* out;     // backward, query rows
+  const void* out;     // backward, query rows (null: delta is written by the delta pass)
   float* delta;
   const float* lse;
   float* lse2;
@@ -197,6 +205,25 @@ struct BwdParams {
   short plan_kt[kMaxBwdPlan];
   signed char plan_parts[kMaxBwdPlan];
 };
+// Exact delta pass: delta_i = sum_j P_ij dP_ij over the visible keys of each query row,
+// from the backward pre-pass's fp16 operands (self-attention, S rows per head, a
+// multiple of 128). Written scaled by 2^(edo+ev), as the main kernel reads delta.
+struct DeltaParams {
+  CUtensorMap map_q;   // scaled rotated q (fp16), box {64, 128}
+  CUtensorMap map_do;  // scaled dout (fp16), box {64, 128}
+  CUtensorMap map_k;   // scaled rotated k (fp16), box {64, 128}
+  CUtensorMap map_v;   // scaled v (fp16), box {64, 128}
+  const float* lse2;   // lse * log2(e), [B*Hq*S] (+inf on padding rows)
+  const float* maxes;  // the abs-max pass's four maxima
+  float* delta;        // [B*Hq*S], written
+  int* status;
+  int B, Hq, Hkv, S, D;
+  float scale_log2;    // scale * log2(e)
+  int causal;
+  int inject_timeout;
+};
+cudaError_t launch_delta(const DeltaParams& p, cudaStream_t stream);
+
 // Query-tile rows used by the backward main kernel for head dimension D.
 inline int bwd_query_tile(int) { return 64; }
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
@@ -211,8 +238,10 @@ struct DecParams {
   float* part_lse;    // [nchunks][rows]: each chunk's lse (-inf: no key seen)
   void* out;          // [rows][D] bf16
   float* lse;         // [rows]
-  const float* cos_tab;
+  const float* cos_tab;  // table hi parts
   const float* sin_tab;
+  const float* cos_lo;   // table lo parts
+  const float* sin_lo;
   int rope_interleaved;
   int* status;
   int B, Hq, Hkv, Sq, Skv, D;

@@ -11,12 +11,13 @@
 // array's device address (cudaGetSymbolAddress, with that device current), so
 // that first call belongs before any stream capture.
 //
-// The array holds, for one call: a status word, the RoPE cos/sin table and the
-// rotated q and k. Every call on a device uses the same array and leaves its
-// contents behind; the status word is cleared at the start of each call and
-// everything else is fully rewritten before it is read. Two calls whose work
+// The array holds, for one call: the RoPE cos/sin table and the rotated q and k.
+// Every call on a device uses the same array and leaves its contents behind;
+// everything in it is fully rewritten before it is read. Two calls whose work
 // overlaps on the GPU (different streams, or different host threads) race on
-// the array and produce undefined results: serialise them.
+// the array and produce undefined results: serialise them. A kernel wait that
+// expires is recorded in the library's status word (a static device variable,
+// found without allocating), which attn_sync_status reads.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -97,13 +98,14 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   if (static_cast<long long>(B) * Hq * S >= (1LL << 31)) return ATTN_ERR_INVALID;
   if ((D != 64 && D != 128) || S % gbattn::kTile != 0) return ATTN_ERR_UNSUPPORTED;
 
-  // Scratch layout: status | cos | sin | rotated q | rotated k.
+  // Scratch layout: table (cos hi | sin hi | cos lo | sin lo) | rotated q | rotated k.
   const long long qrows = static_cast<long long>(B) * Hq * S;
   const long long krows = static_cast<long long>(B) * Hkv * S;
-  const size_t tab = round256(static_cast<size_t>(S) * (D / 2) * sizeof(float));
+  const long long tab_n = (static_cast<long long>(S) * (D / 2) + 63) / 64 * 64;  // floats per array
+  const size_t tab = static_cast<size_t>(tab_n) * sizeof(float);
   const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
-  const size_t need = 256 + 2 * tab + qbytes + kbytes;
+  const size_t need = 4 * tab + qbytes + kbytes;
   if (need > kScratchBytes) return ATTN_ERR_UNSUPPORTED;  // beyond the fixed array
 
   int dev = 0, major = 0, minor = 0;
@@ -115,23 +117,24 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   void* base = nullptr;
   int st = scratch_address(dev, &base);
   if (st != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = gbattn::device_status_word(&status)) != ATTN_OK) return st;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* w = static_cast<uint8_t*>(base);
-  int* status = reinterpret_cast<int*>(w);
-  float* cs = reinterpret_cast<float*>(w + 256);
-  float* sn = reinterpret_cast<float*>(w + 256 + tab);
-  void* qr = w + 256 + 2 * tab;
-  void* kr = w + 256 + 2 * tab + qbytes;
+  float* tabp = reinterpret_cast<float*>(w);
+  void* qr = w + 4 * tab;
+  void* kr = w + 4 * tab + qbytes;
 
-  bool ok = cudaMemsetAsync(status, 0, sizeof(int), stream) == cudaSuccess;
-  ok = ok && gbattn::launch_rope_table(cs, sn, S, D, static_cast<double>(rope_theta), stream) ==
-                 cudaSuccess;
+  bool ok = gbattn::launch_rope_table(tabp, tab_n, S, D, static_cast<double>(rope_theta),
+                                      stream) == cudaSuccess;
   gbattn::RowPrepParams rp{};
   rp.bwd = 0;
   rp.D = D;
-  rp.cos_tab = cs;
-  rp.sin_tab = sn;
+  rp.cos_tab = tabp;
+  rp.sin_tab = tabp + tab_n;
+  rp.cos_lo = tabp + 2 * tab_n;
+  rp.sin_lo = tabp + 3 * tab_n;
   rp.seg[0] = {q, qr, nullptr, nullptr, qrows, S, S, 0};
   rp.seg[1] = {k, kr, nullptr, nullptr, krows, S, S, 0};
   ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;

@@ -24,8 +24,12 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict__ sin_tab, int S,
-                                  int D, double theta) {
+// cos and sin of p * theta^(-2i/D), p < S, i < D/2, evaluated in fp64 and stored as
+// fp32 pairs: hi = fp32(x), lo = fp32(x - hi), so that hi + lo carries about 48
+// significant bits of the fp64 value. The four arrays [S][D/2] are cos hi, sin hi,
+// cos lo, sin lo, n = S*D/2 floats apart.
+__global__ void rope_table_kernel(float* __restrict__ tab, long long n, int S, int D,
+                                  double theta) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
   const int half = D / 2;
@@ -34,10 +38,13 @@ __global__ void rope_table_kernel(float* __restrict__ cos_tab, float* __restrict
   const int p = static_cast<int>(idx / half);
   const int i = static_cast<int>(idx % half);
   const double inv_freq = pow(theta, -2.0 * i / static_cast<double>(D));
-  double s, c;
-  sincos(static_cast<double>(p) * inv_freq, &s, &c);
-  cos_tab[idx] = static_cast<float>(c);
-  sin_tab[idx] = static_cast<float>(s);
+  double sv, cv;
+  sincos(static_cast<double>(p) * inv_freq, &sv, &cv);
+  const float ch = static_cast<float>(cv), sh = static_cast<float>(sv);
+  tab[idx] = ch;
+  tab[n + idx] = sh;
+  tab[2 * n + idx] = static_cast<float>(cv - static_cast<double>(ch));
+  tab[3 * n + idx] = static_cast<float>(sv - static_cast<double>(sh));
 }
 
 struct alignas(16) Vec8x16 {
@@ -137,110 +144,199 @@ __global__ void __launch_bounds__(kAbsMaxThreads) absmax_kernel(const AbsMaxPara
   }
 }
 
-// One thread per (output row, c) with c < D/16 and the two element groups of
-// rope_off_a / rope_off_b. Rows [0, seg[0].rows) are query rows, the next
-// seg[1].rows are key rows; a segment's outputs hold Sp rows per head, of which
-// the first S are its input rows (the rest, when the sequence is padded to whole
-// tiles, are written as rows that contribute nothing: zero operands, delta 0 and,
-// in the backward, lse * log2 e = +inf so that their probabilities are 0).
+// Work of one thread of the row pre-pass: kRopePairs rotation pairs (table entries
+// loaded once) of one row position, in kHeadsPerThread heads.
+constexpr int kRopePairs = 4;
+constexpr int kHeadsPerThread = 1;
+
+template <int N>
+struct alignas(4 * N) Bf16xN {  // N bf16 / fp16 values
+  uint32_t w[N / 2];
+};
+template <int N>
+__device__ __forceinline__ void loadn_bf16(const void* p, float (&o)[N]) {
+  const Bf16xN<N> x = *reinterpret_cast<const Bf16xN<N>*>(p);
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.w[i]));
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void storen_bf16(void* p, const float (&o)[N]) {
+  Bf16xN<N> x;
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+    x.w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<Bf16xN<N>*>(p) = x;
+}
+// Rounds to bf16 (nearest even), multiplies by the power of two s (exact) and stores
+// as fp16 (exact while the result is a normal fp16 number).
+template <int N>
+__device__ __forceinline__ void storen_bf16_scaled_f16(void* p, const float (&o)[N], float s) {
+  Bf16xN<N> x;
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float a = __bfloat162float(__float2bfloat16_rn(o[2 * i])) * s;
+    const float b = __bfloat162float(__float2bfloat16_rn(o[2 * i + 1])) * s;
+    __half2 h = __floats2half2_rn(a, b);
+    x.w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<Bf16xN<N>*>(p) = x;
+}
+__device__ __forceinline__ void load4(const float* p, float (&o)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+}
+__device__ __forceinline__ void zero4(float* p) {
+  *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Threads of one segment: (position, chunk c < D/(2 kRopePairs), group of
+// kHeadsPerThread heads), chunks fastest, then positions, so that the threads of a row
+// are adjacent lanes and a warp covers consecutive rows of one head.
+template <int D>
+__device__ __forceinline__ long long seg_threads(const RowSegment& sg) {
+  if (sg.rows == 0) return 0;
+  const long long heads = sg.rows / sg.Sp;
+  return static_cast<long long>(sg.Sp) * (D / (2 * kRopePairs)) *
+         ((heads + kHeadsPerThread - 1) / kHeadsPerThread);
+}
+
+// Query rows (segment 0) and key rows (segment 1) of one call: each output row holds
+// the rotated input row of its head and position (half-split or interleaved pairs,
+// the exact rotation rounded to bf16). A segment's outputs hold Sp rows per head, of
+// which the first S are its input rows; when the sequence is padded to whole tiles the
+// rest are written as rows that contribute nothing (zero operands, delta 0 and, in
+// the backward, lse * log2 e = +inf so that their probabilities are 0).
 template <int D, bool kBwd, bool kPad>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
-  constexpr int T = D / 16;  // threads per row
+  constexpr int NP = kRopePairs;
+  constexpr int HT = kHeadsPerThread;
+  constexpr int T = D / (2 * NP);  // threads per row
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long grow = t / T;
-  const int c = static_cast<int>(t % T);
-  const bool is_q = grow < p.seg[0].rows;
+  const long long n0 = seg_threads<D>(p.seg[0]);
+  const bool is_q = t < n0;
   const RowSegment& sg = is_q ? p.seg[0] : p.seg[1];
-  const long long row0 = is_q ? grow : grow - p.seg[0].rows;
-  // Threads past the last row read row 0 of the segment (a valid address), take
-  // part in the shuffles below and write nothing.
-  const bool live = row0 < sg.rows;
-  // output row, its head and row within the head (rows < 2^31: 32-bit division)
-  const unsigned ro32 = live ? static_cast<unsigned>(row0) : 0u;
-  const unsigned head = ro32 / static_cast<unsigned>(sg.Sp);
-  const int i = static_cast<int>(ro32 - head * static_cast<unsigned>(sg.Sp));
-  const long long ro = ro32;
+  const long long u = is_q ? t : t - n0;
+  // the T threads of a row leave together (thread counts are multiples of T)
+  if (u >= seg_threads<D>(sg)) return;
+  const int c = static_cast<int>(u % T);
+  const long long pr = u / T;
+  const int i = static_cast<int>(pr % sg.Sp);  // row within the head
+  const int g = static_cast<int>(pr / sg.Sp);  // head group
+  const int heads = static_cast<int>(sg.rows / sg.Sp);
+  const int h0 = g * HT;
+  const int nh = min(HT, heads - h0);
   const bool real = !kPad || i < sg.S;  // kPad = false: every output row is an input row
-  const long long ri =  // input row
-      !kPad ? ro : (real ? static_cast<long long>(head) * sg.S + i : 0);
   const int pos = sg.pos0 + (real ? i : 0);
   const bool inter = p.rope_interleaved != 0;
-  const int oa = rope_off_a(c, inter), ob = rope_off_b(c, D, inter);
-  const long long e1 = ri * D + oa, e2 = ri * D + ob;  // input elements
-  const long long f1 = ro * D + oa, f2 = ro * D + ob;  // output elements
-  const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
-  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e1, x1);
-  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
-  load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
-  load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
-  rope_rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
-  if (!real) {
+  const int oa = rope_off_a_n<NP>(c, inter), ob = rope_off_b_n<NP>(c, D, inter);
+  const bool x2_in = kBwd || sg.y2 != nullptr;  // a second tensor (dout / v) to copy
+  const bool dot = kBwd && is_q && p.out != nullptr;  // delta from out
+  auto row_in = [&](int k) {  // input row of head h0 + k
+    const long long h = h0 + k;
+    return !kPad ? h * sg.Sp + i : h * sg.S + (real ? i : 0);
+  };
+  // Every load of the thread's heads is issued before any is used (the table, then
+  // NP elements of each of the row's halves per head and tensor), so that enough
+  // bytes are in flight for the HBM stream.
+  Bf16xN<NP> xa[HT], xb[HT], za[HT], zb[HT], oa_[HT], ob_[HT];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) y1[k] = y2[k] = 0.f;
-  }
-  if constexpr (!kBwd) {
-    if (live) {
-      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
-      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
-      if (sg.y2 != nullptr) {  // padded copy of v (key rows)
-        float a1[8], a2[8];
-        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
-        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
-        if (!real) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
-        }
-        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
-        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
+  for (int k = 0; k < HT; ++k) {
+    if (k < nh) {
+      const long long r = row_in(k) * D;
+      xa[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x) + r + oa);
+      xb[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x) + r + ob);
+      if (x2_in) {
+        za[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x2) + r + oa);
+        zb[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x2) + r + ob);
+      }
+      if (dot) {
+        oa_[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(p.out) + r + oa);
+        ob_[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(p.out) + r + ob);
       }
     }
-  } else {
-    const BwdExponents ex = bwd_exponents(p.maxes);
-    const float s_rot = exp2i(is_q ? ex.q : ex.k);
-    const float s_x2 = exp2i(is_q ? ex.dout : ex.v);
-    float a1[8], a2[8];
-    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
+  }
+  float chi[NP], clo[NP], shi[NP], slo[NP];
+  const long long te = (long long)pos * H + NP * c;
+  load4(p.cos_tab + te, chi);
+  load4(p.sin_tab + te, shi);
+  load4(p.cos_lo + te, clo);
+  load4(p.sin_lo + te, slo);
+  BwdExponents ex{0, 0, 0, 0};
+  if constexpr (kBwd) ex = bwd_exponents(p.maxes);
+  const float s_rot = exp2i(is_q ? ex.q : ex.k);
+  const float s_x2 = exp2i(is_q ? ex.dout : ex.v);
+  // lanes of this row, for the delta reduction
+  const unsigned lane = threadIdx.x & 31u;
+  const unsigned row_mask = ((1u << T) - 1u) << (lane & ~static_cast<unsigned>(T - 1));
+  auto unpack = [](const Bf16xN<NP>& v, float (&o)[NP]) {
+#pragma unroll
+    for (int e = 0; e < NP / 2; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.w[e]));
+      o[2 * e] = f.x;
+      o[2 * e + 1] = f.y;
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < HT; ++k) {
+    if (k >= nh) break;
+    const long long ro = static_cast<long long>(h0 + k) * sg.Sp + i;  // output row
+    const long long f1 = ro * D + oa, f2 = ro * D + ob;               // output elements
+    float x1[NP], x2[NP], y1[NP], y2[NP], a1[NP], a2[NP];
+    unpack(xa[k], x1);
+    unpack(xb[k], x2);
+    rope_rotate_exact<NP>(x1, x2, chi, clo, shi, slo, inter, y1, y2);
+    if (x2_in) {
+      unpack(za[k], a1);
+      unpack(zb[k], a2);
+    }
     if (!real) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
+      for (int e = 0; e < NP; ++e) y1[e] = y2[e] = a1[e] = a2[e] = 0.f;
     }
-    if (live) {
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f1, y1, s_rot);
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f2, y2, s_rot);
-      // x2 is already bf16: scaling by a power of two and storing fp16 is exact
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
-      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
-    }
-    // delta for query rows. Every thread computes it and takes part in the
-    // shuffle (a warp may straddle the query/key boundary); key rows read row 0
-    // of `out` and write nothing.
-    float o1[8], o2[8];
-    const long long eo = is_q ? 0 : ri * D;
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e1 - eo), o1);
-    load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e2 - eo), o2);
-    float dot = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dot += a1[k] * o1[k] + a2[k] * o2[k];
-#pragma unroll
-    for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (!is_q && live && p.dk_zero != nullptr && i < p.dk_zero_rows) {
-      store8(p.dk_zero + f1, z);
-      store8(p.dk_zero + f2, z);
-      store8(p.dv_zero + f1, z);
-      store8(p.dv_zero + f2, z);
-    }
-    if (is_q && live) {
-      if (c == 0) {
-        p.delta[ro] = real ? dot * exp2i(ex.dout + ex.v) : 0.f;
-        p.lse2[ro] = real ? p.lse[ri] * kLog2e : INFINITY;
+    if constexpr (!kBwd) {
+      storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
+      storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
+      if (sg.y2 != nullptr) {  // padded copy of v (key rows)
+        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
+        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
       }
-      store8(p.dqacc + f1, z);
-      store8(p.dqacc + f2, z);
+    } else {
+      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f1, y1, s_rot);
+      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f2, y2, s_rot);
+      // x2 is already bf16: scaling by a power of two and storing fp16 is exact
+      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
+      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
+      if (is_q) {
+        // delta_i = dout_i . out_i (unless the exact delta pass writes it instead)
+        if (dot) {
+          float o1[NP], o2[NP];
+          unpack(oa_[k], o1);
+          unpack(ob_[k], o2);
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < NP; ++e) d += a1[e] * o1[e] + a2[e] * o2[e];
+#pragma unroll
+          for (int o = T / 2; o > 0; o >>= 1) d += __shfl_xor_sync(row_mask, d, o);
+          if (c == 0) p.delta[ro] = real ? d * exp2i(ex.dout + ex.v) : 0.f;
+        }
+        if (c == 0) p.lse2[ro] = real ? p.lse[row_in(k)] * kLog2e : INFINITY;
+        zero4(p.dqacc + f1);
+        zero4(p.dqacc + f2);
+      } else if (p.dk_zero != nullptr && i < p.dk_zero_rows) {
+        zero4(p.dk_zero + f1);
+        zero4(p.dk_zero + f2);
+        zero4(p.dv_zero + f1);
+        zero4(p.dv_zero + f2);
+      }
     }
   }
 }
@@ -373,11 +469,11 @@ long long blocks_for(long long threads) { return (threads + 255) / 256; }
 
 }  // namespace
 
-cudaError_t launch_rope_table(float* cos_tab, float* sin_tab, int S, int D, double theta,
+cudaError_t launch_rope_table(float* tab, long long n, int S, int D, double theta,
                               cudaStream_t stream) {
-  const long long n = (long long)S * (D / 2);
-  return launch_pdl(rope_table_kernel, dim3((unsigned)blocks_for(n)), dim3(256), 0, stream, cos_tab,
-                    sin_tab, S, D, theta);
+  const long long cnt = (long long)S * (D / 2);
+  return launch_pdl(rope_table_kernel, dim3((unsigned)blocks_for(cnt)), dim3(256), 0, stream, tab,
+                    n, S, D, theta);
 }
 
 cudaError_t launch_absmax(const AbsMaxParams& p_in, cudaStream_t stream) {
@@ -402,7 +498,14 @@ cudaError_t launch_absmax(const AbsMaxParams& p_in, cudaStream_t stream) {
 }
 
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
-  const long long threads = (p.seg[0].rows + p.seg[1].rows) * (p.D / 16);
+  auto seg_thr = [&](const RowSegment& sg) {
+    if (sg.rows == 0) return 0LL;
+    const long long heads = sg.rows / sg.Sp;
+    return static_cast<long long>(sg.Sp) * (p.D / (2 * kRopePairs)) *
+           ((heads + kHeadsPerThread - 1) / kHeadsPerThread);
+  };
+  const long long threads = seg_thr(p.seg[0]) + seg_thr(p.seg[1]);
+  if (threads == 0) return cudaSuccess;
   const unsigned grid = (unsigned)blocks_for(threads);
   const bool pad = p.seg[0].S != p.seg[0].Sp || p.seg[1].S != p.seg[1].Sp;
 #define GB_PREP(DD, BW, PD) \
