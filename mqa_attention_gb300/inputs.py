@@ -19,6 +19,7 @@ import numpy as np
 
 __all__ = [
     "normal_bf16_bits",
+    "scale_bf16_bits",
     "bf16_bits_to_f64",
     "bf16_bits_to_f32",
     "seed_for",
@@ -86,3 +87,22 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def scale_bf16_bits(bits: np.ndarray, factor: float, index=None) -> np.ndarray:
+    """bf16 bit patterns of (value * factor), rounded to nearest even, for the whole
+    array or only at ``index`` (a numpy index into the array). Used to give seeded
+    inputs a larger spread or single large elements. The product of a bf16 value and
+    a factor with few significant bits (3, 6, 16, 4096, ...) is exact in fp32, so the
+    one rounding to bf16 is the only one (checked)."""
+    out = bits.copy()
+    sel = out if index is None else out[index]
+    x = bf16_bits_to_f32(np.asarray(sel)).astype(np.float64) * float(factor)
+    x32 = x.astype(np.float32)
+    if not np.array_equal(x32.astype(np.float64), x):
+        raise ValueError("factor leaves products that are not exact in fp32")
+    y = _f32_to_bf16_bits(np.atleast_1d(x32)).reshape(np.shape(sel))
+    if index is None:
+        return y.astype(np.uint16)
+    out[index] = y
+    return out

@@ -87,6 +87,28 @@ def test_ex_entry_points_reject_unknown_rope_modes(built_lib, mode):
                            10000.0, mode, 0.125, 1, None) == M.ATTN_ERR_INVALID
 
 
+@pytest.mark.parametrize("mode", [0x100 | 0x200, 0x400, 0x100 | 2])
+def test_bwd_rejects_bad_delta_flags(built_lib, mode):
+    """ATTN_DELTA_EXACT (0x100) and ATTN_DELTA_FROM_OUT (0x200) exclude each other; no
+    other flag exists; the layout must still be valid."""
+    assert built_lib.attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1,
+                                 128, 64, 10000.0, mode, 0.125, 1, None) == M.ATTN_ERR_INVALID
+    assert built_lib.attn_bwd_bf16(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1,
+                                   128, 64, 10000.0, mode, 0.125, 1, None) == M.ATTN_ERR_INVALID
+
+
+def test_delta_flags_only_where_they_apply(built_lib):
+    """The exact delta pass needs the whole attention of each query row: a partial
+    block's backward and every forward entry point refuse the flag."""
+    lib = built_lib
+    exact = M.DELTA_MODES["exact"]
+    assert lib.attn_bwd_partial(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1,
+                                128, 128, 64, 0, 0, 10000.0, exact, 0.125, 1,
+                                None) == M.ATTN_ERR_INVALID
+    assert lib.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 128, 64, 10000.0, exact, 0.125,
+                           1, None) == M.ATTN_ERR_INVALID
+
+
 def test_profile_arguments(built_lib):
     assert built_lib.attn_profile_begin(0) == M.ATTN_ERR_INVALID
     n, ms = ctypes.c_int(), ctypes.c_float()

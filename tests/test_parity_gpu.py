@@ -4,6 +4,8 @@ Tolerances: out, dq, dk, dv max-abs 2e-2 and mean-abs 2e-3; lse abs 1e-3
 against the oracle with bf16-rounded RoPE(q), RoPE(k) (the precision in which
 the rotated operands reach the score product); out and the gradients are also
 held to the same bounds against the oracle with exact fp64 RoPE."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -57,20 +59,27 @@ def assert_close(name, got, want, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     assert mx <= max_abs and mn <= mean_abs, f"{name}: max-abs {mx:.3e} mean-abs {mn:.3e}"
 
 
-def grad_bounds(wl):
-    """(max-abs, mean-abs) bounds for dq/dk/dv. The stated 2e-2 / 2e-3 cover the
-    workloads, whose groups have G = Hq/Hkv <= 8 query heads. dk and dv sum the
-    independent rounding errors (delta from the bf16 `out`, fp16 dS and P) of
-    all G heads, so their spread grows as sqrt(G): shapes with G > 8 scale both
-    bounds by sqrt(G/8)."""
-    f = max(1.0, (wl.Hq // wl.Hkv / 8) ** 0.5)
-    return MAX_ABS * f, MEAN_ABS * f
-
-
 def check_all(wl, g, f, backward=True, rope="half"):
-    """Full oracle comparison (both RoPE precisions)."""
-    gmax, gmean = grad_bounds(wl)
+    """Full oracle comparison at the stated bounds, whatever the group size, against
+    the oracle whose rotated q~, k~ are rounded to bf16 (the library's definition:
+    the operands the score product receives); against the exact-fp64-RoPE oracle too
+    while G = Hq/Hkv <= 8. Beyond that the two oracles themselves differ by more than
+    the bounds (dk sums the bf16 rounding of q~ over all G heads: at G = 48,
+    S = 384, D = 128 they differ by 0.045 in dk and 0.029 in dv), so no result can
+    meet both; there the exact-RoPE errors are only printed."""
+    gmax, gmean = MAX_ABS, MEAN_ABS
+    gate_exact = wl.Hq // wl.Hkv <= 8
     for rr in (True, False):
+        if not rr and not gate_exact:
+            out, _ = O.attention_forward(f["q"], f["k"], f["v"], wl.scale, wl.theta, wl.causal,
+                                         rope=rope)
+            msg = [f"out {err(g['out'], out)[0]:.3e}"]
+            if backward:
+                want = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale,
+                                            wl.theta, wl.causal, rope=rope)
+                msg += [f"{n} {err(g[n], w)[0]:.3e}" for n, w in zip(("dq", "dk", "dv"), want)]
+            print(f"exact-RoPE oracle, G={wl.Hq // wl.Hkv}: max-abs " + ", ".join(msg))
+            continue
         out, lse = O.attention_forward(f["q"], f["k"], f["v"], wl.scale, wl.theta, wl.causal,
                                        rope=rope, round_rotated=rr)
         assert_close(f"out(rr={rr})", g["out"], out)
@@ -85,7 +94,7 @@ def check_all(wl, g, f, backward=True, rope="half"):
 
 
 SMALL = [
-    # (B, Hq, Hkv, S, D, causal): single tile, odd tile counts, G in {1,2,3,4,8,32}
+    # (B, Hq, Hkv, S, D, causal): single tile, odd tile counts, G in {1,2,3,4,8,32,48}
     (1, 4, 1, 128, 64, True),
     (1, 2, 1, 256, 128, True),
     (2, 4, 2, 384, 64, True),
@@ -93,6 +102,7 @@ SMALL = [
     (1, 8, 1, 256, 64, True),
     (1, 4, 4, 256, 128, True),
     (1, 32, 1, 128, 64, True),
+    (1, 48, 1, 256, 128, True),
     (2, 2, 1, 256, 64, False),
     (1, 4, 2, 384, 128, False),
     # more steps than SMs: CTAs of the persistent backward cross key-tile units,
@@ -179,7 +189,7 @@ def test_bf16_gradients(B, Hq, Hkv, S, D, causal, rope):
     assert ((a - b).abs() <= torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + slack).all(), "dq"
     want = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta, wl.causal,
                                 rope=rope, round_rotated=True)
-    gmax, gmean = grad_bounds(wl)
+    gmax, gmean = MAX_ABS, MEAN_ABS
     for name, got, ref in zip(("dq", "dk", "dv"), g16, want):
         e = (got.double().cpu() - ref).abs()
         half_ulp = ref.abs() * 2.0 ** -8
@@ -282,7 +292,8 @@ def _sample(S, n, seed):
 
 def test_long_context_sampled():
     """S = 32768: out, lse, dq on 256 seeded query rows of every head; dk, dv on
-    256 seeded key rows of KV head 0; exact sums over the full tensors."""
+    256 seeded key rows of every KV head (all 32768 query rows of its group enter);
+    exact sums over the full tensors."""
     wl = by_index(5)
     dev, f = gen(wl)
     g = run_gpu(wl, dev)
@@ -295,9 +306,9 @@ def test_long_context_sampled():
     assert_close("dq", g["dq"][:, :, rows], dq)
     keys = _sample(wl.S, 256, 5002)
     dk, dv = O.backward_dkdv_keys(f["q"], f["k"], f["v"], f["dout"], keys, wl.scale, wl.theta,
-                                  round_rotated=True, batches=[0], kv_heads=[0], row_block=2048)
-    assert_close("dk", g["dk"][0:1, 0:1, keys], dk)
-    assert_close("dv", g["dv"][0:1, 0:1, keys], dv)
+                                  round_rotated=True, row_block=2048)
+    assert_close("dk", g["dk"][:, :, keys], dk)
+    assert_close("dv", g["dv"][:, :, keys], dv)
     _full_tensor_invariants(wl, g, f)
 
 
@@ -347,3 +358,216 @@ def test_power_of_two_input_scales_are_exact(D, hkv):
     # differ by fp32 rounding of those sums, bounded here against the largest |dq|
     want = base["dq"] * 2.0 ** -8
     assert (got["dq"] - want).abs().max().item() <= 2.0 ** -16 * want.abs().max().item()
+
+
+# ------------------------------------------------------------------ the method's numerics
+# Inputs whose softmax rows are far from the diffuse N(0, 1) case: the row maximum that
+# the online softmax subtracts ("ColossalAI 中的 PaLM 教学实现…", §2.5) then decides
+# nearly all of each row. These use the exact delta pass (ATTN_DELTA_EXACT): with
+# delta = dout . out from the bf16 `out`, the rounding of out dominates dq and dk on
+# peaked rows. They are held to the stated bounds against the oracle whose rotated
+# q~, k~ are rounded to bf16 (the operands the score product receives; the kernels
+# round the exact rotation, so both sides hold the same q~, k~): with scores of
+# standard deviation 9-36 a one-ulp change of q~ moves a score by up to ~0.1, far
+# beyond what the exact-rotation oracle could be compared against.
+
+
+def gen_scaled(wl, factors):
+    """Seeded inputs with some tensors multiplied exactly (bf16 rounding of the
+    product): factors maps a tensor name to (factor, index or None)."""
+    host = {n: I.normal_bf16_bits(I.seed_for(wl.index, n), s) for n, s in wl.shapes().items()}
+    for n, spec in factors.items():
+        for fac, idx in spec:
+            host[n] = I.scale_bf16_bits(host[n], fac, idx)
+    dev = {n: torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).cuda()
+           for n, h in host.items()}
+    f64 = {n: torch.from_numpy(I.bf16_bits_to_f64(h)) for n, h in host.items()}
+    return dev, f64
+
+
+def run_exact(wl, dev):
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+    dq, dk, dv = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta,
+                            wl.scale, wl.causal, delta="exact")
+    torch.cuda.synchronize()
+    assert M.sync_status() == 0
+    return {n: t.double().cpu() for n, t in
+            (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def oracle_b(wl, f):
+    out, lse = O.attention_forward(f["q"], f["k"], f["v"], wl.scale, wl.theta, wl.causal,
+                                   round_rotated=True)
+    dq, dk, dv = O.attention_backward(f["q"], f["k"], f["v"], f["dout"], wl.scale, wl.theta,
+                                      wl.causal, round_rotated=True)
+    return {"out": out, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+def score_std(wl, f):
+    ang = O.rope_angles(wl.S, wl.D, wl.theta)
+    qr = O.round_to_bf16(O.rope_half_split(f["q"], ang))
+    kr = O.round_to_bf16(O.rope_half_split(f["k"], ang))
+    G = wl.Hq // wl.Hkv
+    return (wl.scale * qr[0, 0] @ kr[0, 0 // G].T).std().item()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,sigma", [
+    (1, 4, 1, 512, 64, 3.0),
+    (1, 4, 1, 512, 64, 6.0),
+    (1, 8, 2, 384, 128, 3.0),
+    (1, 4, 2, 384, 128, 6.0),
+])
+def test_peaked_softmax(B, Hq, Hkv, S, D, sigma):
+    """q and k drawn N(0, sigma^2): score standard deviation sigma^2 (9 or 36), rows
+    dominated by one or a few keys."""
+    wl = Workload(400 + int(sigma) + D, "peaked", B, Hq, Hkv, S, D,
+                  10000.0 if D == 64 else 500000.0, True)
+    dev, f = gen_scaled(wl, {"q": [(sigma, None)], "k": [(sigma, None)]})
+    assert score_std(wl, f) > 0.8 * sigma ** 2
+    g = run_exact(wl, dev)
+    want = oracle_b(wl, f)
+    for n in ("out", "dq", "dk", "dv"):
+        assert_close(n, g[n], want[n])
+    assert_close("lse", g["lse"], want["lse"], LSE_ABS, LSE_ABS)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,key", [
+    (1, 4, 1, 512, 64, 400),
+    (1, 4, 2, 512, 128, 450),
+])
+def test_late_row_maximum_jump(B, Hq, Hkv, S, D, key):
+    """One key late in the sequence multiplied by 16: for the rows after it the row
+    maximum jumps, in the last key tile, by more than 2^8 in base 2 over the maximum
+    of every earlier tile, so the forward's lazy rescale must rescale O and the row
+    sum there."""
+    wl = Workload(420 + D, "late", B, Hq, Hkv, S, D, 10000.0 if D == 64 else 500000.0, True)
+    dev, f = gen_scaled(wl, {"k": [(16.0, (slice(None), slice(None), key))]})
+    # the jump happens for some row of head 0: score of the large key against the
+    # maximum over the key tiles before its own, in base-2 units
+    ang = O.rope_angles(S, D, wl.theta)
+    qr = O.round_to_bf16(O.rope_half_split(f["q"], ang))[0, 0]
+    kr = O.round_to_bf16(O.rope_half_split(f["k"], ang))[0, 0]
+    s = wl.scale * qr[key:] @ kr.T
+    before = s[:, :key // 128 * 128].max(dim=1).values
+    jump = (s[:, key] - before) / math.log(2.0)
+    assert jump.max().item() > 8.0, jump.max().item()
+    g = run_exact(wl, dev)
+    want = oracle_b(wl, f)
+    for n in ("out", "dq", "dk", "dv"):
+        assert_close(n, g[n], want[n])
+    assert_close("lse", g["lse"], want["lse"], LSE_ABS, LSE_ABS)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D", [(1, 4, 1, 512, 64), (1, 4, 2, 384, 128)])
+def test_fp16_scale_outliers(B, Hq, Hkv, S, D):
+    """One element of q and one of dout multiplied by 2^12: the backward's per-tensor
+    power-of-two fp16 scales follow the outliers, which pushes every other element of
+    those tensors 2^12 closer to fp16's subnormal range. Everything outside the
+    outliers' reach keeps the stated bounds. What an outlier feeds grows by up to
+    ~2^12 and is held to the stated bound plus the fp16 rounding of its own magnitude
+    (2^-10 of the largest element there): for the dout outlier, dv's column 7 and dq's row and, through that
+    row's dS, the dk rows of every key the row sees; for the q outlier, dq's row and
+    dk's two columns of its rotation pair over the keys its row sees."""
+    wl = Workload(440 + D, "outlier", B, Hq, Hkv, S, D, 10000.0 if D == 64 else 500000.0, True)
+    iq, ido = S // 3, S // 2
+    dev, f = gen_scaled(wl, {"q": [(4096.0, (0, 0, iq, 5))],
+                             "dout": [(4096.0, (0, 0, ido, 7))]})
+    g = run_exact(wl, dev)
+    want = oracle_b(wl, f)
+    assert_close("out", g["out"], want["out"])
+    assert_close("lse", g["lse"], want["lse"], LSE_ABS, LSE_ABS)
+
+    def mask(shape, *idx):
+        m = torch.zeros(shape, dtype=torch.bool)
+        for i in idx:
+            m[i] = True
+        return m
+
+    qpair = [5, 5 + D // 2]  # the dimensions the q outlier's rotation pair spans
+    dk_q = mask(want["dk"].shape, (0, 0, slice(0, iq + 1), qpair))
+    dk_do = mask(want["dk"].shape, (0, 0, slice(0, ido + 1))) & ~dk_q
+    reach = {
+        # dout outlier: column 7 of dv for the keys its row sees, dq's row, and through
+        # that row's dS every dk row it sees; q outlier: dq's row, and dk's rotation pair
+        "dv": [mask(want["dv"].shape, (0, 0, slice(0, ido + 1), 7))],
+        "dq": [mask(want["dq"].shape, (0, 0, iq)), mask(want["dq"].shape, (0, 0, ido))],
+        "dk": [dk_q, dk_do],
+    }
+    for n, masks in reach.items():
+        rest = torch.ones_like(want[n], dtype=torch.bool)
+        for m in masks:
+            e = (g[n] - want[n]).abs()[m].max().item()
+            bound = MAX_ABS + 2.0 ** -10 * want[n][m].abs().max().item()
+            assert e <= bound, f"{n} in an outlier's reach: max-abs {e:.3e} > {bound:.3e}"
+            rest &= ~m
+        e = (g[n] - want[n]).abs()[rest]
+        assert e.max().item() <= MAX_ABS and e.mean().item() <= MEAN_ABS, \
+            f"{n} outside the outliers' reach: {e.max().item():.3e} / {e.mean().item():.3e}"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D", [
+    (1, 32, 1, 256, 128),
+    (1, 48, 1, 256, 64),
+    (1, 48, 1, 384, 128),
+    (2, 48, 2, 512, 128),
+])
+def test_large_query_groups(B, Hq, Hkv, S, D):
+    """Many query heads over one K/V head (multi-query, "ColossalAI 中的 PaLM 教学实现…",
+    §2.5; its large presets have 32-48 heads): dk and dv sum all G heads' terms. The
+    default backward (attn_bwd) is held to the stated bounds, no factor of G."""
+    wl = Workload(460 + Hq + D, "groups", B, Hq, Hkv, S, D, 10000.0 if D == 64 else 500000.0,
+                  True)
+    dev, f = gen(wl)
+    g = run_gpu(wl, dev)
+    check_all(wl, g, f)
+
+
+def test_delta_modes_agree_on_diffuse_rows():
+    """On N(0, 1) inputs the exact delta pass and delta from `out` differ only by the
+    rounding of out: both meet the bounds, and they are not bit-identical (the flag is
+    honoured)."""
+    wl = Workload(480, "delta", 1, 8, 2, 512, 128, 500000.0, True)
+    dev, f = gen(wl)
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+    ge = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                    wl.causal, delta="exact")
+    go = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta, wl.scale,
+                    wl.causal, delta="from_out")
+    torch.cuda.synchronize()
+    assert M.sync_status() == 0
+    want = oracle_b(wl, f)
+    for res in (ge, go):
+        for n, t in zip(("dq", "dk", "dv"), res):
+            assert_close(n, t.double().cpu(), want[n])
+    assert not torch.equal(ge[1], go[1])
+    # dv does not depend on delta: identical
+    assert torch.equal(ge[2], go[2])
+
+
+@pytest.mark.parametrize("D,rope,theta,pos0,factor", [
+    (64, "half", 10000.0, 0, 1.0),
+    (128, "half", 500000.0, 0, 6.0),
+    (128, "interleaved", 500000.0, 28672, 1.0),
+    (64, "interleaved", 10000.0, 0, 3.0),
+])
+def test_rope_is_the_rounded_exact_rotation(D, rope, theta, pos0, factor):
+    """attn_rope (the rotation every kernel applies to q and k before the score
+    product) returns, element for element, the bf16 value nearest the fp64 rotation:
+    the oracle's RoPE ("Picotron模型实现解析Llama架构与Flash Attention集成", §1;
+    "深度学习系统设计llama3-from-scratch：并行计算架构", §RoPE) rounded to bf16 (nearest
+    even). 16 heads x 4096 positions, about 2-4 million elements, thousands of them
+    within an fp32 rounding of a bf16 midpoint."""
+    heads, S = 16, 4096
+    bits = I.normal_bf16_bits(9000 + D + pos0 % 97, (heads, S, D))
+    if factor != 1.0:
+        bits = I.scale_bf16_bits(bits, factor)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    y = M.rope(x, theta, pos0=pos0, rope=rope)
+    torch.cuda.synchronize()
+    f = torch.from_numpy(I.bf16_bits_to_f64(bits))
+    ang = O.rope_angles(S, D, theta, pos0)
+    rot = O.rope_half_split(f, ang) if rope == "half" else O.rope_interleaved(f, ang)
+    want = O.round_to_bf16(rot)
+    got = y.double().cpu()
+    bad = (got != want)
+    assert bad.sum().item() == 0, f"{bad.sum().item()} of {bad.numel()} elements differ"
