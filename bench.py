@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--decode", type=int, default=0, metavar="SQ",
                     help="SQ > 0: time attn_decode, SQ new tokens per sequence against a "
                          "cache of the workload's S keys (HBM-bound: reported in GB/s)")
+    ap.add_argument("--single", action="store_true",
+                    help="time only --workload (by default the other workloads follow the "
+                         "headline under other_workloads)")
     ap.add_argument("--blocks", type=int, default=1,
                     help="N > 1: run the step as N x N query / key-value blocks through "
                          "attn_fwd_partial, attn_merge and attn_bwd_partial")
@@ -228,6 +231,48 @@ def oracle_sample_heads(wl, host, budget_s=10.0):
     return done * per_head / dt / 1e12, done, dt
 
 
+def oracle_sample_rows(wl, host, rows_per_head=64, budget_s=5.0):
+    """fp64 oracle out, lse and dq of `rows_per_head` seeded query rows of successive
+    heads (for sequences too long for whole heads), until `budget_s` is spent.
+    Credited 10*D FLOPs per causal pair of those rows (the reference arm's unit).
+    Returns (TFLOP/s, heads, s)."""
+    import oracle as O
+
+    f = {n: torch.from_numpy(I.bf16_bits_to_f64(host[n])) for n in host}
+    G = wl.Hq // wl.Hkv
+    rng = np.random.default_rng(4321)
+    t0 = time.perf_counter()
+    flops, done = 0, 0
+    while time.perf_counter() - t0 < budget_s and done < wl.B * wl.Hq:
+        b, h = divmod(done, wl.Hq)
+        rows = torch.from_numpy(np.sort(rng.choice(wl.S, size=rows_per_head, replace=False)))
+        q = f["q"][b:b + 1, h:h + 1]
+        k, v = f["k"][b:b + 1, h // G:h // G + 1], f["v"][b:b + 1, h // G:h // G + 1]
+        O.forward_rows(q, k, v, rows, wl.scale, wl.theta, wl.causal)
+        O.backward_dq_rows(q, k, v, f["dout"][b:b + 1, h:h + 1], rows, wl.scale, wl.theta,
+                           wl.causal)
+        flops += 10 * wl.D * (int((rows + 1).sum()) if wl.causal else rows_per_head * wl.S)
+        done += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, done, dt
+
+
+def cpu_baseline_of(wl, host, budget_s):
+    """The oracle on this host: whole heads (fwd(+bwd)) where a head takes at most a few
+    seconds, sampled rows otherwise."""
+    threads = torch.get_num_threads()
+    if wl.S <= 8192:
+        tf, heads, secs = oracle_sample_heads(wl, host, budget_s)
+        sample = (f"{heads} of {wl.B * wl.Hq} query heads, full S={wl.S}, "
+                  f"fwd{'+bwd' if wl.backward else ''} in fp64 ({secs:.1f} s)")
+    else:
+        tf, heads, secs = oracle_sample_rows(wl, host, budget_s=budget_s)
+        sample = (f"64 seeded query rows of each of {heads} heads (out, lse, dq in fp64), "
+                  f"{secs:.1f} s")
+    return {"value": tf, "unit": "TFLOP/s", "cores": threads, "host_cores": os.cpu_count(),
+            "kind": "oracle", "sample": sample}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     """The fp64 oracle timed as the reference arm (rank 0 only). Each step: the
@@ -270,9 +315,9 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic N(0,1) bf16 inputs, seeded",
-        "config": config_of(wl, args.gpus, l2="n/a (host)"),
+        "config": config_of(wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": unit, "cores": torch.get_num_threads(),
-                         "kind": "oracle",
+                         "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"per step {R} query rows of one head (out, lse, dq)"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -293,7 +338,11 @@ def bwd_prologue_bytes(wl):
     return absmax + reads + writes
 
 
-def config_of(wl, n, l2, rope="half", grads="fp32"):
+L2_NOTE = ("GPU arm: L2 flushed between steps (256 MiB write); the host oracle arm has no "
+           "device cache")
+
+
+def config_of(wl, n, rope="half", grads="fp32", l2=L2_NOTE):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
             "rope_theta": wl.theta, "rope": rope, "grads": grads, "causal": wl.causal,
             "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
@@ -301,6 +350,104 @@ def config_of(wl, n, l2, rope="half", grads="fp32"):
 
 
 # ------------------------------------------------------------------ our arm
+def kernel_names(M):
+    return ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"), (M.KERNEL_BWD_PREP, "bwd_prep"),
+            (M.KERNEL_DELTA, "delta"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
+            (M.KERNEL_DQ_FINAL, "dq_finalize"))
+
+
+def launches_per_step(wl):
+    """Our kernels in one step: RoPE pre-pass + forward; abs-max + pre-pass (+ the exact
+    delta pass for groups above 8) + main + dq finalisation."""
+    if not wl.backward:
+        return 2
+    return 2 + 4 + (1 if wl.Hq // wl.Hkv > 8 else 0)
+
+
+def roofline_of(wl, kern, peak_tf, peak_src, value):
+    dom = max(kern.items(), key=lambda kv: kv[1]["avg_ms"])
+    algo_flops = {"attn_fwd": wl.fwd_flops, "attn_bwd_main": wl.bwd_flops}
+    if dom[0] not in algo_flops:
+        return None
+    achieved = algo_flops[dom[0]] / (dom[1]["avg_ms"] * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak_tf,
+            "unit": "TFLOP/s", "frac": achieved / peak_tf,
+            "traffic": ncu_traffic(dom[0], wl.name),
+            "peak_source": f"{peak_src} bf16 dense (burst)",
+            "step_frac_of_peak": value / peak_tf}
+
+
+def time_workload(M, wl, steps, warmup, flush, stream):
+    """Device time of `steps` fwd(+bwd) steps of `wl` (inputs resident, L2 flushed between
+    steps, CUDA events on the launching stream) and the per-kernel times of a second run
+    of the same steps. Returns (ms per step, {kernel: {launches, avg_ms}})."""
+    host = host_inputs(wl, 0)
+    dev = {n: to_bf16_tensor(h, "cuda") for n, h in host.items()}
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["dout"]
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, wl.S), dtype=torch.float32, device="cuda")
+    dq = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(k.shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+    dims = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, wl.scale, wl.causal)
+
+    def step():
+        M.attn_fwd(q, k, v, out, lse, *dims, stream=stream)
+        if wl.backward:
+            M.attn_bwd(q, k, v, out, lse, do, dq, dk, dv, *dims, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if M.sync_status() != 0:
+        raise SystemExit(f"device status error during warm-up ({wl.name})")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    M.profile_begin(max(4096, 2 * steps))
+    for i in range(steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    M.profile_end()
+    kern = {}
+    for kind, name in kernel_names(M):
+        n, tot = M.profile_query(kind)
+        if n:
+            kern[name] = {"launches": n, "avg_ms": tot / n}
+    if M.sync_status() != 0:
+        raise SystemExit(f"device status error ({wl.name})")
+    return ms, kern
+
+
+def other_workload_lines(args, M, flush, stream, peak_tf, peak_src):
+    """The other benchmark workloads (their shapes are in the workloads module), each
+    with its own step time, per-kernel times, roofline fraction and oracle baseline."""
+    lines = []
+    for wl in WORKLOADS:
+        if wl.name == args.workload:
+            continue
+        steps = max(3, min(args.steps, 10 if wl.S > 8192 else 20))
+        ms, kern = time_workload(M, wl, steps, max(3, args.warmup), flush, stream)
+        value = wl.flops / (ms * 1e-3) / 1e12
+        entry = {"workload": wl.name, "config": config_of(wl, 1), "value": value,
+                 "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+                 "kernels_ms": {n: round(d["avg_ms"], 5) for n, d in kern.items()},
+                 "gpu_launches": launches_per_step(wl) * steps,
+                 "roofline": roofline_of(wl, kern, peak_tf, peak_src, value),
+                 "cpu_baseline": None}
+        if not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline_of(wl, host_inputs(wl, 0), 4.0)
+        lines.append(entry)
+    return lines
+
+
 def run_ours(args, rank, world, local):
     import mqa_attention_gb300 as M
     from mqa_attention_gb300 import build as B
@@ -381,14 +528,10 @@ def run_ours(args, rank, world, local):
     M.profile_end()
     status = M.sync_status()
     kern = {}
-    for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
-                       (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
-                       (M.KERNEL_DQ_FINAL, "dq_finalize")):
+    for kind, name in kernel_names(M):
         n, tot = M.profile_query(kind)
         if n:
             kern[name] = {"launches": n, "avg_ms": tot / n}
-    # our kernels per step: RoPE pre-pass + forward; abs-max + pre-pass + main + dq finalisation
-    launches_per_step = 2 + (4 if wl.backward else 0)
 
     # ---- end to end through host buffers
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
@@ -464,16 +607,7 @@ def run_ours(args, rank, world, local):
     total_flops = wl.flops * world
     value = total_flops / (ms * 1e-3) / 1e12
     # dominant kernel: the one with the largest share of the step
-    dom = max(kern.items(), key=lambda kv: kv[1]["avg_ms"])
-    algo_flops = {"attn_fwd": wl.fwd_flops, "attn_bwd_main": wl.bwd_flops}
-    roof = None
-    if dom[0] in algo_flops:
-        achieved = algo_flops[dom[0]] / (dom[1]["avg_ms"] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                "traffic": ncu_traffic(dom[0], wl.name),
-                "peak_source": f"{peak_src} bf16 dense (burst)",
-                "step_frac_of_peak": value / world / peak_tf}
+    roof = roofline_of(wl, kern, peak_tf, peak_src, value / world)
     # the backward prologue (abs-max pass + row pass) is HBM-bound: its algorithmic bytes
     # against the measured copy bandwidth
     prologue = None
@@ -489,28 +623,27 @@ def run_ours(args, rank, world, local):
     if "attn_fwd" in kern:
         passes["fwd"] = kern["attn_fwd"]["avg_ms"] + kern.get("rope", {"avg_ms": 0.0})["avg_ms"]
     if "attn_bwd_main" in kern:
-        passes["bwd"] = sum(kern[k]["avg_ms"] for k in ("bwd_prep", "attn_bwd_main", "dq_finalize")
-                            if k in kern)
+        passes["bwd"] = sum(kern[k]["avg_ms"] for k in ("bwd_prep", "delta", "attn_bwd_main",
+                                                        "dq_finalize") if k in kern)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        tf, heads, secs = oracle_sample_heads(wl, host)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
-               "sample": f"{heads} of {wl.B * wl.Hq} query heads, full S={wl.S}, "
-                         f"fwd{'+bwd' if wl.backward else ''} in fp64 ({secs:.1f} s)"}
+        cpu = cpu_baseline_of(wl, host, 10.0)
+    others = None
+    if world == 1 and args.rope == "half" and args.grads == "fp32" and not args.single:
+        others = other_workload_lines(args, M, flush, stream, peak_tf, peak_src)
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
-        "config": config_of(wl, world, l2="flushed between steps (256 MiB write)", rope=args.rope,
-                            grads=args.grads),
+        "config": config_of(wl, world, rope=args.rope, grads=args.grads),
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers; each step's inputs in and results out on two "
                           "copy streams over three device buffer sets, overlapped with "
                           "the neighbouring steps' compute"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step(wl) * args.steps,
         "roofline": roof,
         "prologue_roofline": prologue,
         "passes_ms": {k: round(v, 5) for k, v in passes.items()},
@@ -518,6 +651,7 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": cpu,
         "clocks": clocks,
         "device_status": status,
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -627,8 +761,7 @@ def run_blocks(args, rank, world, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
-        "config": dict(config_of(wl, world, l2="flushed between steps (256 MiB write)",
-                                 rope=args.rope), blocks=f"{nb} x {nb}", block_rows=blk,
+        "config": dict(config_of(wl, world, rope=args.rope), blocks=f"{nb} x {nb}", block_rows=blk,
                        block_pairs=len(pairs)),
         "e2e": None,
         "note": "block schedule through the partial entry points; device time only",
@@ -754,8 +887,9 @@ def run_decode(args, rank, world, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v, seeded (splitmix64 + Box-Muller)",
-        "config": dict(config_of(wl, world, l2=f"each call reads its own cache copy ({ncopy} "
-                                                   "copies, >= 256 MiB)", rope=args.rope),
+        "config": dict(config_of(wl, world, rope=args.rope,
+                                 l2=f"each call reads its own cache copy ({ncopy} copies, "
+                                    ">= 256 MiB)"),
                        passes="decode fwd", new_tokens=sq, bytes_per_step=moved),
         "e2e": {"value": moved * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": q.numel() * 2,
