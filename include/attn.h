@@ -29,8 +29,8 @@
  *   Heads    query head h reads K/V head h / (Hq / Hkv) (contiguous groups).
  *   RoPE     half-split: for i < D/2, angle = p * theta^(-2i/D) at position p = 0..S-1;
  *            y_i = x_i cos - x_{i+D/2} sin, y_{i+D/2} = x_{i+D/2} cos + x_i sin.
- *            The rotated q and k are rounded to bf16 before the score product: to the
- *            bf16 value nearest the exact rotation (cos/sin evaluated in fp64).
+ *            The rotated q and k are rounded to bf16 before the score product (see
+ *            ATTN_ROPE_EXACT for how).
  *   Sizes    D in {64, 128}; S > 0 (the kernels work in 128-row tiles: for an S that is
  *            not a multiple of 128 they run on copies padded to whole tiles, with the
  *            padding rows contributing nothing, and copy the valid rows out, at the
@@ -48,11 +48,13 @@
  *            from the pool, no host synchronisation; a call on another stream waits
  *            for the build on the device. At most 8 (D, rope_theta) tables are kept per
  *            device (least recently used dropped first); a dropped table is freed in
- *            stream order after every use recorded for it, except a table read under
- *            stream capture, which stays allocated (a graph may still read it). A call
- *            that needs a table built while `stream` is capturing returns
- *            ATTN_ERR_UNSUPPORTED: make the first call for a (D, rope_theta, length)
- *            outside capture.
+ *            stream order on the stream that drops it when only that stream read it,
+ *            and otherwise (read by other streams, or under stream capture, where a
+ *            graph may still read it) stays allocated until the process exits. A call
+ *            under stream capture needs its table built and already seen complete by
+ *            an earlier call outside capture (else ATTN_ERR_UNSUPPORTED): run a call
+ *            for the same (D, rope_theta) and length, and one more after it has
+ *            finished, before capturing (the usual warm-up does both).
  *   Device   the current CUDA device must be an sm_103 GPU (GB300).
  *   Errors   every entry point returns ATTN_OK (0) or one of the codes below and writes
  *            nothing when it rejects its arguments. Device-side failures of a launched
@@ -123,6 +125,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
  *                         (llama3-from-scratch §RoPE). */
 enum { ATTN_ROPE_HALF = 0, ATTN_ROPE_INTERLEAVED = 1 };
 
+/* Rounding of the rotated q and k, OR-ed into the rope_mode argument of any entry point
+ * that takes one. By default the rotation runs in fp32 (the table's cosines and sines
+ * rounded to fp32) and is rounded once to bf16; in about 1 element of 40,000 that bf16
+ * value differs from the value nearest the exact rotation, by one ulp or (where the
+ * rotation cancels to far below its inputs) by up to 2^-22 (|x_i| + |x_(i+D/2)|). With
+ * ATTN_ROPE_EXACT every rotated element is the bf16 value nearest the exact rotation
+ * (cos/sin in fp64; evaluated with error-free products and sums, slower pre-passes).
+ * A backward call must use the same rounding as the forward call whose out and lse it
+ * receives (its recomputed scores are then the forward's). */
+enum { ATTN_ROPE_EXACT = 0x10 };
+
 /* Delta flags, OR-ed into the rope_mode argument of attn_bwd_ex and attn_bwd_bf16 (not
  * attn_bwd_partial, whose out is the merged result of every K/V block):
  *   ATTN_DELTA_EXACT     always form delta_i = sum_j P_ij dP_ij with the extra pass:
@@ -134,9 +147,9 @@ enum { ATTN_ROPE_HALF = 0, ATTN_ROPE_INTERLEAVED = 1 };
 enum { ATTN_DELTA_EXACT = 0x100, ATTN_DELTA_FROM_OUT = 0x200 };
 
 /* attn_fwd / attn_bwd with the RoPE pair layout chosen by rope_mode (one of the
- * ATTN_ROPE_* values, for attn_bwd_ex optionally OR-ed with one ATTN_DELTA_* flag;
- * anything else returns ATTN_ERR_INVALID). Arguments, layouts, ownership and errors are
- * otherwise those of attn_fwd / attn_bwd; attn_fwd(...) is
+ * ATTN_ROPE_* layouts, optionally OR-ed with ATTN_ROPE_EXACT, and for attn_bwd_ex with one
+ * ATTN_DELTA_* flag; anything else returns ATTN_ERR_INVALID). Arguments, layouts,
+ * ownership and errors are otherwise those of attn_fwd / attn_bwd; attn_fwd(...) is
  * attn_fwd_ex(..., rope_theta, ATTN_ROPE_HALF, scale, ...). */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                 int Hq, int Hkv, int S, int D, float rope_theta, int rope_mode, float scale,

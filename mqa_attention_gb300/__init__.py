@@ -51,6 +51,7 @@ __all__ = [
     "KERNEL_DQ_FINAL",
     "KERNEL_DELTA",
     "DELTA_MODES",
+    "ROPE_EXACT",
 ]
 
 LIB_NAME = "libmqa_attention_gb300.so"
@@ -60,6 +61,7 @@ ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT
 KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL, KERNEL_DELTA = range(6)
 # delta flags OR-ed into the rope_mode of attn_bwd_ex / attn_bwd_bf16 (ATTN_DELTA_*)
 DELTA_MODES = {"auto": 0, "exact": 0x100, "from_out": 0x200}
+ROPE_EXACT = 0x10  # ATTN_ROPE_EXACT: rotated q, k rounded as the exact rotation rounds
 
 EXPORTED_SYMBOLS = (
     "attn_fwd",
@@ -278,13 +280,15 @@ def attn_decode(q, k_rot, v, out, lse, B, Hq, Hkv, Sq, Skv, D, q_pos0, rope_thet
            "attn_decode")
 
 
-def rope(x, rope_theta, pos0=0, out=None, stream=None, rope="half"):
-    """bf16 RoPE(x) of x [..., S, D] (rows at positions pos0..pos0+S-1)."""
+def rope(x, rope_theta, pos0=0, out=None, stream=None, rope="half", exact=False):
+    """bf16 RoPE(x) of x [..., S, D] (rows at positions pos0..pos0+S-1); exact=True
+    rounds as the exact rotation rounds (ATTN_ROPE_EXACT)."""
     import torch
 
     S, D = x.shape[-2], x.shape[-1]
     y = torch.empty_like(x) if out is None else out
-    attn_rope(x, y, x.numel() // (S * D), S, pos0, D, rope_theta, ROPE_MODES[rope], stream)
+    attn_rope(x, y, x.numel() // (S * D), S, pos0, D, rope_theta,
+              ROPE_MODES[rope] | (ROPE_EXACT if exact else 0), stream)
     return y
 
 
@@ -353,29 +357,30 @@ def _shapes(q, k):
     return B, Hq, Hkv, S, D
 
 
-def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None, rope="half"):
-    """Allocates out / lse like q and runs attn_fwd (attn_fwd_ex for rope="interleaved").
-    q: [B,Hq,S,D], k, v: [B,Hkv,S,D]."""
+def forward(q, k, v, rope_theta, scale=None, causal=True, stream=None, rope="half",
+            exact_rope=False):
+    """Allocates out / lse like q and runs attn_fwd (attn_fwd_ex for rope="interleaved" or
+    exact_rope=True, ATTN_ROPE_EXACT). q: [B,Hq,S,D], k, v: [B,Hkv,S,D]."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    if rope == "half":
+    mode = ROPE_MODES[rope] | (ROPE_EXACT if exact_rope else 0)
+    if mode == 0:
         attn_fwd(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, scale, causal, stream)
     else:
-        attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, ROPE_MODES[rope], scale,
-                    causal, stream)
+        attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, rope_theta, mode, scale, causal, stream)
     return out, lse
 
 
 def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, stream=None,
-             rope="half", grad_dtype=None, delta="auto"):
+             rope="half", grad_dtype=None, delta="auto", exact_rope=False):
     """Allocates dq, dk, dv and runs attn_bwd (attn_bwd_ex for rope="interleaved" or a
     delta mode other than "auto", attn_bwd_bf16 for grad_dtype=torch.bfloat16; fp32
     gradients otherwise). delta: "auto" (attn_bwd's choice), "exact" (the extra pass over
-    the scores) or "from_out" (dout . out)."""
+    the scores) or "from_out" (dout . out). exact_rope: as the forward call's."""
     import torch
 
     B, Hq, Hkv, S, D = _shapes(q, k)
@@ -384,7 +389,7 @@ def backward(q, k, v, out, lse, dout, rope_theta, scale=None, causal=True, strea
     dq = torch.empty(q.shape, dtype=gd, device=q.device)
     dk = torch.empty(k.shape, dtype=gd, device=q.device)
     dv = torch.empty(v.shape, dtype=gd, device=q.device)
-    mode = ROPE_MODES[rope] | DELTA_MODES[delta]
+    mode = ROPE_MODES[rope] | DELTA_MODES[delta] | (ROPE_EXACT if exact_rope else 0)
     if gd == torch.bfloat16:
         attn_bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, rope_theta, mode,
                       scale, causal, stream)

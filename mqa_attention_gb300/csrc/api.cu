@@ -32,9 +32,12 @@ struct RopeTable {
   int npos = 0;
   long long n = 0;
   cudaEvent_t ready = nullptr;  // recorded after the build
-  // The last use by each stream that read the table outside stream capture: a retired
-  // table is freed once all of them have completed.
-  std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;
+  bool known_ready = false;     // the build was seen complete (no wait needed any more)
+  // Streams that read the table outside stream capture (at most kRopeStreams tracked;
+  // many_streams beyond that). A retired table is freed in stream order on the stream
+  // that retires it only when that stream is the only one that read it.
+  std::vector<cudaStream_t> uses;
+  bool many_streams = false;
   bool pinned = false;   // read under stream capture: a graph may hold its address
   bool retired = false;  // replaced or evicted: freed when the last holder releases it
   int active = 0;        // calls between rope_acquire and rope_release
@@ -55,8 +58,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// RoPE tables kept per device (distinct (D, theta) pairs), and streams whose last use
-// of one table is tracked separately.
+// RoPE tables kept per device (distinct (D, theta) pairs), and streams tracked per table.
 constexpr int kRopeKeys = 8;
 constexpr int kRopeStreams = 8;
 bool g_inject_timeout = false;
@@ -174,6 +176,15 @@ int validate(const void* const* ptrs, int nptr, int B, int Hq, int Hkv, int S, i
 
 int round_tile(int S) { return (S + kTile - 1) / kTile * kTile; }
 
+// rope_mode of an entry point: one ATTN_ROPE_* layout, optionally with ATTN_ROPE_EXACT,
+// plus the flags in `allowed`. Returns false for anything else.
+bool parse_rope_mode(int rope_mode, int allowed, int* layout, bool* exact) {
+  *layout = rope_mode & 0xf;
+  *exact = (rope_mode & ATTN_ROPE_EXACT) != 0;
+  if (*layout != ATTN_ROPE_HALF && *layout != ATTN_ROPE_INTERLEAVED) return false;
+  return (rope_mode & ~(0xf | ATTN_ROPE_EXACT | allowed)) == 0;
+}
+
 // Query / K-V block arguments of the partial entry points: Sq, Skv multiples of
 // 128 (checked with the other sizes by validate), positions non-negative
 // multiples of 128, the last position below 2^30.
@@ -256,13 +267,16 @@ bool stream_capturing(cudaStream_t stream) {
   return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
 }
 
-// Releases a retired table's memory in stream order on `stream` (alive and not capturing):
-// after every recorded use. A table read under capture stays allocated (a graph may
-// still read it). Caller holds g_mu.
+// Releases a retired table in stream order on `stream` (alive and not capturing) when
+// every read of it was enqueued on `stream`: the free then follows them. A table read
+// by another stream, or under stream capture (a graph may still read it), stays
+// allocated until the process exits; recording an event after every call to order a
+// free after other streams' reads would cost each call its overlap with the next
+// kernel (an event between two launches holds back the second's early start).
 void rope_free_locked(RopeTable& t, cudaStream_t stream) {
-  for (auto& u : t.uses) cudaStreamWaitEvent(stream, u.second, 0);
-  if (!t.pinned && t.buf) cudaFreeAsync(t.buf, stream);
-  for (auto& u : t.uses) cudaEventDestroy(u.second);
+  bool only_here = !t.pinned && !t.many_streams;
+  for (cudaStream_t u : t.uses) only_here = only_here && u == stream;
+  if (only_here && t.buf) cudaFreeAsync(t.buf, stream);
   if (t.ready) cudaEventDestroy(t.ready);
   t.uses.clear();
   t.ready = nullptr;
@@ -291,7 +305,8 @@ struct RopeUse {
 // least doubling its length); at most kRopeKeys (D, theta) pairs are kept, the least
 // recently used evicted first. A build cannot be recorded into a stream capture
 // (ATTN_ERR_UNSUPPORTED): the first call for a (D, theta), or for a longer sequence than
-// before, belongs outside capture. Pair with rope_release after the call's launches.
+// before, belongs outside capture, and so does one more call after the build has
+// completed. Pair with rope_release after the call's launches.
 int rope_acquire(DeviceState* d, int npos, int D, float theta, cudaStream_t stream,
                  bool capturing, RopeUse* out) {
   uint32_t tb;
@@ -335,9 +350,13 @@ int rope_acquire(DeviceState* d, int npos, int D, float theta, cudaStream_t stre
     }
     d->rope[key] = nt;
     t = nt;
-  } else if (cudaEventQuery(t->ready) != cudaSuccess) {
-    // built by another call whose stream may not have finished the build yet
-    if (cudaStreamWaitEvent(stream, t->ready, 0) != cudaSuccess) return ATTN_ERR_CUDA;
+  } else if (!t->known_ready) {
+    // Built by a call whose stream may not have finished the build yet. Outside
+    // capture this stream waits for it on the device; a capture cannot take that
+    // dependency, so the build must already have been seen complete by an earlier call.
+    if (capturing) return ATTN_ERR_UNSUPPORTED;
+    if (cudaEventQuery(t->ready) == cudaSuccess) t->known_ready = true;
+    else if (cudaStreamWaitEvent(stream, t->ready, 0) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   t->active += 1;
   t->tick = ++d->tick;
@@ -351,32 +370,20 @@ int rope_acquire(DeviceState* d, int npos, int D, float theta, cudaStream_t stre
   return ATTN_OK;
 }
 
-// Ends a call's use of its table: records the stream's last use (outside capture) and
+// Ends a call's use of its table: notes the stream that read it (outside capture) and
 // frees the table if it was retired meanwhile and nothing else holds it.
 void rope_release(DeviceState* d, RopeUse& u, cudaStream_t stream, bool capturing) {
   if (!u.t) return;
   std::lock_guard<std::mutex> lk(g_mu);
   RopeTable& t = *u.t;
   t.active -= 1;
-  if (!capturing) {
-    cudaEvent_t ev = nullptr;
-    for (auto& su : t.uses)
-      if (su.first == stream) ev = su.second;
-    if (!ev) {
-      if (static_cast<int>(t.uses.size()) >= kRopeStreams) {
-        // too many streams to track one by one: this stream takes over their uses
-        for (auto& su : t.uses) {
-          cudaStreamWaitEvent(stream, su.second, 0);
-          cudaEventDestroy(su.second);
-        }
-        t.uses.clear();
-      }
-      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess)
-        t.uses.emplace_back(stream, ev);
-      else
-        ev = nullptr;
+  if (!capturing && !t.many_streams) {
+    bool seen = false;
+    for (cudaStream_t s : t.uses) seen = seen || s == stream;
+    if (!seen) {
+      if (static_cast<int>(t.uses.size()) >= kRopeStreams) t.many_streams = true;
+      else t.uses.push_back(stream);
     }
-    if (ev) cudaEventRecord(ev, stream);
   }
   if (t.retired && t.active == 0) {
     if (capturing) d->to_free.push_back(u.t);
@@ -431,7 +438,9 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
   int st = validate(ptrs, 5, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
   if (!ragged && (st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
-  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  int layout = 0;
+  bool exact_rope = false;
+  if (!parse_rope_mode(rope_mode, 0, &layout, &exact_rope)) return ATTN_ERR_INVALID;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != ATTN_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -468,8 +477,10 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
   bool ok = true;
   {
     gbattn::RowPrepParams rp{};
+    rp.status = d->status;
     rp.bwd = 0;
-    rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
+    rp.rope_interleaved = layout == ATTN_ROPE_INTERLEAVED;
+    rp.exact = exact_rope ? 1 : 0;
     rp.D = D;
     rp.cos_tab = rope.u.ch;
     rp.sin_tab = rope.u.sh;
@@ -637,12 +648,14 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   int st = validate(ptrs, 9, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
   if (!ragged && (st = validate_blocks(Sq, Skv, q_pos0, kv_pos0)) != ATTN_OK) return st;
-  // rope_mode: the RoPE pair layout, optionally with one delta flag (self-attention only)
-  const int layout = rope_mode & 0xff;
-  const int dflags = rope_mode & ~0xff;
-  if (layout != ATTN_ROPE_HALF && layout != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
-  if (dflags != 0 && dflags != ATTN_DELTA_EXACT && dflags != ATTN_DELTA_FROM_OUT)
+  // rope_mode: the RoPE pair layout and rounding, optionally with one delta flag
+  // (self-attention only)
+  int layout = 0;
+  bool exact_rope = false;
+  if (!parse_rope_mode(rope_mode, ATTN_DELTA_EXACT | ATTN_DELTA_FROM_OUT, &layout, &exact_rope))
     return ATTN_ERR_INVALID;
+  const int dflags = rope_mode & (ATTN_DELTA_EXACT | ATTN_DELTA_FROM_OUT);
+  if (dflags == (ATTN_DELTA_EXACT | ATTN_DELTA_FROM_OUT)) return ATTN_ERR_INVALID;
   if (!ragged && dflags == ATTN_DELTA_EXACT) return ATTN_ERR_INVALID;
   const int inter = layout == ATTN_ROPE_INTERLEAVED;
   // delta from the scores (the exact pass) or from the bf16 `out` (one HBM read): by
@@ -718,8 +731,10 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     ok = cudaMemsetAsync(maxes, 0, 4 * sizeof(float), stream) == cudaSuccess &&
          gbattn::launch_absmax(ap, stream) == cudaSuccess;
     gbattn::RowPrepParams rp{};
+    rp.status = d->status;
     rp.bwd = 1;
     rp.rope_interleaved = inter;
+    rp.exact = exact_rope ? 1 : 0;
     rp.D = D;
     rp.cos_tab = cs;
     rp.sin_tab = sn;
@@ -854,7 +869,9 @@ int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D, f
       static_cast<long long>(pos0) + S > (1LL << 30))
     return ATTN_ERR_INVALID;
   if (!std::isfinite(rope_theta) || rope_theta <= 0.f) return ATTN_ERR_INVALID;
-  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  int layout = 0;
+  bool exact_rope = false;
+  if (!parse_rope_mode(rope_mode, 0, &layout, &exact_rope)) return ATTN_ERR_INVALID;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   DeviceState* d = nullptr;
   int st = device_state(&d);
@@ -863,8 +880,10 @@ int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D, f
   RopeGuard rope(d, stream);
   if ((st = rope.acquire(pos0 + S, D, rope_theta)) != ATTN_OK) return st;
   gbattn::RowPrepParams rp{};
+    rp.status = d->status;
   rp.bwd = 0;
-  rp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
+  rp.rope_interleaved = layout == ATTN_ROPE_INTERLEAVED;
+  rp.exact = exact_rope ? 1 : 0;
   rp.D = D;
   rp.cos_tab = rope.u.ch;
   rp.sin_tab = rope.u.sh;
@@ -881,7 +900,9 @@ int attn_decode(const void* q, const void* k_rot, const void* v, void* out, floa
   const void* ptrs[] = {q, k_rot, v, out, lse};
   int st = validate(ptrs, 5, B, Hq, Hkv, Sq > Skv ? Sq : Skv, D, rope_theta, scale);
   if (st != ATTN_OK) return st;
-  if (rope_mode != ATTN_ROPE_HALF && rope_mode != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID;
+  int layout = 0;
+  bool exact_rope = false;
+  if (!parse_rope_mode(rope_mode, 0, &layout, &exact_rope)) return ATTN_ERR_INVALID;
   if (q_pos0 < 0 || static_cast<long long>(q_pos0) + Sq > (1LL << 30) ||
       static_cast<long long>(B) * Hkv * Skv >= (1LL << 31))
     return ATTN_ERR_INVALID;
@@ -929,7 +950,8 @@ int attn_decode(const void* q, const void* k_rot, const void* v, void* out, floa
     dp.sin_tab = rope.u.sh;
     dp.cos_lo = rope.u.cl;
     dp.sin_lo = rope.u.sl;
-    dp.rope_interleaved = rope_mode == ATTN_ROPE_INTERLEAVED;
+    dp.rope_interleaved = layout == ATTN_ROPE_INTERLEAVED;
+    dp.exact = exact_rope ? 1 : 0;
     dp.status = d->status;
     dp.B = B; dp.Hq = Hq; dp.Hkv = Hkv; dp.Sq = Sq; dp.Skv = Skv; dp.D = D;
     dp.q_pos0 = q_pos0;

@@ -288,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
             s8[k] = sv[8 * g + k];
           }
           float ya[8], yb[8];
-          rope_rotate16_exact(a, bb, c8, cl8, s8, sl8, p.rope_interleaved != 0, ya, yb);
+          if (p.exact) rope_rotate16_exact(a, bb, c8, cl8, s8, sl8, p.rope_interleaved != 0, ya, yb);
+          else rope_rotate16(a, bb, c8, s8, p.rope_interleaved != 0, 1.f, ya, yb);
           *pa = pack(ya);
           *pb = pack(yb);
         }

@@ -116,6 +116,7 @@ struct RowSegment {
 struct RowPrepParams {
   int bwd;
   int rope_interleaved;  // 0: half-split pairs (i, i + D/2); 1: pairs (2i, 2i + 1)
+  int exact;             // 1: rotated rows rounded as the exact rotation rounds (else fp32)
   RowSegment seg[2];
   int D;
   const float* cos_tab;  // table hi parts
@@ -131,6 +132,7 @@ struct RowPrepParams {
   float* dk_zero;  // backward, key rows: zeroed when the main kernel sums dK/dV partials
   float* dv_zero;
   int dk_zero_rows;  // with dk_zero: rows [0, dk_zero_rows) of each head are zeroed
+  int* status;       // device status word (a wait that expired)
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
@@ -243,6 +245,7 @@ struct DecParams {
   const float* cos_lo;   // table lo parts
   const float* sin_lo;
   int rope_interleaved;
+  int exact;             // 1: the query rows rounded as the exact rotation rounds
   int* status;
   int B, Hq, Hkv, Sq, Skv, D;
   int q_pos0;

@@ -129,6 +129,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   bool ok = gbattn::launch_rope_table(tabp, tab_n, S, D, static_cast<double>(rope_theta),
                                       stream) == cudaSuccess;
   gbattn::RowPrepParams rp{};
+  rp.status = status;
   rp.bwd = 0;
   rp.D = D;
   rp.cos_tab = tabp;

@@ -23,6 +23,7 @@ namespace gbattn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSitePrep = 60;  // status-word site of the pre-pass's wait
 
 // cos and sin of p * theta^(-2i/D), p < S, i < D/2, evaluated in fp64 and stored as
 // fp32 pairs: hi = fp32(x), lo = fp32(x - hi), so that hi + lo carries about 48
@@ -144,25 +145,13 @@ __global__ void __launch_bounds__(kAbsMaxThreads) absmax_kernel(const AbsMaxPara
   }
 }
 
-// Work of one thread of the row pre-pass: kRopePairs rotation pairs (table entries
-// loaded once) of one row position, in kHeadsPerThread heads.
+// Rotation pairs per thread of the row pre-pass (its table entries are loaded once).
 constexpr int kRopePairs = 4;
-constexpr int kHeadsPerThread = 1;
 
 template <int N>
 struct alignas(4 * N) Bf16xN {  // N bf16 / fp16 values
   uint32_t w[N / 2];
 };
-template <int N>
-__device__ __forceinline__ void loadn_bf16(const void* p, float (&o)[N]) {
-  const Bf16xN<N> x = *reinterpret_cast<const Bf16xN<N>*>(p);
-#pragma unroll
-  for (int i = 0; i < N / 2; ++i) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.w[i]));
-    o[2 * i] = f.x;
-    o[2 * i + 1] = f.y;
-  }
-}
 template <int N>
 __device__ __forceinline__ void storen_bf16(void* p, const float (&o)[N]) {
   Bf16xN<N> x;
@@ -195,89 +184,286 @@ __device__ __forceinline__ void zero4(float* p) {
   *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Threads of one segment: (position, chunk c < D/(2 kRopePairs), group of
-// kHeadsPerThread heads), chunks fastest, then positions, so that the threads of a row
-// are adjacent lanes and a warp covers consecutive rows of one head.
-template <int D>
-__device__ __forceinline__ long long seg_threads(const RowSegment& sg) {
-  if (sg.rows == 0) return 0;
-  const long long heads = sg.rows / sg.Sp;
-  return static_cast<long long>(sg.Sp) * (D / (2 * kRopePairs)) *
-         ((heads + kHeadsPerThread - 1) / kHeadsPerThread);
-}
-
-// Query rows (segment 0) and key rows (segment 1) of one call: each output row holds
-// the rotated input row of its head and position (half-split or interleaved pairs,
-// the exact rotation rounded to bf16). A segment's outputs hold Sp rows per head, of
-// which the first S are its input rows; when the sequence is padded to whole tiles the
-// rest are written as rows that contribute nothing (zero operands, delta 0 and, in
-// the backward, lse * log2 e = +inf so that their probabilities are 0).
+// The default row pre-pass: one thread per (output row, c) with c < D/16 and the two
+// 8-element groups of rope_off_a / rope_off_b, the rotation in fp32 with the table's
+// hi parts (rope_rotate16) and one rounding to bf16. Rows [0, seg[0].rows) are query
+// rows, the next seg[1].rows are key rows; a segment's outputs hold Sp rows per head,
+// of which the first S are its input rows (the rest, when the sequence is padded to
+// whole tiles, are written as rows that contribute nothing, as above).
 template <int D, bool kBwd, bool kPad>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
-  constexpr int NP = kRopePairs;
-  constexpr int HT = kHeadsPerThread;
-  constexpr int T = D / (2 * NP);  // threads per row
+  constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long n0 = seg_threads<D>(p.seg[0]);
-  const bool is_q = t < n0;
+  const long long grow = t / T;
+  const int c = static_cast<int>(t % T);
+  const bool is_q = grow < p.seg[0].rows;
   const RowSegment& sg = is_q ? p.seg[0] : p.seg[1];
-  const long long u = is_q ? t : t - n0;
-  // the T threads of a row leave together (thread counts are multiples of T)
-  if (u >= seg_threads<D>(sg)) return;
-  const int c = static_cast<int>(u % T);
-  const long long pr = u / T;
-  const int i = static_cast<int>(pr % sg.Sp);  // row within the head
-  const int g = static_cast<int>(pr / sg.Sp);  // head group
-  const int heads = static_cast<int>(sg.rows / sg.Sp);
-  const int h0 = g * HT;
-  const int nh = min(HT, heads - h0);
+  const long long row0 = is_q ? grow : grow - p.seg[0].rows;
+  // Threads past the last row read row 0 of the segment (a valid address), take
+  // part in the shuffles below and write nothing.
+  const bool live = row0 < sg.rows;
+  // output row, its head and row within the head (rows < 2^31: 32-bit division)
+  const unsigned ro32 = live ? static_cast<unsigned>(row0) : 0u;
+  const unsigned head = ro32 / static_cast<unsigned>(sg.Sp);
+  const int i = static_cast<int>(ro32 - head * static_cast<unsigned>(sg.Sp));
+  const long long ro = ro32;
   const bool real = !kPad || i < sg.S;  // kPad = false: every output row is an input row
+  const long long ri =  // input row
+      !kPad ? ro : (real ? static_cast<long long>(head) * sg.S + i : 0);
   const int pos = sg.pos0 + (real ? i : 0);
   const bool inter = p.rope_interleaved != 0;
-  const int oa = rope_off_a_n<NP>(c, inter), ob = rope_off_b_n<NP>(c, D, inter);
-  const bool x2_in = kBwd || sg.y2 != nullptr;  // a second tensor (dout / v) to copy
-  const bool dot = kBwd && is_q && p.out != nullptr;  // delta from out
-  auto row_in = [&](int k) {  // input row of head h0 + k
-    const long long h = h0 + k;
-    return !kPad ? h * sg.Sp + i : h * sg.S + (real ? i : 0);
-  };
-  // Every load of the thread's heads is issued before any is used (the table, then
-  // NP elements of each of the row's halves per head and tensor), so that enough
-  // bytes are in flight for the HBM stream.
-  Bf16xN<NP> xa[HT], xb[HT], za[HT], zb[HT], oa_[HT], ob_[HT];
+  const int oa = rope_off_a(c, inter), ob = rope_off_b(c, D, inter);
+  const long long e1 = ri * D + oa, e2 = ri * D + ob;  // input elements
+  const long long f1 = ro * D + oa, f2 = ro * D + ob;  // output elements
+  const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float x1[8], x2[8], cs[8], sn[8], y1[8], y2[8];
+  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e1, x1);
+  load8_bf16(static_cast<const __nv_bfloat16*>(sg.x) + e2, x2);
+  load8(p.cos_tab + (long long)pos * H + 8 * c, cs);
+  load8(p.sin_tab + (long long)pos * H + 8 * c, sn);
+  rope_rotate16(x1, x2, cs, sn, inter, 1.f, y1, y2);
+  if (!real) {
 #pragma unroll
-  for (int k = 0; k < HT; ++k) {
-    if (k < nh) {
-      const long long r = row_in(k) * D;
-      xa[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x) + r + oa);
-      xb[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x) + r + ob);
-      if (x2_in) {
-        za[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x2) + r + oa);
-        zb[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(sg.x2) + r + ob);
-      }
-      if (dot) {
-        oa_[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(p.out) + r + oa);
-        ob_[k] = *reinterpret_cast<const Bf16xN<NP>*>(static_cast<const __nv_bfloat16*>(p.out) + r + ob);
+    for (int k = 0; k < 8; ++k) y1[k] = y2[k] = 0.f;
+  }
+  if constexpr (!kBwd) {
+    if (live) {
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
+      store8_bf16(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
+      if (sg.y2 != nullptr) {  // padded copy of v (key rows)
+        float a1[8], a2[8];
+        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
+        load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
+        if (!real) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
+        }
+        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
+        store8_bf16(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
       }
     }
+  } else {
+    const BwdExponents ex = bwd_exponents(p.maxes);
+    const float s_rot = exp2i(is_q ? ex.q : ex.k);
+    const float s_x2 = exp2i(is_q ? ex.dout : ex.v);
+    float a1[8], a2[8];
+    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e1, a1);
+    load8_bf16(static_cast<const __nv_bfloat16*>(sg.x2) + e2, a2);
+    if (!real) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a1[k] = a2[k] = 0.f;
+    }
+    if (live) {
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f1, y1, s_rot);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y) + f2, y2, s_rot);
+      // x2 is already bf16: scaling by a power of two and storing fp16 is exact
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
+      store8_bf16_scaled_f16(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
+    }
+    // delta for query rows, unless the exact delta pass writes it (out is then null:
+    // the same for every thread). Every thread computes it and takes part in the
+    // shuffle (a warp may straddle the query/key boundary); key rows read row 0 of
+    // `out` and write nothing.
+    float dot = 0.f;
+    if (p.out != nullptr) {
+      float o1[8], o2[8];
+      const long long eo = is_q ? 0 : ri * D;
+      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e1 - eo), o1);
+      load8_bf16(static_cast<const __nv_bfloat16*>(p.out) + (e2 - eo), o2);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dot += a1[k] * o1[k] + a2[k] * o2[k];
+#pragma unroll
+      for (int o = T / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    }
+    if (!is_q && live && p.dk_zero != nullptr && i < p.dk_zero_rows) {
+      store8(p.dk_zero + f1, z);
+      store8(p.dk_zero + f2, z);
+      store8(p.dv_zero + f1, z);
+      store8(p.dv_zero + f2, z);
+    }
+    if (is_q && live) {
+      if (c == 0) {
+        if (p.out != nullptr) p.delta[ro] = real ? dot * exp2i(ex.dout + ex.v) : 0.f;
+        p.lse2[ro] = real ? p.lse[ri] * kLog2e : INFINITY;
+      }
+      store8(p.dqacc + f1, z);
+      store8(p.dqacc + f2, z);
+    }
   }
-  float chi[NP], clo[NP], shi[NP], slo[NP];
-  const long long te = (long long)pos * H + NP * c;
-  load4(p.cos_tab + te, chi);
-  load4(p.sin_tab + te, shi);
-  load4(p.cos_lo + te, clo);
-  load4(p.sin_lo + te, slo);
+}
+
+// The row pre-pass streams its rows through shared memory. One CTA per SM takes a
+// contiguous range of items, an item being kBlockRows positions of kBlockHeads heads of
+// one segment. A producer warp keeps the next items' rows in flight with bulk copies
+// into a ring of stages (mbarriers with byte counts), so that the bytes in flight are
+// held in shared memory, not registers, and the table rows of a position block are
+// loaded once for every head group of those positions (two table slots). Sixteen compute
+// warps rotate kRopePairs pairs of one row per thread at a time from shared memory and
+// store the results with coalesced 8-byte stores.
+constexpr int kBlockRows = 16;
+constexpr int kBlockHeads = 4;
+constexpr int kPrepCompute = 512;                 // compute threads (16 warps)
+constexpr int kPrepThreads = kPrepCompute + 32;   // + the producer warp
+
+template <int D, bool kBwd>
+struct PrepCfg {
+  static constexpr int H = D / 2;
+  static constexpr int kTabFloats = kBlockRows * H;        // one table array's block
+  static constexpr int kTabBytes = 4 * kTabFloats * 4;     // cos hi, sin hi, cos lo, sin lo
+  static constexpr int kTensors = kBwd ? 3 : 2;            // row blocks an item holds at most
+  static constexpr int kRowElems = kBlockRows * D;         // one head's rows of an item
+  static constexpr int kLseOff = kTensors * kBlockHeads * kRowElems * 2;
+  static constexpr int kStageBytes = kLseOff + (kBwd ? kBlockHeads * kBlockRows * 4 : 0);
+  static constexpr int kStagesFit = (220 * 1024 - 2 * kTabBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kSmemBytes = 2 * kTabBytes + kStages * kStageBytes + 128;
+  static_assert(kStages >= 2, "row pre-pass ring");
+};
+
+struct PrepItem {
+  int seg, p0, h0, nh, nrows, nreal;
+};
+template <bool kPad>
+__device__ __forceinline__ PrepItem prep_item(const RowPrepParams& p, long long n, long long n0,
+                                              int ng0, int ng1) {
+  PrepItem it;
+  it.seg = n < n0 ? 0 : 1;
+  const RowSegment& sg = p.seg[it.seg];
+  const long long m = it.seg ? n - n0 : n;
+  const int ng = it.seg ? ng1 : ng0;
+  it.p0 = static_cast<int>(m / ng) * kBlockRows;
+  it.h0 = static_cast<int>(m % ng) * kBlockHeads;
+  const int heads = static_cast<int>(sg.rows / sg.Sp);
+  it.nh = min(kBlockHeads, heads - it.h0);
+  it.nrows = min(kBlockRows, sg.Sp - it.p0);  // the last block of a head may be short
+  // input rows that exist (the rest of a padded head is written as zeros)
+  it.nreal = !kPad ? it.nrows : max(0, min(it.nrows, sg.S - it.p0));
+  return it;
+}
+
+// The exact-rotation row pre-pass (RowPrepParams::exact): query rows (segment 0) and
+// key rows (segment 1) of one call, each output row the rotated input row of its head
+// and position, rounded to bf16 as the exact rotation rounds (rope_rotate_fast). A
+// segment's outputs hold Sp rows per head, of which the first S are its input rows;
+// when the sequence is padded to whole tiles the rest are written as rows that
+// contribute nothing (zero operands, delta 0 and, in the backward, lse * log2 e = +inf
+// so that their probabilities are 0).
+template <int D, bool kBwd, bool kPad>
+__global__ void __launch_bounds__(kPrepThreads, 1) row_prep_exact_kernel(const RowPrepParams p) {
+  using C = PrepCfg<D, kBwd>;
+  constexpr int NP = kRopePairs;
+  constexpr int T = D / (2 * NP);  // threads per row
+  constexpr int H = D / 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_tab_full[2], bar_tab_empty[2];
+  __shared__ int abort_flag;
+  float* tabs = reinterpret_cast<float*>(smem);                    // [2][4][R][H]
+  uint8_t* stages = smem + 2 * C::kTabBytes;                       // [kStages][kStageBytes]
+  volatile int* abort_ptr = &abort_flag;
+
+  // items: segment 0 then 1, position blocks then head groups; this CTA's range
+  const int ng0 = p.seg[0].rows ? static_cast<int>((p.seg[0].rows / p.seg[0].Sp + kBlockHeads - 1) / kBlockHeads) : 0;
+  const int ng1 = p.seg[1].rows ? static_cast<int>((p.seg[1].rows / p.seg[1].Sp + kBlockHeads - 1) / kBlockHeads) : 0;
+  const long long n0 = p.seg[0].rows ? static_cast<long long>((p.seg[0].Sp + kBlockRows - 1) / kBlockRows) * ng0 : 0;
+  const long long n1 = p.seg[1].rows ? static_cast<long long>((p.seg[1].Sp + kBlockRows - 1) / kBlockRows) * ng1 : 0;
+  const long long nall = n0 + n1;
+  const long long first = nall * blockIdx.x / gridDim.x;
+  const long long last = nall * (blockIdx.x + 1) / gridDim.x;
+  const bool dot = kBwd && p.out != nullptr;  // delta from out (query rows)
+
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < C::kStages; ++i) {
+      gb::mbar_init(gb::smem_u32(&bar_full[i]), 1);
+      gb::mbar_init(gb::smem_u32(&bar_empty[i]), kPrepCompute);
+    }
+    for (int i = 0; i < 2; ++i) {
+      gb::mbar_init(gb::smem_u32(&bar_tab_full[i]), 1);
+      gb::mbar_init(gb::smem_u32(&bar_tab_empty[i]), kPrepCompute);
+    }
+    gb::fence_mbar_init();
+  }
+  __syncthreads();
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
+
+  if (tid >= kPrepCompute) {
+    // ================================================================ producer
+    if (tid == kPrepCompute) {
+      int tgen = -1, pseg = -1, pp0 = -1;
+      long long issued = 0;
+      for (long long n = first; n < last; ++n) {
+        const PrepItem it = prep_item<kPad>(p, n, n0, ng0, ng1);
+        const RowSegment& sg = p.seg[it.seg];
+        if (it.seg != pseg || it.p0 != pp0) {  // a new position block: its table rows
+          ++tgen;
+          const int ts = tgen & 1;
+          if (!gb::bounded_wait(gb::smem_u32(&bar_tab_empty[ts]), ((tgen >> 1) & 1) ^ 1, abort_ptr,
+                                p.status, kSitePrep))
+            break;
+          const uint32_t tb = static_cast<uint32_t>(it.nrows) * H * 4;
+          const uint32_t full = gb::smem_u32(&bar_tab_full[ts]);
+          gb::mbar_arrive_expect_tx(full, 4 * tb);
+          const long long te = static_cast<long long>(sg.pos0 + it.p0) * H;
+          const float* src[4] = {p.cos_tab, p.sin_tab, p.cos_lo, p.sin_lo};
+          for (int a = 0; a < 4; ++a)
+            gb::bulk_load(gb::smem_u32(tabs + (ts * 4 + a) * C::kTabFloats), src[a] + te, tb, full);
+          pseg = it.seg;
+          pp0 = it.p0;
+        }
+        const int st = static_cast<int>(issued % C::kStages);
+        if (!gb::bounded_wait(gb::smem_u32(&bar_empty[st]), ((issued / C::kStages) & 1) ^ 1,
+                              abort_ptr, p.status, kSitePrep))
+          break;
+        const bool q = it.seg == 0;
+        const bool x2_in = kBwd || sg.y2 != nullptr;
+        const int ntens = 1 + (x2_in ? 1 : 0) + (dot && q ? 1 : 0);
+        const bool lse_in = kBwd && q && !kPad;  // lse rows (padded: read in the loop)
+        const uint32_t rb = static_cast<uint32_t>(it.nreal) * D * 2;
+        const uint32_t lb = lse_in ? static_cast<uint32_t>(it.nreal) * 4 : 0u;
+        const uint32_t full = gb::smem_u32(&bar_full[st]);
+        gb::mbar_arrive_expect_tx(full, static_cast<uint32_t>(it.nh) * (ntens * rb + lb));
+        uint8_t* stg = stages + st * C::kStageBytes;
+        const void* src[3] = {sg.x, x2_in ? sg.x2 : p.out, p.out};
+        if (rb > 0) {
+          for (int k = 0; k < it.nh; ++k) {
+            const long long r = static_cast<long long>(it.h0 + k) * (kPad ? sg.S : sg.Sp) + it.p0;
+            for (int m = 0; m < ntens; ++m)
+              gb::bulk_load(gb::smem_u32(stg + ((m * kBlockHeads + k) * C::kRowElems) * 2),
+                            static_cast<const __nv_bfloat16*>(src[m]) + r * D, rb, full);
+            if (lb > 0)
+              gb::bulk_load(gb::smem_u32(stg + C::kLseOff + k * kBlockRows * 4), p.lse + r, lb,
+                            full);
+          }
+        }
+        ++issued;
+      }
+      // copies already issued land before the CTA releases its shared memory
+      for (long long i = issued - C::kStages > 0 ? issued - C::kStages : 0; i < issued; ++i) {
+        const uint64_t t0 = gb::globaltimer_ns();
+        while (!gb::mbar_try_wait(gb::smem_u32(&bar_full[i % C::kStages]), (i / C::kStages) & 1) &&
+               gb::globaltimer_ns() - t0 < gb::kWaitLimitNs / 4) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ================================================================ compute warps
   BwdExponents ex{0, 0, 0, 0};
   if constexpr (kBwd) ex = bwd_exponents(p.maxes);
-  const float s_rot = exp2i(is_q ? ex.q : ex.k);
-  const float s_x2 = exp2i(is_q ? ex.dout : ex.v);
-  // lanes of this row, for the delta reduction
-  const unsigned lane = threadIdx.x & 31u;
+  const bool inter = p.rope_interleaved != 0;
+  const int c = tid % T;
+  const int oa = rope_off_a_n<NP>(c, inter), ob = rope_off_b_n<NP>(c, D, inter);
+  const unsigned lane = tid & 31u;
   const unsigned row_mask = ((1u << T) - 1u) << (lane & ~static_cast<unsigned>(T - 1));
-  auto unpack = [](const Bf16xN<NP>& v, float (&o)[NP]) {
+  auto lds = [](const __nv_bfloat16* q, float (&o)[NP]) {  // NP bf16 values from shared memory
+    const Bf16xN<NP> v = *reinterpret_cast<const Bf16xN<NP>*>(q);
 #pragma unroll
     for (int e = 0; e < NP / 2; ++e) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.w[e]));
@@ -285,60 +471,116 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
       o[2 * e + 1] = f.y;
     }
   };
-#pragma unroll
-  for (int k = 0; k < HT; ++k) {
-    if (k >= nh) break;
-    const long long ro = static_cast<long long>(h0 + k) * sg.Sp + i;  // output row
-    const long long f1 = ro * D + oa, f2 = ro * D + ob;               // output elements
-    float x1[NP], x2[NP], y1[NP], y2[NP], a1[NP], a2[NP];
-    unpack(xa[k], x1);
-    unpack(xb[k], x2);
-    rope_rotate_exact<NP>(x1, x2, chi, clo, shi, slo, inter, y1, y2);
-    if (x2_in) {
-      unpack(za[k], a1);
-      unpack(zb[k], a2);
+  int tgen = -1, pseg = -1, pp0 = -1;
+  long long used = 0;
+  for (long long n = first; n < last; ++n) {
+    const PrepItem it = prep_item<kPad>(p, n, n0, ng0, ng1);
+    const RowSegment& sg = p.seg[it.seg];
+    const bool q = it.seg == 0;
+    if (it.seg != pseg || it.p0 != pp0) {
+      if (tgen >= 0) gb::mbar_arrive(gb::smem_u32(&bar_tab_empty[tgen & 1]));
+      ++tgen;
+      if (!gb::bounded_wait(gb::smem_u32(&bar_tab_full[tgen & 1]), (tgen >> 1) & 1, abort_ptr,
+                            p.status, kSitePrep))
+        break;
+      pseg = it.seg;
+      pp0 = it.p0;
     }
-    if (!real) {
+    const int st = static_cast<int>(used % C::kStages);
+    if (!gb::bounded_wait(gb::smem_u32(&bar_full[st]), (used / C::kStages) & 1, abort_ptr, p.status,
+                          kSitePrep))
+      break;
+    const float* tab = tabs + (tgen & 1) * 4 * C::kTabFloats;
+    const uint8_t* stg = stages + st * C::kStageBytes;
+    const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(stg);
+    const bool x2_in = kBwd || sg.y2 != nullptr;
+    const float s_rot = exp2i(q ? ex.q : ex.k);
+    const float s_x2 = exp2i(q ? ex.dout : ex.v);
+#pragma unroll 1
+    for (int row = tid / T; row < it.nh * kBlockRows; row += kPrepCompute / T) {
+      const int k = row / kBlockRows, il = row % kBlockRows;
+      if (il >= it.nrows) continue;
+      const int i = it.p0 + il;  // row within the head
+      const bool real = il < it.nreal;
+      const long long ro = static_cast<long long>(it.h0 + k) * sg.Sp + i;  // output row
+      const long long f1 = ro * D + oa, f2 = ro * D + ob;
+      float chi[NP], clo[NP], shi[NP], slo[NP];
 #pragma unroll
-      for (int e = 0; e < NP; ++e) y1[e] = y2[e] = a1[e] = a2[e] = 0.f;
-    }
-    if constexpr (!kBwd) {
-      storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
-      storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
-      if (sg.y2 != nullptr) {  // padded copy of v (key rows)
-        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
-        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
+      for (int a = 0; a < 4; ++a) {
+        const float4 v = *reinterpret_cast<const float4*>(tab + a * C::kTabFloats + il * H + NP * c);
+        float* dst = a == 0 ? chi : a == 1 ? shi : a == 2 ? clo : slo;
+        dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
       }
-    } else {
-      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f1, y1, s_rot);
-      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f2, y2, s_rot);
-      // x2 is already bf16: scaling by a power of two and storing fp16 is exact
-      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
-      storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
-      if (is_q) {
-        // delta_i = dout_i . out_i (unless the exact delta pass writes it instead)
-        if (dot) {
-          float o1[NP], o2[NP];
-          unpack(oa_[k], o1);
-          unpack(ob_[k], o2);
-          float d = 0.f;
-#pragma unroll
-          for (int e = 0; e < NP; ++e) d += a1[e] * o1[e] + a2[e] * o2[e];
-#pragma unroll
-          for (int o = T / 2; o > 0; o >>= 1) d += __shfl_xor_sync(row_mask, d, o);
-          if (c == 0) p.delta[ro] = real ? d * exp2i(ex.dout + ex.v) : 0.f;
+      const __nv_bfloat16* xr = xs + k * C::kRowElems + il * D;
+      float x1[NP], x2[NP], y1[NP], y2[NP], a1[NP], a2[NP];
+      if (real) {
+        lds(xr + oa, x1);
+        lds(xr + ob, x2);
+        if (x2_in) {
+          lds(xr + kBlockHeads * C::kRowElems + oa, a1);
+          lds(xr + kBlockHeads * C::kRowElems + ob, a2);
         }
-        if (c == 0) p.lse2[ro] = real ? p.lse[row_in(k)] * kLog2e : INFINITY;
-        zero4(p.dqacc + f1);
-        zero4(p.dqacc + f2);
-      } else if (p.dk_zero != nullptr && i < p.dk_zero_rows) {
-        zero4(p.dk_zero + f1);
-        zero4(p.dk_zero + f2);
-        zero4(p.dv_zero + f1);
-        zero4(p.dv_zero + f2);
+      } else {
+#pragma unroll
+        for (int e = 0; e < NP; ++e) x1[e] = x2[e] = a1[e] = a2[e] = 0.f;
+      }
+      rope_rotate_fast<NP>(x1, x2, chi, clo, shi, slo, inter, y1, y2);
+      if constexpr (!kBwd) {
+        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f1, y1);
+        storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y) + f2, y2);
+        if (sg.y2 != nullptr) {  // padded copy of v (key rows)
+          storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f1, a1);
+          storen_bf16<NP>(static_cast<__nv_bfloat16*>(sg.y2) + f2, a2);
+        }
+      } else {
+        storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f1, y1, s_rot);
+        storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y) + f2, y2, s_rot);
+        // x2 is already bf16: scaling by a power of two and storing fp16 is exact
+        storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f1, a1, s_x2);
+        storen_bf16_scaled_f16<NP>(static_cast<__half*>(sg.y2) + f2, a2, s_x2);
+        if (q) {
+          // delta_i = dout_i . out_i (unless the exact delta pass writes it instead)
+          if (dot) {
+            float o1[NP], o2[NP];
+            if (real) {
+              lds(xr + 2 * kBlockHeads * C::kRowElems + oa, o1);
+              lds(xr + 2 * kBlockHeads * C::kRowElems + ob, o2);
+            } else {
+#pragma unroll
+              for (int e = 0; e < NP; ++e) o1[e] = o2[e] = 0.f;
+            }
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < NP; ++e) d += a1[e] * o1[e] + a2[e] * o2[e];
+#pragma unroll
+            for (int o = T / 2; o > 0; o >>= 1) d += __shfl_xor_sync(row_mask, d, o);
+            if (c == 0) p.delta[ro] = d * exp2i(ex.dout + ex.v);
+          }
+          if (c == 0) {
+            float l = INFINITY;
+            if (real) {
+              if constexpr (kPad)
+                l = p.lse[static_cast<long long>(it.h0 + k) * sg.S + i];
+              else
+                l = reinterpret_cast<const float*>(stg + C::kLseOff)[k * kBlockRows + il];
+              l *= kLog2e;
+            }
+            p.lse2[ro] = l;
+          }
+          zero4(p.dqacc + f1);
+          zero4(p.dqacc + f2);
+        } else if (p.dk_zero != nullptr && i < p.dk_zero_rows) {
+          zero4(p.dk_zero + f1);
+          zero4(p.dk_zero + f2);
+          zero4(p.dv_zero + f1);
+          zero4(p.dv_zero + f2);
+        }
       }
     }
+    gb::mbar_arrive(gb::smem_u32(&bar_empty[st]));
+    ++used;
   }
+  if (tgen >= 0) gb::mbar_arrive(gb::smem_u32(&bar_tab_empty[tgen & 1]));
 }
 
 // dq in fp32, or rounded to bf16 (nearest even) when kBf16.
@@ -498,18 +740,44 @@ cudaError_t launch_absmax(const AbsMaxParams& p_in, cudaStream_t stream) {
 }
 
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
-  auto seg_thr = [&](const RowSegment& sg) {
-    if (sg.rows == 0) return 0LL;
-    const long long heads = sg.rows / sg.Sp;
-    return static_cast<long long>(sg.Sp) * (p.D / (2 * kRopePairs)) *
-           ((heads + kHeadsPerThread - 1) / kHeadsPerThread);
-  };
-  const long long threads = seg_thr(p.seg[0]) + seg_thr(p.seg[1]);
-  if (threads == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)blocks_for(threads);
   const bool pad = p.seg[0].S != p.seg[0].Sp || p.seg[1].S != p.seg[1].Sp;
+  if (!p.exact) {
+    const long long threads = (p.seg[0].rows + p.seg[1].rows) * (p.D / 16);
+    if (threads == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)blocks_for(threads);
 #define GB_PREP(DD, BW, PD) \
   return launch_pdl(row_prep_kernel<DD, BW, PD>, dim3(grid), dim3(256), 0, stream, p)
+    if (p.D == 128) {
+      if (p.bwd) { if (pad) GB_PREP(128, true, true); else GB_PREP(128, true, false); }
+      else { if (pad) GB_PREP(128, false, true); else GB_PREP(128, false, false); }
+    } else {
+      if (p.bwd) { if (pad) GB_PREP(64, true, true); else GB_PREP(64, true, false); }
+      else { if (pad) GB_PREP(64, false, true); else GB_PREP(64, false, false); }
+    }
+#undef GB_PREP
+  }
+  auto items = [](const RowSegment& sg) {
+    if (sg.rows == 0) return 0LL;
+    const long long heads = sg.rows / sg.Sp;
+    return static_cast<long long>((sg.Sp + kBlockRows - 1) / kBlockRows) *
+           ((heads + kBlockHeads - 1) / kBlockHeads);
+  };
+  const long long n = items(p.seg[0]) + items(p.seg[1]);
+  if (n == 0) return cudaSuccess;
+  int dev = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(n < nsm ? n : nsm);  // one CTA per SM
+#define GB_PREP(DD, BW, PD)                                                                     \
+  do {                                                                                          \
+    constexpr int smem = PrepCfg<DD, BW>::kSmemBytes;                                           \
+    e = cudaFuncSetAttribute(row_prep_exact_kernel<DD, BW, PD>,                                 \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);                \
+    if (e != cudaSuccess) return e;                                                             \
+    return launch_pdl(row_prep_exact_kernel<DD, BW, PD>, dim3(grid), dim3(kPrepThreads), smem,  \
+                      stream, p);                                                               \
+  } while (0)
   if (p.D == 128) {
     if (p.bwd) { if (pad) GB_PREP(128, true, true); else GB_PREP(128, true, false); }
     else { if (pad) GB_PREP(128, false, true); else GB_PREP(128, false, false); }

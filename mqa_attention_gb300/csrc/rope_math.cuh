@@ -188,6 +188,52 @@ __device__ __forceinline__ void rope_rotate16_exact(const float (&a)[8], const f
   rope_rotate_exact<8>(a, b, c_hi, c_lo, s_hi, s_lo, inter, ya, yb);
 }
 
+// The same result at the cost of the plain fp32 rotation for almost every pair: y =
+// fl(x c_hi - fl(y s_hi)) differs from the exact value by less than 2^-22 (|x| + |y|)
+// (two roundings of at most 2^-24 of a magnitude below |x| + |y|, and the hi parts'
+// own error, 2^-24 of a value below 1, times |x| and |y|). When neither output of the
+// pair lies within 2^-21 (|x| + |y|) of a bf16 rounding midpoint (low 16 bits 0x8000),
+// the exact value rounds to bf16 like the plain one; otherwise (about 1 pair in 10^4)
+// the pair is recomputed exactly (rope_pair_exact).
+__device__ __forceinline__ bool rope_far_from_midpoint(float r, float t) {
+  const float mid = __uint_as_float((__float_as_uint(r) & 0xffff0000u) | 0x8000u);
+  return fabsf(__fsub_rn(r, mid)) > t;
+}
+__device__ __forceinline__ void rope_pair_fast(float x, float y, float ch, float cl, float sh,
+                                               float sl, float& rx, float& ry) {
+  const float px = __fmaf_rn(x, ch, -__fmul_rn(y, sh));
+  const float py = __fmaf_rn(y, ch, __fmul_rn(x, sh));
+  const float t = __fmul_rn(__fadd_rn(fabsf(x), fabsf(y)), 4.76837158203125e-7f);  // 2^-21
+  if (rope_far_from_midpoint(px, t) & rope_far_from_midpoint(py, t)) {
+    rx = px;
+    ry = py;
+  } else {
+    rope_pair_exact(x, y, ch, cl, sh, sl, rx, ry);
+  }
+}
+
+// rope_rotate_exact's result through rope_pair_fast.
+template <int NP>
+__device__ __forceinline__ void rope_rotate_fast(const float (&a)[NP], const float (&b)[NP],
+                                                 const float (&c_hi)[NP], const float (&c_lo)[NP],
+                                                 const float (&s_hi)[NP], const float (&s_lo)[NP],
+                                                 bool inter, float (&ya)[NP], float (&yb)[NP]) {
+  if (!inter) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+      rope_pair_fast(a[i], b[i], c_hi[i], c_lo[i], s_hi[i], s_lo[i], ya[i], yb[i]);
+  } else {
+    constexpr int H = NP / 2;
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+      rope_pair_fast(a[2 * j], a[2 * j + 1], c_hi[j], c_lo[j], s_hi[j], s_lo[j], ya[2 * j],
+                     ya[2 * j + 1]);
+      rope_pair_fast(b[2 * j], b[2 * j + 1], c_hi[H + j], c_lo[H + j], s_hi[H + j], s_lo[H + j],
+                     yb[2 * j], yb[2 * j + 1]);
+    }
+  }
+}
+
 // Element offsets (within a row) of the two NP-element groups of chunk c < D/(2 NP):
 // half-split [NP c, NP c + NP) and [D/2 + NP c, +NP); interleaved [2 NP c, +NP) and
 // [2 NP c + NP, +NP). Both use the table entries [NP c, NP c + NP) of the row's position.

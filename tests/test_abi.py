@@ -97,6 +97,19 @@ def test_bwd_rejects_bad_delta_flags(built_lib, mode):
                                    128, 64, 10000.0, mode, 0.125, 1, None) == M.ATTN_ERR_INVALID
 
 
+def test_exact_rope_flag_is_accepted_where_rope_mode_is(built_lib):
+    """ATTN_ROPE_EXACT (0x10) combines with either layout; with a bad layout, or on an
+    entry point that takes no flags besides it, the call is still rejected first."""
+    lib = built_lib
+    ex = M.ROPE_EXACT
+    assert lib.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 128, 96, 10000.0, ex | 1, 0.125,
+                           1, None) == M.ATTN_ERR_UNSUPPORTED  # flag accepted, D rejected
+    assert lib.attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 128, 64, 10000.0, ex | 2, 0.125,
+                           1, None) == M.ATTN_ERR_INVALID
+    assert lib.attn_rope(FAKE, FAKE, 4, 100, 0, 64, 10000.0, ex | 0x100, None) == \
+        M.ATTN_ERR_INVALID
+
+
 def test_delta_flags_only_where_they_apply(built_lib):
     """The exact delta pass needs the whole attention of each query row: a partial
     block's backward and every forward entry point refuse the flag."""

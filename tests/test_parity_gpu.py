@@ -366,10 +366,11 @@ def test_power_of_two_input_scales_are_exact(D, hkv):
 # nearly all of each row. These use the exact delta pass (ATTN_DELTA_EXACT): with
 # delta = dout . out from the bf16 `out`, the rounding of out dominates dq and dk on
 # peaked rows. They are held to the stated bounds against the oracle whose rotated
-# q~, k~ are rounded to bf16 (the operands the score product receives; the kernels
-# round the exact rotation, so both sides hold the same q~, k~): with scores of
-# standard deviation 9-36 a one-ulp change of q~ moves a score by up to ~0.1, far
-# beyond what the exact-rotation oracle could be compared against.
+# q~, k~ are rounded to bf16 (the operands the score product receives), with the
+# kernels' rotated operands rounded as the exact rotation rounds (ATTN_ROPE_EXACT),
+# so that both sides hold the same q~, k~: with scores of standard deviation 9-36 a
+# one-ulp change of one element of q~ moves a score by up to ~0.1, and fp32 rotation
+# makes such a change in about 1 element of 40,000.
 
 
 def gen_scaled(wl, factors):
@@ -386,9 +387,10 @@ def gen_scaled(wl, factors):
 
 
 def run_exact(wl, dev):
-    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal)
+    out, lse = M.forward(dev["q"], dev["k"], dev["v"], wl.theta, wl.scale, wl.causal,
+                         exact_rope=True)
     dq, dk, dv = M.backward(dev["q"], dev["k"], dev["v"], out, lse, dev["dout"], wl.theta,
-                            wl.scale, wl.causal, delta="exact")
+                            wl.scale, wl.causal, delta="exact", exact_rope=True)
     torch.cuda.synchronize()
     assert M.sync_status() == 0
     return {n: t.double().cpu() for n, t in
@@ -551,8 +553,8 @@ def test_delta_modes_agree_on_diffuse_rows():
     (64, "interleaved", 10000.0, 0, 3.0),
 ])
 def test_rope_is_the_rounded_exact_rotation(D, rope, theta, pos0, factor):
-    """attn_rope (the rotation every kernel applies to q and k before the score
-    product) returns, element for element, the bf16 value nearest the fp64 rotation:
+    """attn_rope with ATTN_ROPE_EXACT (the rotation the kernels apply to q and k in that
+    mode) returns, element for element, the bf16 value nearest the fp64 rotation:
     the oracle's RoPE ("Picotron模型实现解析Llama架构与Flash Attention集成", §1;
     "深度学习系统设计llama3-from-scratch：并行计算架构", §RoPE) rounded to bf16 (nearest
     even). 16 heads x 4096 positions, about 2-4 million elements, thousands of them
@@ -562,7 +564,7 @@ def test_rope_is_the_rounded_exact_rotation(D, rope, theta, pos0, factor):
     if factor != 1.0:
         bits = I.scale_bf16_bits(bits, factor)
     x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
-    y = M.rope(x, theta, pos0=pos0, rope=rope)
+    y = M.rope(x, theta, pos0=pos0, rope=rope, exact=True)
     torch.cuda.synchronize()
     f = torch.from_numpy(I.bf16_bits_to_f64(bits))
     ang = O.rope_angles(S, D, theta, pos0)
@@ -571,3 +573,24 @@ def test_rope_is_the_rounded_exact_rotation(D, rope, theta, pos0, factor):
     got = y.double().cpu()
     bad = (got != want)
     assert bad.sum().item() == 0, f"{bad.sum().item()} of {bad.numel()} elements differ"
+
+
+def test_default_rope_rounding_is_within_one_ulp():
+    """The default rotation (fp32, one rounding to bf16) agrees with the exactly rounded
+    one except for rare elements; each differs by at most one bf16 ulp (of the larger
+    of the two) plus the fp32 evaluation's own error, 2^-22 (|x_i| + |x_(i+D/2)|), which
+    only matters where the rotation cancels to a value far below its inputs."""
+    heads, S, D, theta = 16, 4096, 128, 500000.0
+    bits = I.normal_bf16_bits(9100, (heads, S, D))
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    a = M.rope(x, theta).float()
+    b = M.rope(x, theta, exact=True).float()
+    torch.cuda.synchronize()
+    diff = a != b
+    assert diff.sum().item() <= 1e-3 * diff.numel()
+    ulp = torch.ldexp(torch.ones_like(b), torch.frexp(torch.maximum(a.abs(), b.abs()))[1] - 8)
+    xf = x.float()
+    mag = xf[..., :D // 2].abs() + xf[..., D // 2:].abs()
+    mag = torch.cat([mag, mag], dim=-1)
+    bound = ulp + 2.0 ** -22 * mag
+    assert ((a - b).abs()[diff] <= bound[diff]).all()
