@@ -79,7 +79,9 @@ enum {
   ATTN_ERR_UNSUPPORTED = 2, /* D not in {64,128}, a partial block or position not a multiple
                                of 128, or device is not sm_103 */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-  ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait expired (see attn_sync_status) */
+  ATTN_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (see attn_sync_status) */
+  ATTN_ERR_BOUNDS = 5       /* debug build only: a kernel's index check failed and the access
+                               was skipped (see attn_sync_status) */
 };
 
 /* Forward pass.
@@ -224,7 +226,10 @@ int attn_bwd_bf16(const void* q, const void* k, const void* v, const void* out, 
 
 /* Waits for all work on `stream`, then reads and clears the device status word of the
  * current device: ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel gave up on a wait since the
- * last call (its outputs are then undefined). Synchronises the host with `stream`. */
+ * last call, or (in the library built with GB_BOUNDS_CHECK, which checks every global
+ * index and TMA coordinate before using it) ATTN_ERR_BOUNDS if a check failed; the
+ * outputs are then undefined. The first failure since the last call is the one kept.
+ * Synchronises the host with `stream`. */
 int attn_sync_status(attn_stream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */

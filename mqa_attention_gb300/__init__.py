@@ -55,9 +55,13 @@ __all__ = [
 ]
 
 LIB_NAME = "libmqa_attention_gb300.so"
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+# MQA_ATTENTION_GB300_LIB selects another build of the library (for example the
+# bounds-checking one, libmqa_attention_gb300_debug.so) for the whole process.
+LIB_PATH = os.environ.get("MQA_ATTENTION_GB300_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 
 ATTN_OK, ATTN_ERR_INVALID, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_ERR_BOUNDS = 5
 KERNEL_ROPE, KERNEL_FWD, KERNEL_BWD_PREP, KERNEL_BWD_MAIN, KERNEL_DQ_FINAL, KERNEL_DELTA = range(6)
 # delta flags OR-ed into the rope_mode of attn_bwd_ex / attn_bwd_bf16 (ATTN_DELTA_*)
 DELTA_MODES = {"auto": 0, "exact": 0x100, "from_out": 0x200}

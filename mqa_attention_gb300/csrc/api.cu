@@ -24,6 +24,7 @@ using gbattn::kTile;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int gb_status_bounds = 0x200;  // the kernels' kStatusBounds bit
 
 // One RoPE table (see launch_rope_table): positions [0, npos) of one (D, theta), four
 // fp32 arrays n floats apart, built on the stream of the call that first needed it.
@@ -421,6 +422,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported size or device";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case ATTN_ERR_BOUNDS: return "device index check failed";
     default: return "unknown status";
   }
 }
@@ -486,6 +488,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     rp.sin_tab = rope.u.sh;
     rp.cos_lo = rope.u.cl;
     rp.sin_lo = rope.u.sl;
+    rp.tab_rows = rope.u.npos;
     rp.seg[0] = {q, qr, nullptr, nullptr, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, padded ? v : nullptr, padded ? vk : nullptr, krows_p, Skv, Skvp, kv_pos0};
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
@@ -740,6 +743,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     rp.sin_tab = sn;
     rp.cos_lo = rope.u.cl;
     rp.sin_lo = rope.u.sl;
+    rp.tab_rows = rope.u.npos;
     rp.maxes = maxes;
     rp.seg[0] = {q, qr, dout, dos, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, v, vs, krows_p, Skv, Skvp, kv_pos0};
@@ -791,6 +795,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     bp.dv = dv;
     bp.cos_tab = cs;
     bp.sin_tab = sn;
+    bp.tab_rows = rope.u.npos;
     bp.status = d->status;
     bp.B = B; bp.Hq = Hq; bp.Hkv = Hkv; bp.Sq = Sqp; bp.Skv = Skvp; bp.D = D;
     bp.q_tile0 = q_pos0 / kTile;
@@ -813,8 +818,8 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   if (ok) {
     LaunchTimer tm(ATTN_KERNEL_DQ_FINAL, stream);
     ok = gbattn::launch_dq_finalize(dqacc, dq_out, bf16_grads, qrows, Sq, Sqp, q_pos0, D, scale,
-                                    maxes, cs, sn,
-                                    inter, stream) == cudaSuccess;
+                                    maxes, cs, sn, rope.u.npos, inter, d->status,
+                                    stream) == cudaSuccess;
     if (padded)
       ok = ok &&
            gbattn::launch_unpad_rows(dk, dk_out, krows, Skv, Skvp, D, bf16_grads, stream) ==
@@ -889,6 +894,7 @@ int attn_rope(const void* x, void* y, long long heads, int S, int pos0, int D, f
   rp.sin_tab = rope.u.sh;
   rp.cos_lo = rope.u.cl;
   rp.sin_lo = rope.u.sl;
+  rp.tab_rows = rope.u.npos;
   rp.seg[0] = {x, y, nullptr, nullptr, heads * S, S, S, pos0};
   rp.seg[1] = {x, y, nullptr, nullptr, 0, S, S, pos0};
   return gbattn::launch_row_prep(rp, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -950,6 +956,7 @@ int attn_decode(const void* q, const void* k_rot, const void* v, void* out, floa
     dp.sin_tab = rope.u.sh;
     dp.cos_lo = rope.u.cl;
     dp.sin_lo = rope.u.sl;
+    dp.tab_rows = rope.u.npos;
     dp.rope_interleaved = layout == ATTN_ROPE_INTERLEAVED;
     dp.exact = exact_rope ? 1 : 0;
     dp.status = d->status;
@@ -992,7 +999,7 @@ int attn_sync_status(attn_stream_t stream_) {
   if (word != 0) {
     const int zero = 0;
     cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
-    return ATTN_ERR_TIMEOUT;
+    return (word & gb_status_bounds) ? ATTN_ERR_BOUNDS : ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
 }

@@ -58,7 +58,9 @@ constexpr int kWarpMma = 13;
 
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
-  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteTab = 26
+  kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteTab = 26,
+  // index checks of the debug build
+  kChkStage = 27, kChkKv = 28, kChkDq = 29, kChkDkdv = 30, kChkTab = 31
 };
 
 template <int D>
@@ -183,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const int q0p = p.q_tile0 * kTile;          // position of the query block's first row
   const int kv_row = bhk * p.Skv + k0;
   const int nqt = p.Sq / BQ;
+  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.Sq;  // rows of q~, dO, dqacc
+  const long long rows_kv = static_cast<long long>(p.B) * p.Hkv * p.Skv;
   // causal: the query tiles at or after the key tile's position
   int qt_begin = p.causal ? (k0p - q0p) / BQ : 0;
   qt_begin = qt_begin < 0 ? 0 : (qt_begin > nqt ? nqt : qt_begin);
@@ -215,12 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const uint32_t dst = stage_addr(s);
     const int row = step_row(s);
     mbar_arrive_expect_tx(full, 2 * C::kQTileBytes + 2 * BQ * 4);
-    for (int r = 0; r < C::kRegions; ++r) {
-      tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
-      tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
+    if (bounds_ok(row >= 0 && row + BQ <= rows_q, p.status, kChkStage)) {
+      for (int r = 0; r < C::kRegions; ++r) {
+        tma_load_2d(dst + r * C::kQRegionBytes, &p.map_q, r * 64, row, full);
+        tma_load_2d(dst + C::kQTileBytes + r * C::kQRegionBytes, &p.map_do, r * 64, row, full);
+      }
+      bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
+      bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
     }
-    bulk_load(dst + 2 * C::kQTileBytes, p.lse2 + row, BQ * 4, full);
-    bulk_load(dst + 2 * C::kQTileBytes + BQ * 4, p.delta + row, BQ * 4, full);
     return true;
   };
   if (producer) {
@@ -246,10 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.map_do);
     const uint32_t kvb = smem_u32(&bar_kv);
     mbar_arrive_expect_tx(kvb, 2 * C::kKTileBytes);
-    for (int r = 0; r < C::kRegions; ++r) {
-      tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
-      tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
-    }
+    if (bounds_ok(kv_row + kTile <= rows_kv, p.status, kChkKv))
+      for (int r = 0; r < C::kRegions; ++r) {
+        tma_load_2d(sbase + C::kKOff + r * C::kKRegionBytes, &p.map_k, r * 64, kv_row, kvb);
+        tma_load_2d(sbase + C::kVOff + r * C::kKRegionBytes, &p.map_v, r * 64, kv_row, kvb);
+      }
     while (issued < n && issued < C::kStages && issue_stage(issued)) ++issued;  // free stages
   }
   tc_fence_before();
@@ -411,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         // (three exchange stages) gives lane i chunk i of each of the 8 rows, so
         // that every vector reduction covers 4 whole 128-byte row segments.
         const int gl = lane & 7;
-        float* rows0 = p.dqacc + (static_cast<long long>(step_row(2 * m)) + (r & ~7)) * D;
+        const long long row0 = static_cast<long long>(step_row(2 * m)) + (r & ~7);
+        const bool dq_ok = bounds_ok(row0 + 8 <= rows_q, p.status, kChkDq);
+        float* rows0 = p.dqacc + row0 * D;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[8][4];
@@ -438,9 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           }
           // now x[k] = chunk gl of row (group base + k)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            red_add_v4_f32(rows0 + static_cast<long long>(k) * D + 32 * hf + 4 * gl, x[k][0],
-                           x[k][1], x[k][2], x[k][3]);
+          if (dq_ok)
+            for (int k = 0; k < 8; ++k)
+              red_add_v4_f32(rows0 + static_cast<long long>(k) * D + 32 * hf + 4 * gl, x[k][0],
+                             x[k][1], x[k][2], x[k][3]);
         }
       }
     } else {
@@ -456,12 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dq_free[buf]));
         // lane r = d; columns = the 64 query rows of the step
-        float* base = p.dqacc + static_cast<long long>(step_row(s)) * D + r;
+        const long long srow = step_row(s);
+        if (bounds_ok(srow + BQ <= rows_q, p.status, kChkDq)) {
+          float* base = p.dqacc + srow * D + r;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
+          for (int q = 0; q < 32; ++q) red_add_f32(base + (long long)q * D, __uint_as_float(u0[q]));
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+          for (int q = 0; q < 32; ++q)
+            red_add_f32(base + (long long)(q + 32) * D, __uint_as_float(u1[q]));
+        }
       }
     }
   } else {
@@ -543,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const bool sum_parts = nparts > 1;  // another CTA adds into the same dk/dv rows
     if (n == 0) {
       // no query of the block sees these keys: dk = dv = 0 (summed rows start at 0)
-      if (!sum_parts) {
+      if (!sum_parts && bounds_ok(grow < rows_kv, p.status, kChkDkdv)) {
         float4* dst = reinterpret_cast<float4*>((half == 0 ? p.dv : p.dk) + grow * D);
 #pragma unroll
         for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -577,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         // (dS 2^(edo+ev)) (q~ 2^eq). The cos / sin rows of the tile's keys arrive by TMA.
         if (r == 0) {
           mbar_arrive_expect_tx(smem_u32(&bar_tab), 2 * C::kTabBoxes * C::kBoxBytes);
+          if (bounds_ok(k0p + kTile <= p.tab_rows, p.status, kChkTab))
           for (int bx = 0; bx < C::kTabBoxes; ++bx) {
             tma_load_2d(tcos + bx * C::kBoxBytes, &p.map_cos, bx * 32, k0p, smem_u32(&bar_tab));
             tma_load_2d(tsin + bx * C::kBoxBytes, &p.map_sin, bx * 32, k0p, smem_u32(&bar_tab));
@@ -652,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       named_bar_sync(1 + half, 128);
       if (r == 0) {
         const CUtensorMap* map = half == 0 ? &p.map_dv : &p.map_dk;
+        if (bounds_ok(kv_row + kTile <= rows_kv, p.status, kChkDkdv))
         for (int bx = 0; bx < D / 32; ++bx) {
           if (sum_parts) tma_reduce_add_2d(map, bx * 32, kv_row, stage + bx * C::kBoxBytes);
           else tma_store_2d(map, bx * 32, kv_row, stage + bx * C::kBoxBytes);

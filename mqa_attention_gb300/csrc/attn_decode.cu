@@ -40,7 +40,9 @@ constexpr int kWarpMma = 5;
 
 enum : int {
   kSiteQ = 41, kSiteKvFull = 42, kSiteKvEmpty = 43, kSiteSFull = 44, kSitePFull = 45,
-  kSiteODone = 46, kSiteQRot = 47
+  kSiteODone = 46, kSiteQRot = 47,
+  // index checks of the debug build (a tile may end past the last row: TMA fills it)
+  kChkQ = 53, kChkKv = 54, kChkTab = 55, kChkPart = 56
 };
 
 template <int D>
@@ -135,8 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       tma_prefetch_desc(&p.map_k);
       tma_prefetch_desc(&p.map_v);
       mbar_arrive_expect_tx(smem_u32(&bar_q), C::kTileBytes);
-      for (int r = 0; r < C::kRegions; ++r)
-        tma_load_2d(sbase + r * C::kRegionBytes, &p.map_q, r * 64, q_row0, smem_u32(&bar_q));
+      if (bounds_ok(q_row0 >= 0 && q_row0 < p.rows, p.status, kChkQ))
+        for (int r = 0; r < C::kRegions; ++r)
+          tma_load_2d(sbase + r * C::kRegionBytes, &p.map_q, r * 64, q_row0, smem_u32(&bar_q));
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n && ok; ++j) {
@@ -151,8 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           mbar_arrive_expect_tx(full, C::kTileBytes);
           const CUtensorMap* map = w == 0 ? &p.map_k : &p.map_v;
           const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (kt0 + j) * kTile, full);
+          const long long krow = kv_row0 + static_cast<long long>(kt0 + j) * kTile;
+          if (bounds_ok(krow < static_cast<long long>(p.B) * p.Hkv * p.Skv, p.status, kChkKv))
+            for (int r = 0; r < C::kRegions; ++r)
+              tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (kt0 + j) * kTile, full);
           ++issued;
         }
       }
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       // row's cos / sin values are loaded while the tile is in flight.
       float cv[D / 2], sv[D / 2];
       const long long trow = static_cast<long long>(qpos) * (D / 2);
-      if (row_real) {
+      if (row_real && bounds_ok(qpos < p.tab_rows, p.status, kChkTab)) {
         const float4* cs = reinterpret_cast<const float4*>(p.cos_tab + trow);
         const float4* sn = reinterpret_cast<const float4*>(p.sin_tab + trow);
 #pragma unroll
@@ -386,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
     if (ok) {
       tc_fence_after();
       const long long prow = static_cast<long long>(c) * p.rows + grow;
+      const bool part_ok = bounds_ok(!row_real || prow < p.nchunks * p.rows, p.status, kChkPart);
       float* dst = p.part_out + prow * D;
       const bool seen = n > 0 && l > 0.f;
       const float inv_l = seen ? 1.f / l : 0.f;
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t u[32];
         if (n > 0) tmem_ld32(tmem + lane_base + C::kColO + cc * 32, u);
-        if (row_real) {
+        if (row_real && part_ok) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             reinterpret_cast<float4*>(dst + cc * 32)[i] =
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (row_real) p.part_lse[prow] = seen ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (row_real && part_ok) p.part_lse[prow] = seen ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

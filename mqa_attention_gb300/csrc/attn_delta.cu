@@ -33,7 +33,9 @@ constexpr int kWarpMma = 9;
 
 enum : int {
   kSiteQ = 40, kSiteKvFull = 41, kSiteKvEmpty = 42, kSiteSFull = 43, kSitePFree = 44,
-  kSiteInject = 45
+  kSiteInject = 45,
+  // index checks of the debug build
+  kChkKv = 50, kChkQ = 51, kChkRow = 52
 };
 
 template <int D>
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_delta_kernel(const __grid_co
   const int n = n_0 > n_1 ? n_0 : n_1;
   const int q_row0 = bh * p.S;
   const int kv_row0 = (b * p.Hkv + hkv) * p.S;
+  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.S;
+  const long long rows_kv = static_cast<long long>(p.B) * p.Hkv * p.S;
 
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
@@ -107,8 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_delta_kernel(const __grid_co
     mbar_arrive_expect_tx(full, C::kTileBytes);
     const CUtensorMap* map = (i & 1) == 0 ? &p.map_k : &p.map_v;
     const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
-    for (int r = 0; r < C::kRegions; ++r)
-      tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (i >> 1) * kTile, full);
+    if (bounds_ok(kv_row0 + ((i >> 1) + 1LL) * kTile <= rows_kv, p.status, kChkKv))
+      for (int r = 0; r < C::kRegions; ++r)
+        tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (i >> 1) * kTile, full);
     return true;
   };
   if (producer) {
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_delta_kernel(const __grid_co
     mbar_arrive_expect_tx(smem_u32(&bar_q), 2 * nvalid * C::kTileBytes);
     for (int t = 0; t < 2; ++t) {
       if ((t ? n_1 : n_0) == 0) continue;
+      if (!bounds_ok(q_row0 + (2LL * c + t + 1) * kTile <= rows_q, p.status, kChkQ)) continue;
       for (int r = 0; r < C::kRegions; ++r) {
         tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
                     q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
@@ -219,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_delta_kernel(const __grid_co
     const BwdExponents ex = bwd_exponents(p.maxes);
     // S arrives multiplied by 2^(eq+ek); lse2 = lse log2 e (+inf on padding rows)
     const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
-    const float lse2 = nt > 0 ? p.lse2[row] : 0.f;
+    const bool row_ok = bounds_ok(qt >= nq || row < rows_q, p.status, kChkRow);
+    const float lse2 = nt > 0 && row_ok ? p.lse2[row] : 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < nt; ++j) {
       const bool got = bounded_wait(smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.status, kSiteSFull);
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_delta_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p_free[t]));
     }
-    if (qt < nq) p.delta[row] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    if (qt < nq && row_ok) p.delta[row] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   }
 
   tc_fence_before();

@@ -37,7 +37,9 @@ constexpr int kWarpMma = 9;
 // Wait-site codes reported in the status word.
 enum : int {
   kSiteQ = 1, kSiteKvFull = 2, kSiteKvEmpty = 3, kSiteSFull = 4, kSitePFull = 5,
-  kSiteODone = 6, kSiteInject = 7
+  kSiteODone = 6, kSiteInject = 7,
+  // index checks of the debug build
+  kChkKv = 8, kChkQ = 9, kChkOut = 10, kChkLse = 11
 };
 
 template <int D>
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int kv_valid = p.kv_valid > 0 ? p.kv_valid : p.Skv;  // keys that exist per head
   const int q_row0 = bh * p.Sq;
   const int kv_row0 = (b * p.Hkv + hkv) * p.Skv;
+  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.Sq;  // rows of q~, out, lse
+  const long long rows_kv = static_cast<long long>(p.B) * p.Hkv * p.Skv;
 
   // ---- setup. The producer's lane initialises the barriers and, as soon as the
   // previous kernel's writes are visible, starts the Q loads and fills the K/V ring
@@ -149,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_arrive_expect_tx(full, C::kTileBytes);
     const CUtensorMap* map = (i & 1) == 0 ? &p.map_k : &p.map_v;
     const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
-    for (int r = 0; r < C::kRegions; ++r)
-      tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, kv_row0 + (i >> 1) * kTile, full);
+    const long long row = kv_row0 + (i >> 1) * kTile;
+    if (bounds_ok(row + kTile <= rows_kv, p.status, kChkKv))
+      for (int r = 0; r < C::kRegions; ++r)
+        tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, static_cast<int>(row), full);
     return true;
   };
   if (producer) {
@@ -176,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_arrive_expect_tx(smem_u32(&bar_q), nvalid * C::kTileBytes);
     for (int t = 0; t < 2; ++t) {
       if ((t ? n_1 : n_0) == 0) continue;
+      if (!bounds_ok(q_row0 + (2LL * c + t + 1) * kTile <= rows_q, p.status, kChkQ)) continue;
       for (int r = 0; r < C::kRegions; ++r)
         tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
                     q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
@@ -395,19 +402,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       fence_async_smem();
       named_bar_sync(1 + t, 128);
       if (r == 0) {
-        for (int rg = 0; rg < C::kRegions; ++rg)
-          tma_store_2d(&p.map_out, rg * 64, q_row0 + qt * kTile, obuf + rg * C::kRegionBytes);
+        if (bounds_ok(q_row0 + (qt + 1LL) * kTile <= rows_q, p.status, kChkOut))
+          for (int rg = 0; rg < C::kRegions; ++rg)
+            tma_store_2d(&p.map_out, rg * 64, q_row0 + qt * kTile, obuf + rg * C::kRegionBytes);
         bulk_commit();
         bulk_wait_read_all();
       }
-      p.lse[static_cast<long long>(q_row0) + qt * kTile + r] = (m + log2f(l)) * kLn2;
+      const long long lrow = static_cast<long long>(q_row0) + qt * kTile + r;
+      if (bounds_ok(lrow < rows_q, p.status, kChkLse)) p.lse[lrow] = (m + log2f(l)) * kLn2;
     } else if (qt < nq) {
       // a query tile that sees no key of the block: out = 0, lse = -inf
       const long long row = static_cast<long long>(q_row0) + qt * kTile + r;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * D);
+      if (bounds_ok(row < rows_q, p.status, kChkOut)) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * D);
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-      p.lse[row] = -INFINITY;
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        p.lse[row] = -INFINITY;
+      }
     }
   }
 

@@ -123,6 +123,7 @@ struct RowPrepParams {
   const float* sin_tab;
   const float* cos_lo;   // table lo parts
   const float* sin_lo;
+  int tab_rows;          // positions the table holds
   const float* maxes;  // backward
   const void* out;     // backward, query rows (null: delta is written by the delta pass)
   float* delta;
@@ -140,7 +141,8 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 // nearest even when dq_bf16); row r sits at position pos0 + r % S.
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
                                int Sp, int pos0, int D, float scale, const float* maxes, const float* cos_tab,
-                               const float* sin_tab, int rope_interleaved, cudaStream_t stream);
+                               const float* sin_tab, int tab_rows, int rope_interleaved,
+                               int* status, cudaStream_t stream);
 // Merge of two partial attention results of the same rows (bf16 out, fp32 lse);
 // o / l may be oa / la.
 cudaError_t launch_merge(const void* oa, const float* la, const void* ob, const float* lb, void* o,
@@ -190,6 +192,7 @@ struct BwdParams {
   float* dv;           // [B*Hkv*S][D] fp32
   const float* cos_tab;
   const float* sin_tab;
+  int tab_rows;        // positions the cos / sin tables (and their maps) hold
   int* status;
   int B, Hq, Hkv, Sq, Skv, D;  // query and K/V blocks as in FwdParams
   int q_tile0, kv_tile0;
@@ -246,6 +249,7 @@ struct DecParams {
   const float* sin_lo;
   int rope_interleaved;
   int exact;             // 1: the query rows rounded as the exact rotation rounds
+  int tab_rows;          // positions the table holds
   int* status;
   int B, Hq, Hkv, Sq, Skv, D;
   int q_pos0;

@@ -136,6 +136,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   rp.sin_tab = tabp + tab_n;
   rp.cos_lo = tabp + 2 * tab_n;
   rp.sin_lo = tabp + 3 * tab_n;
+  rp.tab_rows = S;
   rp.seg[0] = {q, qr, nullptr, nullptr, qrows, S, S, 0};
   rp.seg[1] = {k, kr, nullptr, nullptr, krows, S, S, 0};
   ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;

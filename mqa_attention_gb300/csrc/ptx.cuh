@@ -86,8 +86,23 @@ GB_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // status code instead of a hung GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// Device status codes (low byte = site of the wait that gave up).
+// Device status codes (low byte = site of the wait that gave up, or of the check).
 constexpr int kStatusTimeout = 0x100;
+constexpr int kStatusBounds = 0x200;
+
+// Index checks of the debug build (compiled with GB_BOUNDS_CHECK): `ok` states that the
+// global index or TMA coordinate about to be used lies inside its buffer. A failed check
+// records `site` in the status word and returns false, and the caller skips the access
+// (a load that would complete a barrier then leaves it waiting until its time limit).
+// In the normal build every check is true at compile time and costs nothing.
+#ifdef GB_BOUNDS_CHECK
+GB_DEV bool bounds_ok(bool ok, int* status, int site) {
+  if (!ok) atomicCAS(status, 0, kStatusBounds | (site & 0xff));
+  return ok;
+}
+#else
+GB_DEV constexpr bool bounds_ok(bool, int*, int) { return true; }
+#endif
 
 // Waits for the phase with parity `parity` of `bar` to complete. Returns false
 // (without waiting further) once `*abort` is set by any thread of the CTA, or

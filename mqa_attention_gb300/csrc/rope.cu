@@ -24,6 +24,8 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSitePrep = 60;  // status-word site of the pre-pass's wait
+// index checks of the debug build
+constexpr int kChkPrepIn = 61, kChkPrepOut = 62, kChkPrepTab = 63, kChkFinal = 64;
 
 // cos and sin of p * theta^(-2i/D), p < S, i < D/2, evaluated in fp64 and stored as
 // fp32 pairs: hi = fp32(x), lo = fp32(x - hi), so that hi + lo carries about 48
@@ -204,16 +206,27 @@ __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   const long long row0 = is_q ? grow : grow - p.seg[0].rows;
   // Threads past the last row read row 0 of the segment (a valid address), take
   // part in the shuffles below and write nothing.
-  const bool live = row0 < sg.rows;
+  bool live = row0 < sg.rows;
   // output row, its head and row within the head (rows < 2^31: 32-bit division)
   const unsigned ro32 = live ? static_cast<unsigned>(row0) : 0u;
   const unsigned head = ro32 / static_cast<unsigned>(sg.Sp);
   const int i = static_cast<int>(ro32 - head * static_cast<unsigned>(sg.Sp));
   const long long ro = ro32;
   const bool real = !kPad || i < sg.S;  // kPad = false: every output row is an input row
-  const long long ri =  // input row
+  long long ri =  // input row
       !kPad ? ro : (real ? static_cast<long long>(head) * sg.S + i : 0);
-  const int pos = sg.pos0 + (real ? i : 0);
+  int pos = sg.pos0 + (real ? i : 0);
+  {
+    const long long in_rows = kPad ? (sg.rows / sg.Sp) * sg.S : sg.rows;
+    // (threads past the last row read row 0 on purpose and write nothing)
+    const bool ok = gb::bounds_ok(!live || ri < in_rows, p.status, kChkPrepIn) &&
+                    gb::bounds_ok(!live || pos < p.tab_rows, p.status, kChkPrepTab);
+    if (!ok) {  // read row 0 and position 0 instead, write nothing
+      ri = 0;
+      pos = 0;
+      live = false;
+    }
+  }
   const bool inter = p.rope_interleaved != 0;
   const int oa = rope_off_a(c, inter), ob = rope_off_b(c, D, inter);
   const long long e1 = ri * D + oa, e2 = ri * D + ob;  // input elements
@@ -411,8 +424,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) row_prep_exact_kernel(const R
           gb::mbar_arrive_expect_tx(full, 4 * tb);
           const long long te = static_cast<long long>(sg.pos0 + it.p0) * H;
           const float* src[4] = {p.cos_tab, p.sin_tab, p.cos_lo, p.sin_lo};
-          for (int a = 0; a < 4; ++a)
-            gb::bulk_load(gb::smem_u32(tabs + (ts * 4 + a) * C::kTabFloats), src[a] + te, tb, full);
+          if (gb::bounds_ok(sg.pos0 + it.p0 + it.nrows <= p.tab_rows, p.status, kChkPrepTab))
+            for (int a = 0; a < 4; ++a)
+              gb::bulk_load(gb::smem_u32(tabs + (ts * 4 + a) * C::kTabFloats), src[a] + te, tb, full);
           pseg = it.seg;
           pp0 = it.p0;
         }
@@ -430,9 +444,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) row_prep_exact_kernel(const R
         gb::mbar_arrive_expect_tx(full, static_cast<uint32_t>(it.nh) * (ntens * rb + lb));
         uint8_t* stg = stages + st * C::kStageBytes;
         const void* src[3] = {sg.x, x2_in ? sg.x2 : p.out, p.out};
+        const long long in_rows = (sg.rows / sg.Sp) * (kPad ? sg.S : sg.Sp);
         if (rb > 0) {
           for (int k = 0; k < it.nh; ++k) {
             const long long r = static_cast<long long>(it.h0 + k) * (kPad ? sg.S : sg.Sp) + it.p0;
+            if (!gb::bounds_ok(r + it.nreal <= in_rows, p.status, kChkPrepIn)) continue;
             for (int m = 0; m < ntens; ++m)
               gb::bulk_load(gb::smem_u32(stg + ((m * kBlockHeads + k) * C::kRowElems) * 2),
                             static_cast<const __nv_bfloat16*>(src[m]) + r * D, rb, full);
@@ -503,6 +519,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) row_prep_exact_kernel(const R
       const int i = it.p0 + il;  // row within the head
       const bool real = il < it.nreal;
       const long long ro = static_cast<long long>(it.h0 + k) * sg.Sp + i;  // output row
+      if (!gb::bounds_ok(ro < sg.rows, p.status, kChkPrepOut)) continue;
       const long long f1 = ro * D + oa, f2 = ro * D + ob;
       float chi[NP], clo[NP], shi[NP], slo[NP];
 #pragma unroll
@@ -589,7 +606,7 @@ __global__ void __launch_bounds__(256)
     dq_finalize_kernel(const float* __restrict__ dqacc, void* __restrict__ dq, long long rows,
                        int S, int Sp, int pos0, float scale, const float* __restrict__ maxes,
                        const float* __restrict__ cos_tab, const float* __restrict__ sin_tab,
-                       int rope_interleaved) {
+                       int tab_rows, int rope_interleaved, int* status) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
   constexpr int T = D / 16;
@@ -603,6 +620,7 @@ __global__ void __launch_bounds__(256)
   const unsigned head = static_cast<unsigned>(row) / static_cast<unsigned>(S);
   const int i = static_cast<int>(static_cast<unsigned>(row) - head * static_cast<unsigned>(S));
   const int pos = pos0 + i;
+  if (!gb::bounds_ok(pos < tab_rows, status, kChkFinal)) return;
   const bool inter = rope_interleaved != 0;
   const long long racc = static_cast<long long>(head) * Sp + i;
   const long long e1 = row * D + rope_off_a(c, inter);
@@ -790,12 +808,13 @@ cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
 
 cudaError_t launch_dq_finalize(const float* dqacc, void* dq, bool dq_bf16, long long rows, int S,
                                int Sp, int pos0, int D, float scale, const float* maxes, const float* cos_tab,
-                               const float* sin_tab, int rope_interleaved, cudaStream_t stream) {
+                               const float* sin_tab, int tab_rows, int rope_interleaved,
+                               int* status, cudaStream_t stream) {
   const long long threads = rows * (D / 16);
   const unsigned grid = (unsigned)blocks_for(threads);
 #define GB_FIN(DD, BF)                                                                       \
   return launch_pdl(dq_finalize_kernel<DD, BF>, dim3(grid), dim3(256), 0, stream, dqacc, dq, rows, \
-                    S, Sp, pos0, scale, maxes, cos_tab, sin_tab, rope_interleaved)
+                    S, Sp, pos0, scale, maxes, cos_tab, sin_tab, tab_rows, rope_interleaved, status)
   if (D == 128) {
     if (dq_bf16) GB_FIN(128, true);
     else GB_FIN(128, false);
