@@ -62,6 +62,11 @@ def parse():
                     help="RoPE pair layout (interleaved runs attn_fwd_ex / attn_bwd_ex)")
     ap.add_argument("--grads", choices=["fp32", "bf16"], default="fp32",
                     help="gradient dtype (bf16 runs attn_bwd_bf16)")
+    ap.add_argument("--delta", choices=["auto", "exact", "from_out"], default="auto",
+                    help="delta of the backward: attn_bwd's choice, the exact pass over the "
+                         "scores (ATTN_DELTA_EXACT) or dout . out (ATTN_DELTA_FROM_OUT)")
+    ap.add_argument("--exact-rope", action="store_true",
+                    help="rotated q, k rounded as the exact rotation rounds (ATTN_ROPE_EXACT)")
     ap.add_argument("--decode", type=int, default=0, metavar="SQ",
                     help="SQ > 0: time attn_decode, SQ new tokens per sequence against a "
                          "cache of the workload's S keys (HBM-bound: reported in GB/s)")
@@ -342,11 +347,16 @@ L2_NOTE = ("GPU arm: L2 flushed between steps (256 MiB write); the host oracle a
            "device cache")
 
 
-def config_of(wl, n, rope="half", grads="fp32", l2=L2_NOTE):
-    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
-            "rope_theta": wl.theta, "rope": rope, "grads": grads, "causal": wl.causal,
-            "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
-            "l2": l2}
+def config_of(wl, n, rope="half", grads="fp32", l2=L2_NOTE, delta="auto", exact_rope=False):
+    c = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "S": wl.S, "D": wl.D,
+         "rope_theta": wl.theta, "rope": rope, "grads": grads, "causal": wl.causal,
+         "passes": "fwd+bwd" if wl.backward else "fwd", "parallelism": f"replicas x{n}",
+         "l2": l2}
+    if delta != "auto":
+        c["delta"] = delta
+    if exact_rope:
+        c["rope_rounding"] = "exact"
+    return c
 
 
 # ------------------------------------------------------------------ our arm
@@ -356,12 +366,13 @@ def kernel_names(M):
             (M.KERNEL_DQ_FINAL, "dq_finalize"))
 
 
-def launches_per_step(wl):
+def launches_per_step(wl, delta="auto"):
     """Our kernels in one step: RoPE pre-pass + forward; abs-max + pre-pass (+ the exact
-    delta pass for groups above 8) + main + dq finalisation."""
+    delta pass: by default for groups above 8) + main + dq finalisation."""
     if not wl.backward:
         return 2
-    return 2 + 4 + (1 if wl.Hq // wl.Hkv > 8 else 0)
+    exact = delta == "exact" or (delta == "auto" and wl.Hq // wl.Hkv > 8)
+    return 2 + 4 + (1 if exact else 0)
 
 
 def roofline_of(wl, kern, peak_tf, peak_src, value):
@@ -472,22 +483,24 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     dims = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, wl.scale, wl.causal)
-    mode = M.ROPE_MODES[args.rope]
+    mode = M.ROPE_MODES[args.rope] | (M.ROPE_EXACT if args.exact_rope else 0)
+    bmode = mode | M.DELTA_MODES[args.delta]
     dims_ex = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, mode, wl.scale, wl.causal)
+    bdims_ex = (wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.theta, bmode, wl.scale, wl.causal)
 
     def fwd(q_, k_, v_, out_, lse_, st):
-        if args.rope == "half":
+        if mode == 0:
             M.attn_fwd(q_, k_, v_, out_, lse_, *dims, stream=st)
         else:
             M.attn_fwd_ex(q_, k_, v_, out_, lse_, *dims_ex, stream=st)
 
     def bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, st):
         if args.grads == "bf16":
-            M.attn_bwd_bf16(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims_ex, stream=st)
-        elif args.rope == "half":
+            M.attn_bwd_bf16(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *bdims_ex, stream=st)
+        elif bmode == 0:
             M.attn_bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims, stream=st)
         else:
-            M.attn_bwd_ex(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *dims_ex, stream=st)
+            M.attn_bwd_ex(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_, *bdims_ex, stream=st)
 
     def step():
         fwd(q, k, v, out, lse, stream)
@@ -629,7 +642,8 @@ def run_ours(args, rank, world, local):
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_of(wl, host, 10.0)
     others = None
-    if world == 1 and args.rope == "half" and args.grads == "fp32" and not args.single:
+    if (world == 1 and args.rope == "half" and args.grads == "fp32" and args.delta == "auto"
+            and not args.exact_rope and not args.single):
         others = other_workload_lines(args, M, flush, stream, peak_tf, peak_src)
     line = {
         "metric": METRIC,
@@ -637,13 +651,14 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic N(0,1) bf16 q/k/v/dO, seeded (splitmix64 + Box-Muller)",
-        "config": config_of(wl, world, rope=args.rope, grads=args.grads),
+        "config": config_of(wl, world, rope=args.rope, grads=args.grads, delta=args.delta,
+                            exact_rope=args.exact_rope),
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host buffers; each step's inputs in and results out on two "
                           "copy streams over three device buffer sets, overlapped with "
                           "the neighbouring steps' compute"},
-        "gpu_launches": launches_per_step(wl) * args.steps,
+        "gpu_launches": launches_per_step(wl, args.delta) * args.steps,
         "roofline": roof,
         "prologue_roofline": prologue,
         "passes_ms": {k: round(v, 5) for k, v in passes.items()},
@@ -743,9 +758,7 @@ def run_blocks(args, rank, world, local):
     M.profile_end()
     status = M.sync_status()
     kern = {}
-    for kind, name in ((M.KERNEL_ROPE, "rope"), (M.KERNEL_FWD, "attn_fwd"),
-                       (M.KERNEL_BWD_PREP, "bwd_prep"), (M.KERNEL_BWD_MAIN, "attn_bwd_main"),
-                       (M.KERNEL_DQ_FINAL, "dq_finalize")):
+    for kind, name in kernel_names(M):
         n, tot = M.profile_query(kind)
         if n:
             kern[name] = tot / args.steps  # ms per step over all blocks
