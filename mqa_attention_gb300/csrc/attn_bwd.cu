@@ -59,6 +59,7 @@ constexpr int kWarpMma = 13;
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
   kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteTab = 26,
+  kSiteKvTmem = 33,
   // index checks of the debug build
   kChkStage = 27, kChkKv = 28, kChkDq = 29, kChkDkdv = 30, kChkTab = 31
 };
@@ -72,7 +73,13 @@ struct BwdCfg {
   static constexpr int kQRegionBytes = BQ * 128;   // 64 query rows x 128 B
   static constexpr int kKTileBytes = kRegions * kKRegionBytes;
   static constexpr int kQTileBytes = kRegions * kQRegionBytes;
-  static constexpr int kStages = 3;
+  // D = 64: K~ and V also sit in tensor memory (packed fp16, the free 64 columns), so
+  // that the score products Sᵀ = K~ Q~ᵀ and dPᵀ = V dOᵀ read their A operand from
+  // there rather than from shared memory, whose bandwidth the N = 64 products
+  // otherwise spend on re-reading K~ and V every step; the freed bandwidth also buys a
+  // fourth Q~/dO stage.
+  static constexpr bool kKvTmem = D == 64;
+  static constexpr int kStages = kKvTmem ? 4 : 3;
   static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int kDsBufs = kDqPair ? 4 : 2;  // dSᵀ buffers (pairs stay adjacent)
   static constexpr int kDsBytes = 16384;           // dSᵀ: 128 key rows x 64 queries fp16
@@ -86,7 +93,9 @@ struct BwdCfg {
   static constexpr uint32_t kColDQ = 256;  // D = 64 only
   static constexpr uint32_t kColDV = kDqPair ? 320 : 256;
   static constexpr uint32_t kColDK = 384;
-  static_assert(kColDK + D <= 512, "TMEM budget");
+  static constexpr uint32_t kColKt = 448;  // D = 64: K~ rows, 32 columns of fp16 pairs
+  static constexpr uint32_t kColVt = 480;  // D = 64: V rows
+  static_assert(kColDK + D <= (kKvTmem ? kColKt : 512u), "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // Epilogue staging, in the shared memory the main loop used: the cos and sin rows
   // of the tile's keys, then dV and dK, as 128-byte swizzled boxes of 32 fp32
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never, bar_tab;
+  __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never, bar_tab, bar_kvt;
   __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
   __shared__ uint32_t tmem_slot;
@@ -236,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(smem_u32(&bar_drain), 1);
     mbar_init(smem_u32(&bar_never), 1);
     mbar_init(smem_u32(&bar_tab), 1);
+    mbar_init(smem_u32(&bar_kvt), 256);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_stage_full[s]), 1);
       mbar_init(smem_u32(&bar_stage_empty[s]), 1);
@@ -303,8 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
         const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
-        mma_ss_w(tmem + C::col_st(s & 1), desc(kKmaj, kaddr + ok_), desc(kKmaj, qaddr + oq),
-                 idesc_st, kk > 0);
+        if constexpr (C::kKvTmem)  // 16 d per product: 8 columns of fp16 pairs
+          mma_ts_w(tmem + C::col_st(s & 1), tmem + C::kColKt + kk * 8, desc(kKmaj, qaddr + oq),
+                   idesc_st, kk > 0);
+        else
+          mma_ss_w(tmem + C::col_st(s & 1), desc(kKmaj, kaddr + ok_), desc(kKmaj, qaddr + oq),
+                   idesc_st, kk > 0);
       }
     };
     auto issue_dp = [&](int s) {
@@ -313,8 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ok_ = (kk >> 2) * C::kKRegionBytes + (kk & 3) * 32;
         const uint32_t oq = (kk >> 2) * C::kQRegionBytes + (kk & 3) * 32;
-        mma_ss_w(tmem + C::col_dpt(s & 1), desc(kKmaj, vaddr + ok_), desc(kKmaj, doaddr + oq),
-                 idesc_st, kk > 0);
+        if constexpr (C::kKvTmem)
+          mma_ts_w(tmem + C::col_dpt(s & 1), tmem + C::kColVt + kk * 8, desc(kKmaj, doaddr + oq),
+                   idesc_st, kk > 0);
+        else
+          mma_ss_w(tmem + C::col_dpt(s & 1), desc(kKmaj, vaddr + ok_), desc(kKmaj, doaddr + oq),
+                   idesc_st, kk > 0);
       }
     };
     auto issue_dvdk = [&](int s, bool first) {
@@ -349,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     if (p.inject_timeout)  // nothing ever arrives on bar_never
       ok = wait(smem_u32(&bar_never), 0, kSiteInject);
     ok = ok && wait(smem_u32(&bar_kv), 0, kSiteKv);
+    if constexpr (C::kKvTmem) ok = ok && wait(smem_u32(&bar_kvt), 0, kSiteKvTmem);
     for (int s = 0; s < 2 && s < n && ok; ++s) {
       ok = wait(smem_u32(&bar_stage_full[s]), 0, kSiteStageFull);
       if (!ok) break;
@@ -486,6 +505,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const float sl2 = p.scale_log2 * exp2i(-(ex.q + ex.k));
     const int key = k0p + r;  // this thread's key position
     const int qb = half * 32;  // this half's first query column
+    if constexpr (C::kKvTmem) {
+      // row r of K~ (warps 0-3) or V (warps 4-7) from its swizzled tile into this
+      // thread's tensor-memory lane: 64 fp16 values as 32 columns of pairs
+      if (bounded_wait(smem_u32(&bar_kv), 0, abort_ptr, p.status, kSiteKv)) {
+        const uint32_t src = sbase + (half == 0 ? C::kKOff : C::kVOff);
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          ld_shared_v4(src + sw128_offset(r, c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        tmem_st32(tmem + lane_base + (half == 0 ? C::kColKt : C::kColVt), w);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_kvt));
+    }
     for (int s = 0; s < n; ++s) {
       const int buf = s & 1;
       const bool got = bounded_wait(smem_u32(&bar_s_full[buf]), (s >> 1) & 1, abort_ptr, p.status,

@@ -11,8 +11,9 @@
 // rescales the partial output when m grows; the final out = O / l and
 // lse = m + ln l equal the plain definition up to rounding.
 //
-// GB300 design: one CTA owns two 128-row query tiles (2c, 2c+1) of one head and
-// streams the 128-key K/V tiles of its KV head through a TMA ring. Warp roles:
+// GB300 design: at D = 128 one CTA owns two 128-row query tiles (2c, 2c+1) of one
+// head and streams the 128-key K/V tiles of its KV head through a TMA ring. Warp
+// roles:
 //   warps 0-3 / 4-7  softmax for query tile 0 / 1 (one thread per row),
 //   warp 8           TMA producer (Q once, then K_j, V_j into the ring),
 //   warp 9           tcgen05 MMA issuer (one thread) and TMEM owner.
@@ -21,6 +22,12 @@
 // and consumed from TMEM by the P.V MMA. While one tile's softmax runs, the
 // tensor core works on the other tile's MMAs. KV tiles above the diagonal are
 // never loaded; only the diagonal tile is masked.
+// At D = 64 a CTA owns one query tile (warps 0-3 softmax, 4 producer, 5 MMA; 256
+// TMEM columns: S, then O) and two CTAs share an SM: the tensor core alternates
+// between their tiles as it does between the two tiles of one CTA at D = 128, and one
+// CTA's start (Q landing, first scores) and epilogue overlap the other's steps. The
+// D = 64 CTAs are short (a few K/V tiles at the sequence lengths this serves), so
+// those fixed parts would otherwise be a large share of their time.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -30,9 +37,6 @@ namespace {
 using namespace gb;
 
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kThreads = 320;
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
 
 // Wait-site codes reported in the status word.
 enum : int {
@@ -44,14 +48,22 @@ enum : int {
 
 template <int D>
 struct FwdCfg {
+  static constexpr int kTiles = D == 128 ? 2 : 1;      // query tiles per CTA
+  static constexpr int kThreads = 128 * kTiles + 64;   // softmax warps, producer, MMA
+  static constexpr int kWarpLoad = 4 * kTiles;
+  static constexpr int kWarpMma = 4 * kTiles + 1;
+  static constexpr int kMinBlocks = 3 - kTiles;        // CTAs per SM the launch asks for
+  static constexpr uint32_t kTmemCols = 256u * kTiles;
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 B (64 bf16)
   static constexpr int kRegions = D / 64;
   static constexpr int kTileBytes = kRegions * kRegionBytes;
-  static constexpr int kSlots = D == 128 ? 5 : 10;     // K/V ring depth (tiles)
-  static constexpr int kKvOff = 2 * kTileBytes;        // after Q_0, Q_1
+  static constexpr int kSlots = 5;                     // K/V ring depth (tiles)
+  static constexpr int kKvOff = kTiles * kTileBytes;   // after the Q tiles
   static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
-  __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
-  __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? D : 0); }
+  __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __device__ static constexpr uint32_t col_o(int t) { return 128u * kTiles + D * t; }
+  static_assert(col_o(kTiles - 1) + D <= kTmemCols, "TMEM budget");
+  static_assert(kMinBlocks * (kSmemBytes + 1024) <= 233472, "shared memory per SM");
 };
 
 // Packed fp32 pairs (fma.rn.f32x2 / add.rn.f32x2: one instruction for two lanes'
@@ -92,12 +104,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
+    attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
+  constexpr int kTiles = C::kTiles;
+  constexpr int kWarpLoad = C::kWarpLoad;
+  constexpr int kWarpMma = C::kWarpMma;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_drain, bar_never;
   __shared__ __align__(8) uint64_t bar_kv_full[C::kSlots], bar_kv_empty[C::kSlots];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_done[2];
+  __shared__ __align__(8) uint64_t bar_s_full[kTiles], bar_p_full[kTiles], bar_o_done[kTiles];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -106,20 +122,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int lane = tid & 31;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
 
-  // ---- work item: heaviest query-tile pairs first
+  // ---- work item: the query tiles kTiles c .. kTiles c + kTiles - 1 of one head,
+  // heaviest first
   const int nq = p.Sq / kTile;
   const int nkv = p.Skv / kTile;
-  const int npairs = (nq + 1) / 2;
+  const int nitems = (nq + kTiles - 1) / kTiles;
   const int BH = p.B * p.Hq;
-  const int c = npairs - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int c = nitems - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / p.Hq;
   const int h = bh % p.Hq;
   const int hkv = h / (p.Hq / p.Hkv);
-  // KV tiles seen by query tile 2c + t: those at or before its position when
+  // KV tiles seen by query tile kTiles c + t: those at or before its position when
   // causal (0 when that tile is past the end, or precedes the whole K/V block)
   auto tiles_of = [&](int t) {
-    const int qt = 2 * c + t;
+    if (t >= kTiles) return 0;
+    const int qt = kTiles * c + t;
     if (qt >= nq) return 0;
     if (!p.causal) return nkv;
     const int vis = p.q_tile0 + qt - p.kv_tile0 + 1;
@@ -138,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // previous kernel's writes are visible, starts the Q loads and fills the K/V ring
   // while the MMA warp allocates tensor memory.
   if (warp == kWarpMma) {
-    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   const bool producer = warp == kWarpLoad && lane == 0;
@@ -168,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(smem_u32(&bar_kv_full[s]), 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
     }
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < kTiles; ++t) {
       mbar_init(smem_u32(&bar_s_full[t]), 1);
       mbar_init(smem_u32(&bar_p_full[t]), 128);
       mbar_init(smem_u32(&bar_o_done[t]), 1);
@@ -180,12 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.map_v);
     const int nvalid = (n_0 > 0) + (n_1 > 0);
     mbar_arrive_expect_tx(smem_u32(&bar_q), nvalid * C::kTileBytes);
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < kTiles; ++t) {
       if ((t ? n_1 : n_0) == 0) continue;
-      if (!bounds_ok(q_row0 + (2LL * c + t + 1) * kTile <= rows_q, p.status, kChkQ)) continue;
+      if (!bounds_ok(q_row0 + (static_cast<long long>(kTiles) * c + t + 1) * kTile <= rows_q,
+                     p.status, kChkQ))
+        continue;
       for (int r = 0; r < C::kRegions; ++r)
         tma_load_2d(sbase + t * C::kTileBytes + r * C::kRegionBytes, &p.map_q, r * 64,
-                    q_row0 + (2 * c + t) * kTile, smem_u32(&bar_q));
+                    q_row0 + (kTiles * c + t) * kTile, smem_u32(&bar_q));
     }
     while (issued < 2 * n && issued < C::kSlots && issue_kv(issued)) ++issued;  // free slots
   }
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ok = ok && n > 0 && wait_kv(0);  // n = 0: both query tiles see no key of the block
     if (ok) {
       tc_fence_after();
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < kTiles; ++t) {
         if ((t ? n_1 : n_0) == 0) continue;
         issue_qk(t, slot_addr(0));
         mma_commit_w(smem_u32(&bar_s_full[t]));
@@ -263,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool next = j + 1 < n;
       ok = wait_kv(iv) && (!next || wait_kv(ik));
       if (!ok) break;
-      for (int t = 0; t < 2 && ok; ++t) {
+      for (int t = 0; t < kTiles && ok; ++t) {
         const int nt = t ? n_1 : n_0;
         if (j >= nt) continue;
         ok = wait(smem_u32(&bar_p_full[t]), j & 1, kSitePFull);
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tS = tmem + lane_base + C::col_s(t);
     const uint32_t tO = tmem + lane_base + C::col_o(t);
     const int nt = t ? n_1 : n_0;
-    const int qt = 2 * c + t;
+    const int qt = kTiles * c + t;
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running maximum, base-2 units (scores * scale * log2 e)
     float l = 0.f;        // running sum of 2^(score2 - m)
@@ -426,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -437,8 +457,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nq = p.Sq / kTile;
-  const unsigned grid = static_cast<unsigned>(((nq + 1) / 2) * p.B * p.Hq);
-  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, p);
+  const unsigned grid = static_cast<unsigned>(((nq + C::kTiles - 1) / C::kTiles) * p.B * p.Hq);
+  return launch_pdl(attn_fwd_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }
 
 }  // namespace
