@@ -367,12 +367,13 @@ def kernel_names(M):
 
 
 def launches_per_step(wl, delta="auto"):
-    """Our kernels in one step: RoPE pre-pass + forward; abs-max + pre-pass (+ the exact
-    delta pass: by default for groups above 8) + main + dq finalisation."""
+    """Our kernels in one step: RoPE pre-pass + forward; zeroing of the abs-max words +
+    abs-max + pre-pass (+ the exact delta pass: by default for groups above 8) + main +
+    dq finalisation."""
     if not wl.backward:
         return 2
     exact = delta == "exact" or (delta == "auto" and wl.Hq // wl.Hkv > 8)
-    return 2 + 4 + (1 if exact else 0)
+    return 2 + 5 + (1 if exact else 0)
 
 
 def roofline_of(wl, kern, peak_tf, peak_src, value):
@@ -778,9 +779,9 @@ def run_blocks(args, rank, world, local):
                        block_pairs=len(pairs)),
         "e2e": None,
         "note": "block schedule through the partial entry points; device time only",
-        # per pair: RoPE pre-pass + forward (+ merge), abs-max + pre-pass + main +
-        # dq finalisation
-        "gpu_launches": (2 * nfwd + (nfwd - nb) + 4 * nfwd) * args.steps,
+        # per pair: RoPE pre-pass + forward (+ merge), zeroing + abs-max + pre-pass +
+        # main + dq finalisation
+        "gpu_launches": (2 * nfwd + (nfwd - nb) + 5 * nfwd) * args.steps,
         "roofline": {"bound": "tensor", "kernel": "attn_bwd_main", "achieved": achieved,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "traffic": None, "peak_source": f"{peak_src} bf16 dense (burst)"},

@@ -731,7 +731,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     ap.x[gbattn::kMaxV] = v; ap.n[gbattn::kMaxV] = krows * D;
     ap.x[gbattn::kMaxDO] = dout; ap.n[gbattn::kMaxDO] = qrows * D;
     ap.maxes = maxes;
-    ok = cudaMemsetAsync(maxes, 0, 4 * sizeof(float), stream) == cudaSuccess &&
+    ok = gbattn::launch_zero_words(maxes, 4, stream) == cudaSuccess &&
          gbattn::launch_absmax(ap, stream) == cudaSuccess;
     gbattn::RowPrepParams rp{};
     rp.status = d->status;

@@ -96,6 +96,7 @@ struct AbsMaxParams {
   int blk0[5];     // CTAs [blk0[t], blk0[t+1]) read tensor t (set by launch_absmax)
 };
 cudaError_t launch_absmax(const AbsMaxParams& p, cudaStream_t stream);
+cudaError_t launch_zero_words(void* w, int n, cudaStream_t stream);  // n <= 32
 
 // Row pre-pass over the query rows (segment 0) and key rows (segment 1) of one
 // call, in one launch. Forward (bwd == 0): y = bf16(R x) for both segments.

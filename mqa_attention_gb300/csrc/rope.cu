@@ -757,6 +757,19 @@ cudaError_t launch_absmax(const AbsMaxParams& p_in, cudaStream_t stream) {
                     0, stream, p);
 }
 
+// Zeroes n <= 32 words (the abs-max pass's maxima) as a launch of its own: a memset
+// node between two kernels would hold back the abs-max pass's programmatic early start.
+__global__ void zero_words_kernel(uint32_t* __restrict__ w, int n) {
+  gb::pdl_wait();  // the previous kernel in the stream has completed
+  gb::pdl_launch_dependents();
+  if (static_cast<int>(threadIdx.x) < n) w[threadIdx.x] = 0u;
+}
+
+cudaError_t launch_zero_words(void* w, int n, cudaStream_t stream) {
+  if (n <= 0 || n > 32) return cudaErrorInvalidValue;
+  return launch_pdl(zero_words_kernel, dim3(1), dim3(32), 0, stream, static_cast<uint32_t*>(w), n);
+}
+
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream) {
   const bool pad = p.seg[0].S != p.seg[0].Sp || p.seg[1].S != p.seg[1].Sp;
   if (!p.exact) {
