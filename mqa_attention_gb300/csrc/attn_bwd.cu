@@ -44,6 +44,8 @@
 // the scales are undone in the epilogues.
 // Warp roles: 0-7 softmax (two 32-query halves), 8-11 dQ drain, 12 TMA
 // producer, 13 MMA issuer (whole warp, one elected lane issues) and TMEM owner.
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -465,11 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             }
           }
           // now x[k] = chunk gl of row (group base + k)
+          if (dq_ok) {
 #pragma unroll
-          if (dq_ok)
             for (int k = 0; k < 8; ++k)
               red_add_v4_f32(rows0 + static_cast<long long>(k) * D + 32 * hf + 4 * gl, x[k][0],
                              x[k][1], x[k][2], x[k][3]);
+          }
         }
       }
     } else {
@@ -535,37 +538,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       tmem_ld32x2(tmem + lane_base + C::col_st(buf) + qb, tmem + lane_base + C::col_dpt(buf) + qb,
                   sv, dpv);
       uint32_t pk[16], dk[16];
-      // keys after the query are masked on the diagonal steps only
+      // keys after the query are masked on the diagonal steps only: query columns
+      // below lim; the other steps take the loop without the selects
       const int lim = (p.causal && q0 < k0p + kTile) ? key - q0 - qb : -1;
+      auto columns = [&](auto masked) {
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const float4 l4 = lse4[g];
-        const float4 d4 = del4[g];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pr[4], dsv[4];
+        for (int g = 0; g < 8; ++g) {
+          const float4 l4 = lse4[g];
+          const float4 d4 = del4[g];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], dsv[4];
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {  // two query columns per packed f32x2 operation
-          const float2 x = ffma2(make_float2(__uint_as_float(sv[4 * g + e]),
-                                             __uint_as_float(sv[4 * g + e + 1])),
-                                 make_float2(sl2, sl2), make_float2(-lv[e], -lv[e + 1]));
-          float2 pv = make_float2(ex2(x.x), ex2(x.y));
-          pv.x = (4 * g + e < lim) ? 0.f : pv.x;
-          pv.y = (4 * g + e + 1 < lim) ? 0.f : pv.y;
-          const float2 dp = fsub2(make_float2(__uint_as_float(dpv[4 * g + e]),
-                                              __uint_as_float(dpv[4 * g + e + 1])),
-                                  make_float2(dl[e], dl[e + 1]));
-          const float2 ds = fmul2(pv, dp);
-          pr[e] = pv.x;
-          pr[e + 1] = pv.y;
-          dsv[e] = ds.x;
-          dsv[e + 1] = ds.y;
+          for (int e = 0; e < 4; e += 2) {  // two query columns per packed f32x2 operation
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[4 * g + e]),
+                                               __uint_as_float(sv[4 * g + e + 1])),
+                                   make_float2(sl2, sl2), make_float2(-lv[e], -lv[e + 1]));
+            float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            if constexpr (decltype(masked)::value) {
+              pv.x = (4 * g + e < lim) ? 0.f : pv.x;
+              pv.y = (4 * g + e + 1 < lim) ? 0.f : pv.y;
+            }
+            const float2 dp = fsub2(make_float2(__uint_as_float(dpv[4 * g + e]),
+                                                __uint_as_float(dpv[4 * g + e + 1])),
+                                    make_float2(dl[e], dl[e + 1]));
+            const float2 ds = fmul2(pv, dp);
+            pr[e] = pv.x;
+            pr[e + 1] = pv.y;
+            dsv[e] = ds.x;
+            dsv[e + 1] = ds.y;
+          }
+          pk[2 * g] = pack_fp16(pr[0], pr[1]);
+          pk[2 * g + 1] = pack_fp16(pr[2], pr[3]);
+          dk[2 * g] = pack_fp16(dsv[0], dsv[1]);
+          dk[2 * g + 1] = pack_fp16(dsv[2], dsv[3]);
         }
-        pk[2 * g] = pack_fp16(pr[0], pr[1]);
-        pk[2 * g + 1] = pack_fp16(pr[2], pr[3]);
-        dk[2 * g] = pack_fp16(dsv[0], dsv[1]);
-        dk[2 * g + 1] = pack_fp16(dsv[2], dsv[3]);
-      }
+      };
+      if (__any_sync(0xffffffffu, lim > 0)) columns(std::true_type{});
+      else columns(std::false_type{});
       // Pᵀ and dSᵀ over this half's own (already read) Sᵀ columns. The previous
       // readers of these TMEM columns and of this step's dSᵀ shared-memory buffer
       // belong to earlier steps whose MMAs were issued before Sᵀ(s), so they had
