@@ -53,6 +53,7 @@ FWD_CASES = [
     (1, 4, 2, 256, 384, 128, 384, 0, True),    # keys all before the queries: no mask
     (1, 4, 1, 256, 256, 64, 256, 256, True),   # the diagonal block
     (1, 2, 2, 384, 256, 128, 0, 128, True),    # keys partly after: query tile 0 sees none
+    (1, 2, 2, 384, 256, 64, 0, 128, True),     # the same at D = 64 (one query tile per CTA)
     (2, 8, 1, 128, 512, 64, 1024, 256, False),  # non-causal, offset positions
 ]
 
@@ -74,11 +75,12 @@ def test_forward_partial(B, Hq, Hkv, Sq, Skv, D, qp, kp, causal):
     assert (out.double().cpu()[empty] == 0).all()
 
 
-def test_backward_partial_with_empty_tiles():
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_partial_with_empty_tiles(D):
     """A key block partly after the query block, given the oracle's out and lse."""
-    B, Hq, Hkv, Sq, Skv, D, qp, kp = 1, 4, 2, 384, 256, 128, 0, 128
-    theta, scale = 500000.0, 128 ** -0.5
-    dev, f = tensors(321, {"q": (B, Hq, Sq, D), "k": (B, Hkv, Skv, D), "v": (B, Hkv, Skv, D),
+    B, Hq, Hkv, Sq, Skv, qp, kp = 1, 4, 2, 384, 256, 0, 128
+    theta, scale = (10000.0 if D == 64 else 500000.0), D ** -0.5
+    dev, f = tensors(321 + D, {"q": (B, Hq, Sq, D), "k": (B, Hkv, Skv, D), "v": (B, Hkv, Skv, D),
                            "dout": (B, Hq, Sq, D)})
     wo, wl = O.attention_forward_partial(f["q"], f["k"], f["v"], scale, theta, qp, kp, True,
                                          round_rotated=True)
