@@ -22,8 +22,8 @@
 // dK / dV in shared memory and writes (or adds) them as TMA tiles.
 //
 // Per step s (buffer b = s & 1), in TMEM:
-//   Sᵀ_b  = K~ Q~ᵀ  [128 keys x 64 queries]   (SS MMA)
-//   dPᵀ_b = V dOᵀ   [128 keys x 64 queries]   (SS MMA)
+//   Sᵀ_b  = K~ Q~ᵀ  [128 keys x 64 queries]   (SS MMA; D = 64: TS, K~ from TMEM)
+//   dPᵀ_b = V dOᵀ   [128 keys x 64 queries]   (SS MMA; D = 64: TS, V from TMEM)
 //   softmax warps: Pᵀ = 2^(Sᵀ scale log2e - lse2), dSᵀ = Pᵀ (dPᵀ - delta), packed as
 //     fp16 back over the step's own Sᵀ columns (softmax half h: Pᵀ at
 //     [128b+32h, +16), dSᵀ at [128b+32h+16, +16)); dSᵀ also to shared memory
@@ -36,7 +36,10 @@
 // reductions. Two (Sᵀ, dPᵀ) buffers let the score MMAs of step s+2 run while
 // the softmax of step s+1 works.
 // TMEM columns: Sᵀ_0 [0,64) dPᵀ_0 [64,128) Sᵀ_1 [128,192) dPᵀ_1 [192,256), then
-//   D = 128: dV [256,384) dK [384,512);  D = 64: dQ [256,320) dV [320,384) dK [384,448).
+//   D = 128: dV [256,384) dK [384,512);
+//   D = 64:  dQ [256,320) dV [320,384) dK [384,448), K~ [448,480) V [480,512) (fp16
+//            pairs, copied from shared memory by the softmax warps at the start).
+// Q~/dO tiles (with lse2 and delta) arrive through a TMA ring of 3 stages (4 at D = 64).
 // All products run in fp16 (kind::f16 with fp16 A and B): the operands q~, k~,
 // v, dO arrive from the pre-pass multiplied by exact powers of two (q~ and k~
 // hold their bf16-rounded values, so the recomputed scores equal the

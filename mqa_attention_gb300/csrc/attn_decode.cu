@@ -64,7 +64,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D>
+// kExact: the Q rows are rotated with the exactly rounded rotation (ATTN_ROPE_EXACT);
+// a separate instantiation, so that the default kernel's code holds none of it.
+template <int D, bool kExact>
 __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -245,11 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           cv[4 * i] = a.x; cv[4 * i + 1] = a.y; cv[4 * i + 2] = a.z; cv[4 * i + 3] = a.w;
           sv[4 * i] = bq.x; sv[4 * i + 1] = bq.y; sv[4 * i + 2] = bq.z; sv[4 * i + 3] = bq.w;
         }
-        // the lo parts are read group by group below: bring their lines to L1 now
+        // exact rounding reads the lo parts group by group below: bring their lines to
+        // L1 now
+        if constexpr (kExact) {
 #pragma unroll
-        for (int i = 0; i < D / 2; i += 32) {
-          asm volatile("prefetch.global.L1 [%0];" ::"l"(p.cos_lo + trow + i));
-          asm volatile("prefetch.global.L1 [%0];" ::"l"(p.sin_lo + trow + i));
+          for (int i = 0; i < D / 2; i += 32) {
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p.cos_lo + trow + i));
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p.sin_lo + trow + i));
+          }
         }
       }
       ok = __all_sync(0xffffffffu, bounded_wait(smem_u32(&bar_q), 0, abort_ptr, p.status, kSiteQ));
@@ -277,24 +282,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode_kernel(const __grid_c
           // interleaved: columns [16g, +16) hold the pairs of frequencies 8g + k
           uint4* pa = chunk(rope_off_a(g, p.rope_interleaved != 0));
           uint4* pb = chunk(rope_off_b(g, D, p.rope_interleaved != 0));
-          float a[8], bb[8], c8[8], s8[8], cl8[8], sl8[8];
+          float a[8], bb[8], c8[8], s8[8];
           unpack(*pa, a);
           unpack(*pb, bb);
-          const float4* clo = reinterpret_cast<const float4*>(p.cos_lo + trow + 8 * g);
-          const float4* slo = reinterpret_cast<const float4*>(p.sin_lo + trow + 8 * g);
-          const float4 c0 = __ldg(clo), c1 = __ldg(clo + 1), s0 = __ldg(slo), s1 = __ldg(slo + 1);
-          cl8[0] = c0.x; cl8[1] = c0.y; cl8[2] = c0.z; cl8[3] = c0.w;
-          cl8[4] = c1.x; cl8[5] = c1.y; cl8[6] = c1.z; cl8[7] = c1.w;
-          sl8[0] = s0.x; sl8[1] = s0.y; sl8[2] = s0.z; sl8[3] = s0.w;
-          sl8[4] = s1.x; sl8[5] = s1.y; sl8[6] = s1.z; sl8[7] = s1.w;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             c8[k] = cv[8 * g + k];
             s8[k] = sv[8 * g + k];
           }
           float ya[8], yb[8];
-          if (p.exact) rope_rotate16_exact(a, bb, c8, cl8, s8, sl8, p.rope_interleaved != 0, ya, yb);
-          else rope_rotate16(a, bb, c8, s8, p.rope_interleaved != 0, 1.f, ya, yb);
+          if constexpr (kExact) {
+            float cl8[8], sl8[8];
+            const float4* clo = reinterpret_cast<const float4*>(p.cos_lo + trow + 8 * g);
+            const float4* slo = reinterpret_cast<const float4*>(p.sin_lo + trow + 8 * g);
+            const float4 c0 = __ldg(clo), c1 = __ldg(clo + 1), s0 = __ldg(slo), s1 = __ldg(slo + 1);
+            cl8[0] = c0.x; cl8[1] = c0.y; cl8[2] = c0.z; cl8[3] = c0.w;
+            cl8[4] = c1.x; cl8[5] = c1.y; cl8[6] = c1.z; cl8[7] = c1.w;
+            sl8[0] = s0.x; sl8[1] = s0.y; sl8[2] = s0.z; sl8[3] = s0.w;
+            sl8[4] = s1.x; sl8[5] = s1.y; sl8[6] = s1.z; sl8[7] = s1.w;
+            rope_rotate16_exact(a, bb, c8, cl8, s8, sl8, p.rope_interleaved != 0, ya, yb);
+          } else {
+            rope_rotate16(a, bb, c8, s8, p.rope_interleaved != 0, 1.f, ya, yb);
+          }
           *pa = pack(ya);
           *pb = pack(yb);
         }
@@ -509,14 +518,21 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecPa
   if (e == 0) p.lse[row] = a.ws > 0.f ? a.m + logf(a.ws) : -INFINITY;
 }
 
-template <int D>
-cudaError_t launch_decode_d(const DecParams& p, cudaStream_t stream) {
+template <int D, bool kExact>
+cudaError_t launch_decode_chunks(const DecParams& p, cudaStream_t stream) {
   using C = DecCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, kExact>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attn_decode_kernel<D>, dim3(static_cast<unsigned>(p.nchunks * p.B * p.Hkv)),
-                 dim3(kThreads), C::kSmemBytes, stream, p);
+  return launch_pdl(attn_decode_kernel<D, kExact>,
+                    dim3(static_cast<unsigned>(p.nchunks * p.B * p.Hkv)), dim3(kThreads),
+                    C::kSmemBytes, stream, p);
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecParams& p, cudaStream_t stream) {
+  cudaError_t e = p.exact ? launch_decode_chunks<D, true>(p, stream)
+                          : launch_decode_chunks<D, false>(p, stream);
   if (e != cudaSuccess) return e;
   const long long mthreads = p.rows * (D / 8) * kMergeL;
   return launch_pdl(decode_merge_kernel<D>,
