@@ -146,6 +146,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
   const int n_0 = tiles_of(0);
   const int n_1 = tiles_of(1);
   const int n = n_0 > n_1 ? n_0 : n_1;
+  // The K/V tiles stream from the last visible one down to tile 0: stream position j
+  // holds K/V tile n - 1 - j, and query tile t (which sees tiles 0 .. n_t - 1) joins at
+  // position n - n_t with its diagonal tile. Tile 2c+1 sees one tile more than 2c, so
+  // its extra step comes first and both tiles end on tile 0 together: the CTA's two
+  // epilogues run side by side instead of one waiting for the other's last step.
+  auto start_of = [&](int t) { return n - (t ? n_1 : n_0); };
   const int kv_valid = p.kv_valid > 0 ? p.kv_valid : p.Skv;  // keys that exist per head
   const int q_row0 = bh * p.Sq;
   const int kv_row0 = (b * p.Hkv + hkv) * p.Skv;
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
     mbar_arrive_expect_tx(full, C::kTileBytes);
     const CUtensorMap* map = (i & 1) == 0 ? &p.map_k : &p.map_v;
     const uint32_t dst = sbase + C::kKvOff + slot * C::kTileBytes;
-    const long long row = kv_row0 + (i >> 1) * kTile;
+    const long long row = kv_row0 + static_cast<long long>(n - 1 - (i >> 1)) * kTile;
     if (bounds_ok(row + kTile <= rows_kv, p.status, kChkKv))
       for (int r = 0; r < C::kRegions; ++r)
         tma_load_2d(dst + r * C::kRegionBytes, map, r * 64, static_cast<int>(row), full);
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
     if (ok) {
       tc_fence_after();
       for (int t = 0; t < kTiles; ++t) {
-        if ((t ? n_1 : n_0) == 0) continue;
+        if ((t ? n_1 : n_0) == 0 || start_of(t) > 0) continue;
         issue_qk(t, slot_addr(0));
         mma_commit_w(smem_u32(&bar_s_full[t]));
       }
@@ -285,13 +291,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
       if (!ok) break;
       for (int t = 0; t < kTiles && ok; ++t) {
         const int nt = t ? n_1 : n_0;
-        if (j >= nt) continue;
-        ok = wait(smem_u32(&bar_p_full[t]), j & 1, kSitePFull);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(t, slot_addr(iv), j > 0);
-        if (j == nt - 1) mma_commit_w(smem_u32(&bar_o_done[t]));
-        if (next && j + 1 < nt) {
+        const int jt = j - start_of(t);  // the tile's own step
+        if (nt > 0 && jt >= 0) {
+          ok = wait(smem_u32(&bar_p_full[t]), jt & 1, kSitePFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, slot_addr(iv), jt > 0);
+          if (jt == nt - 1) mma_commit_w(smem_u32(&bar_o_done[t]));
+        }
+        if (next && nt > 0 && jt + 1 >= 0) {  // the tile's next step, maybe its first
           issue_qk(t, slot_addr(ik));
           mma_commit_w(smem_u32(&bar_s_full[t]));
         }
@@ -331,12 +339,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
           s[cc * 64 + 32 + i] = __uint_as_float(w[i]);
         }
       }
-      if (p.causal && p.kv_tile0 + j == p.q_tile0 + qt) {  // diagonal tile: keys after the query are masked
+      const int kvj = nt - 1 - j;  // the K/V tile of this step (see start_of)
+      if (p.causal && p.kv_tile0 + kvj == p.q_tile0 + qt) {  // diagonal tile: keys after the query are masked
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = i > r ? -INFINITY : s[i];
       }
-      if (!p.causal && (j + 1) * kTile > kv_valid) {  // padding keys of the last tile
-        const int lim = kv_valid - j * kTile;
+      if (!p.causal && (kvj + 1) * kTile > kv_valid) {  // padding keys of the last tile
+        const int lim = kv_valid - kvj * kTile;
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = i >= lim ? -INFINITY : s[i];
       }
