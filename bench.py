@@ -366,14 +366,21 @@ def kernel_names(M):
             (M.KERNEL_DQ_FINAL, "dq_finalize"))
 
 
-def launches_per_step(wl, delta="auto"):
-    """Our kernels in one step: RoPE pre-pass + forward; zeroing of the abs-max words +
-    abs-max + pre-pass (+ the exact delta pass: by default for groups above 8) + main +
-    dq finalisation."""
+def bwd_launches(rows, grads="fp32", exact_delta=False):
+    """Our kernels in one backward call over `rows` query and key rows per head: zeroing
+    of the abs-max words + abs-max + pre-pass (+ the exact delta pass) + main + dq
+    finalisation, and two dk / dv passes for bf16 gradients or padded rows."""
+    padded = rows % 128 != 0
+    return 5 + (1 if exact_delta else 0) + (2 if padded or grads == "bf16" else 0)
+
+
+def launches_per_step(wl, delta="auto", grads="fp32"):
+    """Our kernels in one step: RoPE pre-pass + forward, then the backward call's
+    (bwd_launches; the exact delta pass by default for groups above 8)."""
     if not wl.backward:
         return 2
     exact = delta == "exact" or (delta == "auto" and wl.Hq // wl.Hkv > 8)
-    return 2 + 5 + (1 if exact else 0)
+    return 2 + bwd_launches(wl.S, grads, exact)
 
 
 def roofline_of(wl, kern, peak_tf, peak_src, value):
@@ -659,7 +666,7 @@ def run_ours(args, rank, world, local):
                 "copies": "pinned host buffers; each step's inputs in and results out on two "
                           "copy streams over three device buffer sets, overlapped with "
                           "the neighbouring steps' compute"},
-        "gpu_launches": launches_per_step(wl, args.delta) * args.steps,
+        "gpu_launches": launches_per_step(wl, args.delta, args.grads) * args.steps,
         "roofline": roof,
         "prologue_roofline": prologue,
         "passes_ms": {k: round(v, 5) for k, v in passes.items()},
@@ -779,9 +786,8 @@ def run_blocks(args, rank, world, local):
                        block_pairs=len(pairs)),
         "e2e": None,
         "note": "block schedule through the partial entry points; device time only",
-        # per pair: RoPE pre-pass + forward (+ merge), zeroing + abs-max + pre-pass +
-        # main + dq finalisation
-        "gpu_launches": (2 * nfwd + (nfwd - nb) + 5 * nfwd) * args.steps,
+        # per pair: RoPE pre-pass + forward (+ merge), and a backward call
+        "gpu_launches": (2 * nfwd + (nfwd - nb) + bwd_launches(blk) * nfwd) * args.steps,
         "roofline": {"bound": "tensor", "kernel": "attn_bwd_main", "achieved": achieved,
                      "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "traffic": None, "peak_source": f"{peak_src} bf16 dense (burst)"},

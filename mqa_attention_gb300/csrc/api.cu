@@ -784,6 +784,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
        make_map(&bp.map_k, kr, krows_p, D, kTile, true) &&
        make_map(&bp.map_v, vs, krows_p, D, kTile, true) &&
        make_map_f32(&bp.map_dk, dk, krows_p, D) && make_map_f32(&bp.map_dv, dv, krows_p, D) &&
+       make_map_f32(&bp.map_dqacc, dqacc, qrows_p, D) &&
        make_map_f32(&bp.map_cos, cs, rope.u.npos, D / 2) &&
        make_map_f32(&bp.map_sin, sn, rope.u.npos, D / 2);
   if (ok) {

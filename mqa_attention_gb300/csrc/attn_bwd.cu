@@ -32,9 +32,11 @@
 //   D = 64:  dQ = dS K~ [128 queries x 64 d] once per pair of steps (the two
 //            64-query tiles of one head that follow each other), in its own
 //            64 columns, A taken from the pair's two adjacent dSᵀ buffers.
-// The dQ drain warps add the partials into an fp32 buffer with global
-// reductions. Two (Sᵀ, dPᵀ) buffers let the score MMAs of step s+2 run while
-// the softmax of step s+1 works.
+// The dQ drain warps add the partials into an fp32 buffer: at D = 128 with global
+// reductions (a lane holds one d of 64 query rows); at D = 64, where a lane holds a
+// whole query row, by staging the pair's 128 rows in shared memory and issuing one
+// TMA reduction per 32-column box. Two (Sᵀ, dPᵀ) buffers let the score MMAs of
+// step s+2 run while the softmax of step s+1 works.
 // TMEM columns: Sᵀ_0 [0,64) dPᵀ_0 [64,128) Sᵀ_1 [128,192) dPᵀ_1 [192,256), then
 //   D = 128: dV [256,384) dK [384,512);
 //   D = 64:  dQ [256,320) dV [320,384) dK [384,448), K~ [448,480) V [480,512) (fp16
@@ -64,7 +66,7 @@ constexpr int kWarpMma = 13;
 enum : int {
   kSiteKv = 17, kSiteStageFull = 18, kSiteStageEmpty = 19, kSiteSFull = 20, kSiteDsFull = 21,
   kSiteDqFull = 22, kSiteDqFree = 23, kSiteDone = 24, kSiteInject = 25, kSiteTab = 26,
-  kSiteKvTmem = 33,
+  kSiteKvTmem = 33, kSiteDqStg = 34,
   // index checks of the debug build
   kChkStage = 27, kChkKv = 28, kChkDq = 29, kChkDkdv = 30, kChkTab = 31
 };
@@ -92,7 +94,10 @@ struct BwdCfg {
   static constexpr int kVOff = kKTileBytes;
   static constexpr int kStageOff = 2 * kKTileBytes;
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kSmemBytes = kDsOff + kDsBufs * kDsBytes + 1024;
+  // D = 64: a dQ pair's 128 rows staged for the TMA reduction into the accumulator,
+  // two 128-byte swizzled boxes of 32 fp32 columns x 128 rows
+  static constexpr int kDqStgOff = kDsOff + kDsBufs * kDsBytes;
+  static constexpr int kSmemBytes = kDqStgOff + (kDqPair ? 2 * 128 * 128 : 0) + 1024;
   __device__ static constexpr uint32_t col_st(int buf) { return buf ? 128u : 0u; }
   __device__ static constexpr uint32_t col_dpt(int buf) { return buf ? 192u : 64u; }
   static constexpr uint32_t kColDQ = 256;  // D = 64 only
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   constexpr int BQ = C::BQ;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_kv, bar_done, bar_drain, bar_never, bar_tab, bar_kvt;
+  __shared__ __align__(8) uint64_t bar_stg_full, bar_stg_free;
   __shared__ __align__(8) uint64_t bar_stage_full[C::kStages], bar_stage_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_free[2];
   __shared__ uint32_t tmem_slot;
@@ -251,6 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(smem_u32(&bar_never), 1);
     mbar_init(smem_u32(&bar_tab), 1);
     mbar_init(smem_u32(&bar_kvt), 256);
+    mbar_init(smem_u32(&bar_stg_full), 128);
+    mbar_init(smem_u32(&bar_stg_free), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&bar_stage_full[s]), 1);
       mbar_init(smem_u32(&bar_stage_empty[s]), 1);
@@ -428,6 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const int r = tid & 127;  // TMEM lane: d (D = 128) or query row of the pair (D = 64)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     if constexpr (C::kDqPair) {
+      // A pair's 128 dQ rows (one per lane) go to shared memory as two 128-byte swizzled
+      // boxes of 32 fp32 columns, which the drain's first thread adds into the
+      // accumulator rows with one TMA reduction each. The boxes are rewritten once the
+      // previous pair's reductions have read them.
+      const uint32_t stg = sbase + C::kDqStgOff;
+      const bool issuer = tid == 8 * 32;
       for (int m = 0; m < n / 2; ++m) {
         const bool got =
             bounded_wait(smem_u32(&bar_dq_full[0]), m & 1, abort_ptr, p.status, kSiteDqFull);
@@ -437,45 +451,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_ld32x2(tmem + lane_base + C::kColDQ, tmem + lane_base + C::kColDQ + 32, u0, u1);
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dq_free[0]));
-        // Query rows of steps 2m, 2m+1 are consecutive rows of one head. Within
-        // each group of 8 lanes (8 rows), an 8 x 8 transpose of 16-byte chunks
-        // (three exchange stages) gives lane i chunk i of each of the 8 rows, so
-        // that every vector reduction covers 4 whole 128-byte row segments.
-        const int gl = lane & 7;
-        const long long row0 = static_cast<long long>(step_row(2 * m)) + (r & ~7);
-        const bool dq_ok = bounds_ok(row0 + 8 <= rows_q, p.status, kChkDq);
-        float* rows0 = p.dqacc + row0 * D;
+        if (m > 0) {
+          const bool free_ok = bounded_wait(smem_u32(&bar_stg_free), (m - 1) & 1, abort_ptr,
+                                            p.status, kSiteDqStg);
+          if (!__all_sync(0xffffffffu, free_ok)) break;
+        }
+        // columns 4i..4i+3 sit in 16-byte chunk i ^ (r & 7) of the row's 128 bytes
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[8][4];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[c][e] = __uint_as_float(hf ? u1[4 * c + e] : u0[4 * c + e]);
-#pragma unroll
-          for (int mk = 4; mk > 0; mk >>= 1) {
-            const bool up = (gl & mk) != 0;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              if (c & mk) continue;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                // lanes without bit mk send chunk c|mk and keep c; the others send
-                // chunk c and keep c|mk
-                const float send = up ? x[c][e] : x[c | mk][e];
-                const float got = __shfl_xor_sync(0xffffffffu, send, mk);
-                if (up) x[c][e] = got;
-                else x[c | mk][e] = got;
-              }
-            }
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t off = static_cast<uint32_t>(r * 128 + ((i ^ (r & 7)) << 4));
+          st_shared_v4(stg + off, u0[4 * i], u0[4 * i + 1], u0[4 * i + 2], u0[4 * i + 3]);
+          st_shared_v4(stg + C::kBoxBytes + off, u1[4 * i], u1[4 * i + 1], u1[4 * i + 2],
+                       u1[4 * i + 3]);
+        }
+        fence_async_smem();
+        mbar_arrive(smem_u32(&bar_stg_full));
+        if (issuer && bounded_wait(smem_u32(&bar_stg_full), m & 1, abort_ptr, p.status,
+                                   kSiteDqStg)) {
+          // query rows of steps 2m, 2m+1: consecutive rows of one head
+          const int row0 = step_row(2 * m);
+          if (bounds_ok(row0 >= 0 && row0 + 128LL <= rows_q, p.status, kChkDq)) {
+            tma_reduce_add_2d(&p.map_dqacc, 0, row0, stg);
+            tma_reduce_add_2d(&p.map_dqacc, 32, row0, stg + C::kBoxBytes);
           }
-          // now x[k] = chunk gl of row (group base + k)
-          if (dq_ok) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              red_add_v4_f32(rows0 + static_cast<long long>(k) * D + 32 * hf + 4 * gl, x[k][0],
-                             x[k][1], x[k][2], x[k][3]);
-          }
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(smem_u32(&bar_stg_free));
         }
       }
     } else {

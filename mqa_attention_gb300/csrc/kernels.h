@@ -185,6 +185,7 @@ struct BwdParams {
   CUtensorMap map_dv;  // dv (fp32) [B*Hkv*S, D], box {32, 128}
   CUtensorMap map_cos; // RoPE cos table (fp32) [positions, D/2], box {32, 128}
   CUtensorMap map_sin; // RoPE sin table, the same
+  CUtensorMap map_dqacc;  // D = 64: the dQ accumulator (fp32) [B*Hq*S, D], box {32, 128}
   const float* lse2;   // lse * log2(e), [B*Hq*S]
   const float* delta;  // scaled delta, [B*Hq*S]
   const float* maxes;  // the abs-max pass's four maxima
