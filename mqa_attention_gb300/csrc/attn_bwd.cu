@@ -439,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // A pair's 128 dQ rows (one per lane) go to shared memory as two 128-byte swizzled
       // boxes of 32 fp32 columns, which the drain's first thread adds into the
       // accumulator rows with one TMA reduction each. The boxes are rewritten once the
-      // previous pair's reductions have read them.
+      // previous pair's reductions have read them; the first thread checks that only
+      // after it has read the next pair's partials, so that the check never holds back
+      // the release of the dQ columns.
       const uint32_t stg = sbase + C::kDqStgOff;
       const bool issuer = tid == 8 * 32;
       for (int m = 0; m < n / 2; ++m) {
@@ -452,6 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_dq_free[0]));
         if (m > 0) {
+          if (issuer) {
+            bulk_wait_read_all();
+            mbar_arrive(smem_u32(&bar_stg_free));
+          }
           const bool free_ok = bounded_wait(smem_u32(&bar_stg_free), (m - 1) & 1, abort_ptr,
                                             p.status, kSiteDqStg);
           if (!__all_sync(0xffffffffu, free_ok)) break;
@@ -475,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             tma_reduce_add_2d(&p.map_dqacc, 32, row0, stg + C::kBoxBytes);
           }
           bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(smem_u32(&bar_stg_free));
         }
       }
+      // the last reductions have read the boxes before the CTA releases its shared memory
+      if (issuer) bulk_wait_read_all();
     } else {
       for (int s = 0; s < n; ++s) {
         const int buf = s & 1;
