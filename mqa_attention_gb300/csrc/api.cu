@@ -464,10 +464,11 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
   const size_t qbytes = round256(static_cast<size_t>(qrows_p) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows_p) * D * 2);
   const size_t lbytes = padded ? round256(static_cast<size_t>(qrows_p) * 4) : 0;
+  const size_t cbytes = 256;  // the forward's unit counter
   uint8_t* ws = nullptr;
   if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws),
-                              qbytes + kbytes + (padded ? kbytes + qbytes : 0) + lbytes, d->pool,
-                              stream) != cudaSuccess)
+                              qbytes + kbytes + (padded ? kbytes + qbytes : 0) + lbytes + cbytes,
+                              d->pool, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   void* qr = ws;
   void* kr = ws + qbytes;
@@ -475,6 +476,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
   void* vk = padded ? static_cast<void*>(ws + qbytes + kbytes) : const_cast<void*>(v);
   void* ok_out = padded ? static_cast<void*>(ws + qbytes + 2 * kbytes) : out;
   float* ok_lse = padded ? reinterpret_cast<float*>(ws + 2 * qbytes + 2 * kbytes) : lse;
+  int* counter = reinterpret_cast<int*>(ws + qbytes + kbytes + (padded ? kbytes + qbytes : 0) + lbytes);
 
   bool ok = true;
   {
@@ -491,6 +493,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     rp.tab_rows = rope.u.npos;
     rp.seg[0] = {q, qr, nullptr, nullptr, qrows_p, Sq, Sqp, q_pos0};
     rp.seg[1] = {k, kr, padded ? v : nullptr, padded ? vk : nullptr, krows_p, Skv, Skvp, kv_pos0};
+    rp.zero_word = counter;
     LaunchTimer tm(ATTN_KERNEL_ROPE, stream);
     ok = gbattn::launch_row_prep(rp, stream) == cudaSuccess;
     tm.done();
@@ -510,6 +513,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* out, fl
     fp.scale_log2 = scale * 1.4426950408889634f;
     fp.causal = causal ? 1 : 0;
     fp.inject_timeout = g_inject_timeout ? 1 : 0;
+    fp.unit_counter = counter;
     LaunchTimer tm(ATTN_KERNEL_FWD, stream);
     ok = gbattn::launch_fwd(fp, stream) == cudaSuccess;
     tm.done();

@@ -22,12 +22,15 @@
 // and consumed from TMEM by the P.V MMA. While one tile's softmax runs, the
 // tensor core works on the other tile's MMAs. KV tiles above the diagonal are
 // never loaded; only the diagonal tile is masked.
-// At D = 64 a CTA owns one query tile (warps 0-3 softmax, 4 producer, 5 MMA; 256
-// TMEM columns: S, then O) and two CTAs share an SM: the tensor core alternates
-// between their tiles as it does between the two tiles of one CTA at D = 128, and one
-// CTA's start (Q landing, first scores) and epilogue overlap the other's steps. At
-// the D = 64 shapes measured (S = 1024, 2048) a query tile sees 4.5-8.5 K/V tiles on
-// average, so those fixed parts would otherwise be a large share of a CTA's time.
+// At D = 64 a CTA works on one query tile at a time (warps 0-3 softmax, 4 producer, 5
+// MMA; 256 TMEM columns) and two CTAs share an SM: the tensor core alternates between
+// their tiles as it does between the two tiles of one CTA at D = 128, and one CTA's
+// fixed parts (Q landing, first scores, epilogue) overlap the other's steps. At the
+// D = 64 shapes measured (S = 1024, 2048) a query tile sees 4.5-8.5 K/V tiles on
+// average, so those fixed parts would otherwise be a large share of a tile's time.
+// The persistent form below (attn_fwd_persist_kernel) also keeps the CTAs resident
+// across tiles; the one-tile-per-CTA form remains for blocks where a query tile may
+// see no key.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -459,6 +462,387 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
   }
 }
 
+// ---------------------------------------------------------------- D = 64, persistent
+// At D = 64 a CTA's own start (the Q tile landing, ~1 µs) and the gap before the next
+// CTA takes its place (~1.2 µs) are as long as a query tile's loop of a few K/V tiles.
+// This form keeps two CTAs per SM for the whole launch. Each takes query tiles, heaviest
+// first, from a counter (its first tile is blockIdx.x) and runs them back to back.
+// The producer loads a tile's Q into one of two buffers while the previous tile still
+// streams its K/V, and the P.V products of consecutive tiles accumulate into two O
+// buffers, so a tile's epilogue (O to shared memory, TMA store) runs beside the next
+// tile's first products. A tile's Q buffer holds its output for the store.
+// Every query tile must see at least one K/V tile (the host checks that).
+struct PersistCfg {
+  static constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
+  static constexpr int kWarpLoad = 4;
+  static constexpr int kWarpMma = 5;
+  static constexpr uint32_t kTmemCols = 256;  // S [0,128), O_0 [128,192), O_1 [192,256)
+  static constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int kSlots = 4;              // K/V ring depth (tiles)
+  static constexpr int kKvOff = 2 * kTileBytes;  // after the two Q buffers
+  static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
+  __device__ static constexpr uint32_t col_o(int k) { return 128u + 64u * k; }
+  static_assert(2 * (kSmemBytes + 1024 + 1024) <= 233472, "two CTAs per SM");
+};
+enum : int { kSiteUnit = 12, kSiteUnitEmpty = 13, kSiteQEmpty = 14, kSiteOEmpty = 15, kSiteStg = 16 };
+
+__global__ void __launch_bounds__(PersistCfg::kThreads, 2)
+    attn_fwd_persist_kernel(const __grid_constant__ FwdParams p) {
+  using C = PersistCfg;
+  constexpr int D = 64;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_unit_full[2], bar_unit_empty[2], bar_q_full[2], bar_q_empty[2];
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kSlots], bar_kv_empty[C::kSlots];
+  __shared__ __align__(8) uint64_t bar_s_full, bar_p_full, bar_o_done[2], bar_o_empty[2], bar_stg;
+  __shared__ __align__(8) uint64_t bar_drain, bar_never;
+  __shared__ int unit_rec[2][2];  // (query tile unit, its K/V tiles); unit -1: none left
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int nq = p.Sq / kTile;
+  const int nkv = p.Skv / kTile;
+  const int BH = p.B * p.Hq;
+  const int units = nq * BH;
+  const int kv_valid = p.kv_valid > 0 ? p.kv_valid : p.Skv;
+  const long long rows_q = static_cast<long long>(p.B) * p.Hq * p.Sq;
+  const long long rows_kv = static_cast<long long>(p.B) * p.Hkv * p.Skv;
+  // unit u: query tile nq - 1 - u / BH of head u % BH (causal: heaviest first)
+  auto unit_qt = [&](int u) { return nq - 1 - u / BH; };
+  auto unit_bh = [&](int u) { return u % BH; };
+  auto tiles_of = [&](int u) {
+    if (!p.causal) return nkv;
+    const int vis = p.q_tile0 + unit_qt(u) - p.kv_tile0 + 1;
+    return vis < 0 ? 0 : (vis > nkv ? nkv : vis);
+  };
+  auto qbuf = [&](int k) { return sbase + (k & 1) * C::kTileBytes; };
+  auto slot_addr = [&](int i) { return sbase + C::kKvOff + (i % C::kSlots) * C::kTileBytes; };
+
+  if (warp == C::kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == C::kWarpLoad && lane == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_unit_full[s]), 1);
+      mbar_init(smem_u32(&bar_unit_empty[s]), 5);  // the MMA warp and the 4 softmax warps
+      mbar_init(smem_u32(&bar_q_full[s]), 1);
+      mbar_init(smem_u32(&bar_q_empty[s]), 1);
+      mbar_init(smem_u32(&bar_o_done[s]), 1);
+      mbar_init(smem_u32(&bar_o_empty[s]), 128);
+    }
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_p_full), 128);
+    mbar_init(smem_u32(&bar_stg), 128);
+    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_never), 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+  // Nothing above touched global memory: this prologue may overlap the kernel before
+  // it in the stream (the RoPE pre-pass, which also zeroes the unit counter).
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == C::kWarpLoad) {
+    // ================================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.map_q);
+      tma_prefetch_desc(&p.map_k);
+      tma_prefetch_desc(&p.map_v);
+      int issued = 0;    // K/V ring loads issued
+      int q_issued = 0;  // Q loads issued
+      for (int k = 0;; ++k) {
+        const int s = k & 1;
+        int u = k == 0 ? static_cast<int>(blockIdx.x)
+                       : static_cast<int>(gridDim.x) + atomicAdd(p.unit_counter, 1);
+        if (u >= units) u = -1;
+        const int n = u >= 0 ? tiles_of(u) : 0;
+        if (k >= 2 && !bounded_wait(smem_u32(&bar_unit_empty[s]), ((k >> 1) - 1) & 1, &abort_flag,
+                                    p.status, kSiteUnitEmpty))
+          break;
+        unit_rec[s][0] = u;
+        unit_rec[s][1] = n;
+        mbar_arrive(smem_u32(&bar_unit_full[s]));
+        if (u < 0) break;
+        // Q into buffer s once the store of unit k-2's output (staged there) has read it
+        if (k >= 2 && !bounded_wait(smem_u32(&bar_q_empty[s]), ((k >> 1) - 1) & 1, &abort_flag,
+                                    p.status, kSiteQEmpty))
+          break;
+        const int bh = unit_bh(u);
+        const long long qrow = static_cast<long long>(bh) * p.Sq + unit_qt(u) * kTile;
+        mbar_arrive_expect_tx(smem_u32(&bar_q_full[s]), C::kTileBytes);
+        if (bounds_ok(qrow + kTile <= rows_q, p.status, kChkQ))
+          tma_load_2d(qbuf(k), &p.map_q, 0, static_cast<int>(qrow), smem_u32(&bar_q_full[s]));
+        ++q_issued;
+        // its K/V tiles through the ring, the diagonal one first
+        const int b = bh / p.Hq;
+        const int hkv = (bh % p.Hq) / (p.Hq / p.Hkv);
+        const long long kv_row0 = static_cast<long long>(b * p.Hkv + hkv) * p.Skv;
+        bool ok = true;
+        for (int i = 0; i < 2 * n && ok; ++i, ++issued) {
+          const int slot = issued % C::kSlots;
+          ok = bounded_wait(smem_u32(&bar_kv_empty[slot]), ((issued / C::kSlots) & 1) ^ 1,
+                            &abort_flag, p.status, kSiteKvEmpty);
+          if (!ok) break;
+          const uint32_t full = smem_u32(&bar_kv_full[slot]);
+          mbar_arrive_expect_tx(full, C::kTileBytes);
+          const long long row = kv_row0 + static_cast<long long>(n - 1 - (i >> 1)) * kTile;
+          if (bounds_ok(row + kTile <= rows_kv, p.status, kChkKv))
+            tma_load_2d(slot_addr(issued), (i & 1) == 0 ? &p.map_k : &p.map_v, 0,
+                        static_cast<int>(row), full);
+        }
+        if (!ok) break;
+      }
+      // Loads already issued land before the CTA releases its shared memory (a no-op in
+      // a healthy run): at most one per ring slot and one per Q buffer is in flight.
+      for (int i = issued - C::kSlots > 0 ? issued - C::kSlots : 0; i < issued; ++i)
+        drain_wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1);
+      for (int k = q_issued - 2 > 0 ? q_issued - 2 : 0; k < q_issued; ++k)
+        drain_wait(smem_u32(&bar_q_full[k & 1]), (k >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == C::kWarpMma) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+    constexpr uint64_t kKmaj = sdesc_hi(16, 1024);
+    constexpr uint64_t kMnV = sdesc_hi(C::kTileBytes, 1024);
+    auto desc = [](uint64_t hi, uint32_t addr) { return hi | static_cast<uint64_t>(addr >> 4); };
+    auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, bounded_wait(bar, parity, abort_ptr, p.status, site));
+    };
+    auto wait_kv = [&](int i) {
+      return wait(smem_u32(&bar_kv_full[i % C::kSlots]), (i / C::kSlots) & 1, kSiteKvFull);
+    };
+    auto issue_qk = [&](uint32_t qaddr, uint32_t kaddr) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_w(tmem, desc(kKmaj, qaddr + kk * 32), desc(kKmaj, kaddr + kk * 32), idesc_qk, kk > 0);
+    };
+    auto issue_pv = [&](uint32_t ocol, uint32_t vaddr, bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts_w(tmem + ocol, tmem + kk * 8, desc(kMnV, vaddr + kk * 16 * 128), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
+    };
+    bool ok = true;
+    if (p.inject_timeout)  // nothing ever arrives on bar_never
+      ok = wait(smem_u32(&bar_never), 0, kSiteInject);
+    int i = 0;  // ring loads consumed
+    int g = 0;  // steps of all units so far (S / P barrier phases)
+    for (int k = 0; ok; ++k) {
+      const int s = k & 1;
+      ok = wait(smem_u32(&bar_unit_full[s]), (k >> 1) & 1, kSiteUnit);
+      if (!ok) break;
+      const int u = unit_rec[s][0];
+      const int n = unit_rec[s][1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_unit_empty[s]));
+      if (u < 0) break;
+      ok = wait(smem_u32(&bar_q_full[s]), (k >> 1) & 1, kSiteQ) && wait_kv(i);
+      // O_s is free once the epilogue of unit k-2 has read it
+      if (ok && k >= 2) ok = wait(smem_u32(&bar_o_empty[s]), ((k >> 1) - 1) & 1, kSiteOEmpty);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk(qbuf(k), slot_addr(i));
+      mma_commit_w(smem_u32(&bar_s_full));
+      mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
+      ++i;
+      for (int j = 0; j < n; ++j, ++g) {
+        const bool next = j + 1 < n;
+        ok = wait_kv(i) && (!next || wait_kv(i + 1)) &&
+             wait(smem_u32(&bar_p_full), g & 1, kSitePFull);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(C::col_o(s), slot_addr(i), j > 0);
+        if (!next) mma_commit_w(smem_u32(&bar_o_done[s]));
+        mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
+        ++i;
+        if (next) {
+          issue_qk(qbuf(k), slot_addr(i));
+          mma_commit_w(smem_u32(&bar_s_full));
+          mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
+          ++i;
+        }
+      }
+    }
+    // Every MMA issued above completes before the tensor memory is released.
+    mma_commit_w(smem_u32(&bar_drain));
+    drain_wait(smem_u32(&bar_drain), 0);
+    __syncwarp();
+  } else {
+    // ================================================================ softmax
+    const int r = tid;  // row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base;
+    const float sl2 = p.scale_log2;
+    int g = 0;
+    // thread 0: 1 + the buffer of a store whose shared-memory reads may be in flight, or 0;
+    // once they are done the buffer may take a Q tile
+    int pending = 0;
+    auto release = [&]() {
+      if (pending) {
+        bulk_wait_read_all();
+        mbar_arrive(smem_u32(&bar_q_empty[pending - 1]));
+        pending = 0;
+      }
+    };
+    for (int k = 0;; ++k) {
+      const int s = k & 1;
+      const bool have = bounded_wait(smem_u32(&bar_unit_full[s]), (k >> 1) & 1, abort_ptr, p.status,
+                                     kSiteUnit);
+      if (!__all_sync(0xffffffffu, have)) break;
+      const int u = unit_rec[s][0];
+      const int n = unit_rec[s][1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_unit_empty[s]));
+      if (u < 0) break;
+      const int qt = unit_qt(u);
+      const uint32_t tO = tmem + lane_base + C::col_o(s);
+      float m = -INFINITY;  // running maximum, base-2 units (scores * scale * log2 e)
+      float l = 0.f;        // running sum of 2^(score2 - m)
+      bool ok = true;
+      for (int j = 0; j < n; ++j, ++g) {
+        const bool got = bounded_wait(smem_u32(&bar_s_full), g & 1, abort_ptr, p.status, kSiteSFull);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sc[128];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t a[32], w[32];
+          tmem_ld32x2(tS + cc * 64, tS + cc * 64 + 32, a, w);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            sc[cc * 64 + e] = __uint_as_float(a[e]);
+            sc[cc * 64 + 32 + e] = __uint_as_float(w[e]);
+          }
+        }
+        const int kvj = n - 1 - j;  // the K/V tile of this step (diagonal first)
+        if (p.causal && p.kv_tile0 + kvj == p.q_tile0 + qt) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e) sc[e] = e > r ? -INFINITY : sc[e];
+        }
+        if (!p.causal && (kvj + 1) * kTile > kv_valid) {  // padding keys of the last tile
+          const int lim = kv_valid - kvj * kTile;
+#pragma unroll
+          for (int e = 0; e < 128; ++e) sc[e] = e >= lim ? -INFINITY : sc[e];
+        }
+        float mp[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mp[q] = fmaxf(sc[q], sc[q + 4]);
+#pragma unroll
+        for (int e = 8; e < 128; e += 8)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mp[q] = fmax3(mp[q], sc[e + q], sc[e + 4 + q]);
+        const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), mp[3], mp[3]);
+        const float mx2 = mx * sl2;
+        float alpha = 1.f;
+        bool grew = false;
+        // lazy rescaling, as in the kernel above (threshold 2^8)
+        if (mx2 > m + 8.f) {
+          alpha = ex2(m - mx2);
+          grew = true;
+          m = mx2;
+        }
+        float2 rp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+        const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m, -m);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 x =
+                ffma2(make_float2(sc[hh * 64 + 2 * e], sc[hh * 64 + 2 * e + 1]), sl2x2, negm);
+            const float2 a = make_float2(ex2(x.x), ex2(x.y));
+            rp[e & 3] = fadd2(rp[e & 3], a);
+            pk[e] = pack_bf16(a.x, a.y);
+          }
+          tmem_st32(tS + hh * 32, pk);
+        }
+        const float2 r2 = fadd2(fadd2(rp[0], rp[1]), fadd2(rp[2], rp[3]));
+        l = l * alpha + (r2.x + r2.y);
+        if (j > 0 && __any_sync(0xffffffffu, grew)) {
+          const float f = grew ? alpha : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full));
+        if (j == 0 && tid == 0) release();  // the previous unit's store, behind this step
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      const bool done = bounded_wait(smem_u32(&bar_o_done[s]), (k >> 1) & 1, abort_ptr, p.status,
+                                     kSiteODone);
+      if (!__all_sync(0xffffffffu, done)) break;
+      tc_fence_after();
+      uint32_t o[2][32];
+      tmem_ld32x2(tO, tO + 32, o[0], o[1]);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_o_empty[s]));
+      const float inv_l = 1.f / l;
+      const uint32_t obuf = qbuf(k);  // the unit's Q tile: its last score product is done
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(o[h][8 * q4 + 2 * e]) * inv_l,
+                             __uint_as_float(o[h][8 * q4 + 2 * e + 1]) * inv_l);
+          st_shared_v4(obuf + sw128_offset(r, 4 * h + q4), w[0], w[1], w[2], w[3]);
+        }
+      fence_async_smem();
+      mbar_arrive(smem_u32(&bar_stg));
+      const long long qrow = static_cast<long long>(unit_bh(u)) * p.Sq + qt * kTile;
+      if (tid == 0) {
+        release();
+        if (bounded_wait(smem_u32(&bar_stg), k & 1, abort_ptr, p.status, kSiteStg)) {
+          if (bounds_ok(qrow + kTile <= rows_q, p.status, kChkOut))
+            tma_store_2d(&p.map_out, 0, static_cast<int>(qrow), obuf);
+          bulk_commit();
+          pending = 1 + s;
+        }
+      }
+      if (bounds_ok(qrow + r < rows_q, p.status, kChkLse)) p.lse[qrow + r] = (m + log2f(l)) * kLn2;
+    }
+    // the last store has read its buffer before the CTA releases its shared memory
+    if (tid == 0 && pending) bulk_wait_read_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -473,7 +857,23 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
-  return p.D == 128 ? launch_fwd_d<128>(p, stream) : launch_fwd_d<64>(p, stream);
+  if (p.D == 128) return launch_fwd_d<128>(p, stream);
+  // the persistent form needs the unit counter and a key tile for every query tile
+  if (p.unit_counter != nullptr && (!p.causal || p.q_tile0 >= p.kv_tile0) && p.Skv >= kTile) {
+    using C = PersistCfg;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_persist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    const long long units = static_cast<long long>(p.Sq / kTile) * p.B * p.Hq;
+    const unsigned grid = static_cast<unsigned>(units < 2LL * nsm ? units : 2LL * nsm);
+    return launch_pdl(attn_fwd_persist_kernel, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
+                      stream, p);
+  }
+  return launch_fwd_d<64>(p, stream);
 }
 
 }  // namespace gbattn

@@ -135,6 +135,7 @@ struct RowPrepParams {
   float* dv_zero;
   int dk_zero_rows;  // with dk_zero: rows [0, dk_zero_rows) of each head are zeroed
   int* status;       // device status word (a wait that expired)
+  int* zero_word;    // forward: set to 0 (the next forward launch's unit counter), or null
 };
 cudaError_t launch_row_prep(const RowPrepParams& p, cudaStream_t stream);
 
@@ -172,6 +173,9 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int inject_timeout;
+  // D = 64: query tiles handed out to the persistent CTAs beyond their first (zeroed by
+  // the RoPE pre-pass before the launch); null: one CTA per query tile
+  int* unit_counter;
 };
 cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream);
 

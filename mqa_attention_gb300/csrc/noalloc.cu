@@ -98,14 +98,15 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   if (static_cast<long long>(B) * Hq * S >= (1LL << 31)) return ATTN_ERR_INVALID;
   if ((D != 64 && D != 128) || S % gbattn::kTile != 0) return ATTN_ERR_UNSUPPORTED;
 
-  // Scratch layout: table (cos hi | sin hi | cos lo | sin lo) | rotated q | rotated k.
+  // Scratch layout: table (cos hi | sin hi | cos lo | sin lo) | rotated q | rotated k |
+  // the forward's unit counter (256 bytes).
   const long long qrows = static_cast<long long>(B) * Hq * S;
   const long long krows = static_cast<long long>(B) * Hkv * S;
   const long long tab_n = (static_cast<long long>(S) * (D / 2) + 63) / 64 * 64;  // floats per array
   const size_t tab = static_cast<size_t>(tab_n) * sizeof(float);
   const size_t qbytes = round256(static_cast<size_t>(qrows) * D * 2);
   const size_t kbytes = round256(static_cast<size_t>(krows) * D * 2);
-  const size_t need = 4 * tab + qbytes + kbytes;
+  const size_t need = 4 * tab + qbytes + kbytes + 256;
   if (need > kScratchBytes) return ATTN_ERR_UNSUPPORTED;  // beyond the fixed array
 
   int dev = 0, major = 0, minor = 0;
@@ -125,6 +126,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   float* tabp = reinterpret_cast<float*>(w);
   void* qr = w + 4 * tab;
   void* kr = w + 4 * tab + qbytes;
+  int* counter = reinterpret_cast<int*>(w + 4 * tab + qbytes + kbytes);
 
   bool ok = gbattn::launch_rope_table(tabp, tab_n, S, D, static_cast<double>(rope_theta),
                                       stream) == cudaSuccess;
@@ -139,6 +141,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   rp.tab_rows = S;
   rp.seg[0] = {q, qr, nullptr, nullptr, qrows, S, S, 0};
   rp.seg[1] = {k, kr, nullptr, nullptr, krows, S, S, 0};
+  rp.zero_word = counter;
   ok = ok && gbattn::launch_row_prep(rp, stream) == cudaSuccess;
   gbattn::FwdParams fp{};
   ok = ok && map_bf16(&fp.map_q, qr, qrows, D) && map_bf16(&fp.map_k, kr, krows, D) &&
@@ -152,5 +155,6 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   fp.scale_log2 = scale * 1.4426950408889634f;
   fp.causal = causal ? 1 : 0;
   fp.inject_timeout = 0;
+  fp.unit_counter = counter;
   return gbattn::launch_fwd(fp, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

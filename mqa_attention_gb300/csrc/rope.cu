@@ -196,6 +196,7 @@ template <int D, bool kBwd, bool kPad>
 __global__ void __launch_bounds__(256) row_prep_kernel(const RowPrepParams p) {
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
+  if (p.zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *p.zero_word = 0;
   constexpr int T = D / 16;  // threads per row
   constexpr int H = D / 2;
   const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -404,6 +405,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) row_prep_exact_kernel(const R
   __syncthreads();
   gb::pdl_wait();  // the previous kernel in the stream has completed
   gb::pdl_launch_dependents();
+  if (p.zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *p.zero_word = 0;
 
   if (tid >= kPrepCompute) {
     // ================================================================ producer
