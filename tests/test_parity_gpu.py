@@ -105,11 +105,12 @@ SMALL = [
     (1, 48, 1, 256, 128, True),
     (2, 2, 1, 256, 64, False),
     (1, 4, 2, 384, 128, False),
-    # more steps than SMs: CTAs of the persistent backward cross key-tile units,
-    # some units whole in one CTA, others split between two
+    # more key-tile units than SMs, the heaviest split between two CTAs
     (2, 8, 2, 1024, 64, True),
     (1, 8, 8, 1536, 128, True),
     (1, 4, 2, 1152, 128, False),
+    # 1024 query tiles at D = 64: each persistent forward CTA (two per SM) takes several
+    (8, 64, 8, 256, 64, True),
 ]
 
 
