@@ -110,7 +110,8 @@ SMALL = [
     (1, 8, 8, 1536, 128, True),
     (1, 4, 2, 1152, 128, False),
     # 1024 query tiles at D = 64: each persistent forward CTA (two per SM) takes several
-    (8, 64, 8, 256, 64, True),
+    # (MHA: with G = 8 over 512 heads the two oracle readings alone differ by 0.018 in dk)
+    (8, 64, 64, 256, 64, True),
 ]
 
 
