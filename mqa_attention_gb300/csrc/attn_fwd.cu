@@ -468,20 +468,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, FwdCfg<D>::kMinBlocks)
 // This form keeps two CTAs per SM for the whole launch. Each takes query tiles, heaviest
 // first, from a counter (its first tile is blockIdx.x) and runs them back to back.
 // The producer loads a tile's Q into one of two buffers while the previous tile still
-// streams its K/V, and the P.V products of consecutive tiles accumulate into two O
-// buffers, so a tile's epilogue (O to shared memory, TMA store) runs beside the next
-// tile's first products. A tile's Q buffer holds its output for the store.
+// streams its K/V. P has tensor-memory columns of its own (S [0,128), P [128,192), O
+// [192,256)), so the scores of the next K/V tile are computed as soon as the softmax
+// has read the current ones into registers, beside its exponentials, instead of after
+// the P.V product. A tile's Q buffer holds its output for the store.
 // Every query tile must see at least one K/V tile (the host checks that).
 struct PersistCfg {
   static constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
   static constexpr int kWarpLoad = 4;
   static constexpr int kWarpMma = 5;
-  static constexpr uint32_t kTmemCols = 256;  // S [0,128), O_0 [128,192), O_1 [192,256)
+  static constexpr uint32_t kTmemCols = 256;  // S [0,128), P [128,192) (bf16), O [192,256)
   static constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
   static constexpr int kSlots = 4;              // K/V ring depth (tiles)
   static constexpr int kKvOff = 2 * kTileBytes;  // after the two Q buffers
   static constexpr int kSmemBytes = kKvOff + kSlots * kTileBytes + 1024;
-  __device__ static constexpr uint32_t col_o(int k) { return 128u + 64u * k; }
+  static constexpr uint32_t kColP = 128;
+  static constexpr uint32_t kColO = 192;
   static_assert(2 * (kSmemBytes + 1024 + 1024) <= 233472, "two CTAs per SM");
 };
 enum : int { kSiteUnit = 12, kSiteUnitEmpty = 13, kSiteQEmpty = 14, kSiteOEmpty = 15, kSiteStg = 16 };
@@ -493,7 +495,8 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_unit_full[2], bar_unit_empty[2], bar_q_full[2], bar_q_empty[2];
   __shared__ __align__(8) uint64_t bar_kv_full[C::kSlots], bar_kv_empty[C::kSlots];
-  __shared__ __align__(8) uint64_t bar_s_full, bar_p_full, bar_o_done[2], bar_o_empty[2], bar_stg;
+  __shared__ __align__(8) uint64_t bar_s_full, bar_s_free, bar_p_full, bar_p_free;
+  __shared__ __align__(8) uint64_t bar_o_done, bar_o_empty, bar_stg;
   __shared__ __align__(8) uint64_t bar_drain, bar_never;
   __shared__ int unit_rec[2][2];  // (query tile unit, its K/V tiles); unit -1: none left
   __shared__ uint32_t tmem_slot;
@@ -532,15 +535,17 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
       mbar_init(smem_u32(&bar_unit_empty[s]), 5);  // the MMA warp and the 4 softmax warps
       mbar_init(smem_u32(&bar_q_full[s]), 1);
       mbar_init(smem_u32(&bar_q_empty[s]), 1);
-      mbar_init(smem_u32(&bar_o_done[s]), 1);
-      mbar_init(smem_u32(&bar_o_empty[s]), 128);
     }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(smem_u32(&bar_kv_full[s]), 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_s_free), 128);
     mbar_init(smem_u32(&bar_p_full), 128);
+    mbar_init(smem_u32(&bar_p_free), 1);
+    mbar_init(smem_u32(&bar_o_done), 1);
+    mbar_init(smem_u32(&bar_o_empty), 128);
     mbar_init(smem_u32(&bar_stg), 128);
     mbar_init(smem_u32(&bar_drain), 1);
     mbar_init(smem_u32(&bar_never), 1);
@@ -632,17 +637,28 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss_w(tmem, desc(kKmaj, qaddr + kk * 32), desc(kKmaj, kaddr + kk * 32), idesc_qk, kk > 0);
     };
-    auto issue_pv = [&](uint32_t ocol, uint32_t vaddr, bool acc) {
+    auto issue_pv = [&](uint32_t vaddr, bool acc) {
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_ts_w(tmem + ocol, tmem + kk * 8, desc(kMnV, vaddr + kk * 16 * 128), idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
+        mma_ts_w(tmem + C::kColO, tmem + C::kColP + kk * 8, desc(kMnV, vaddr + kk * 16 * 128),
+                 idesc_pv, (acc || kk > 0) ? 1u : 0u);
     };
     bool ok = true;
     if (p.inject_timeout)  // nothing ever arrives on bar_never
       ok = wait(smem_u32(&bar_never), 0, kSiteInject);
-    int i = 0;  // ring loads consumed
-    int g = 0;  // steps of all units so far (S / P barrier phases)
+    int base = 0;  // ring load of the unit's first K tile (K_j at base + 2j, V_j at base + 2j + 1)
+    int g = 0;     // K/V tiles of all units so far (barrier phases of S and P)
+    // scores of step g into S once the softmax has read step g - 1's
+    auto issue_s = [&](uint32_t qaddr, int ring) {
+      bool w = g == 0 || wait(smem_u32(&bar_s_free), (g - 1) & 1, kSiteSFull);
+      w = w && wait_kv(ring);
+      if (!w) return false;
+      tc_fence_after();
+      issue_qk(qaddr, slot_addr(ring));
+      mma_commit_w(smem_u32(&bar_s_full));
+      mma_commit_w(smem_u32(&bar_kv_empty[ring % C::kSlots]));
+      return true;
+    };
     for (int k = 0; ok; ++k) {
       const int s = k & 1;
       ok = wait(smem_u32(&bar_unit_full[s]), (k >> 1) & 1, kSiteUnit);
@@ -652,32 +668,29 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_unit_empty[s]));
       if (u < 0) break;
-      ok = wait(smem_u32(&bar_q_full[s]), (k >> 1) & 1, kSiteQ) && wait_kv(i);
-      // O_s is free once the epilogue of unit k-2 has read it
-      if (ok && k >= 2) ok = wait(smem_u32(&bar_o_empty[s]), ((k >> 1) - 1) & 1, kSiteOEmpty);
+      ok = wait(smem_u32(&bar_q_full[s]), (k >> 1) & 1, kSiteQ) && issue_s(qbuf(k), base);
       if (!ok) break;
-      tc_fence_after();
-      issue_qk(qbuf(k), slot_addr(i));
-      mma_commit_w(smem_u32(&bar_s_full));
-      mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
-      ++i;
-      for (int j = 0; j < n; ++j, ++g) {
-        const bool next = j + 1 < n;
-        ok = wait_kv(i) && (!next || wait_kv(i + 1)) &&
-             wait(smem_u32(&bar_p_full), g & 1, kSitePFull);
+      for (int j = 0; j < n; ++j) {
+        // the next tile's scores first: they need only the softmax's read of these
+        if (j + 1 < n) {
+          ++g;
+          ok = issue_s(qbuf(k), base + 2 * j + 2);
+          --g;
+          if (!ok) break;
+        }
+        const int iv = base + 2 * j + 1;
+        ok = wait_kv(iv) && wait(smem_u32(&bar_p_full), g & 1, kSitePFull);
+        // O is free once the previous unit's epilogue has read it
+        if (ok && j == 0 && k > 0) ok = wait(smem_u32(&bar_o_empty), (k - 1) & 1, kSiteOEmpty);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(C::col_o(s), slot_addr(i), j > 0);
-        if (!next) mma_commit_w(smem_u32(&bar_o_done[s]));
-        mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
-        ++i;
-        if (next) {
-          issue_qk(qbuf(k), slot_addr(i));
-          mma_commit_w(smem_u32(&bar_s_full));
-          mma_commit_w(smem_u32(&bar_kv_empty[i % C::kSlots]));
-          ++i;
-        }
+        issue_pv(slot_addr(iv), j > 0);
+        mma_commit_w(smem_u32(&bar_p_free));
+        if (j + 1 == n) mma_commit_w(smem_u32(&bar_o_done));
+        mma_commit_w(smem_u32(&bar_kv_empty[iv % C::kSlots]));
+        ++g;
       }
+      base += 2 * n;
     }
     // Every MMA issued above completes before the tensor memory is released.
     mma_commit_w(smem_u32(&bar_drain));
@@ -711,7 +724,8 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
       if (lane == 0) mbar_arrive(smem_u32(&bar_unit_empty[s]));
       if (u < 0) break;
       const int qt = unit_qt(u);
-      const uint32_t tO = tmem + lane_base + C::col_o(s);
+      const uint32_t tO = tmem + lane_base + C::kColO;
+      const uint32_t tP = tmem + lane_base + C::kColP;
       float m = -INFINITY;  // running maximum, base-2 units (scores * scale * log2 e)
       float l = 0.f;        // running sum of 2^(score2 - m)
       bool ok = true;
@@ -733,6 +747,9 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
             sc[cc * 64 + 32 + e] = __uint_as_float(w[e]);
           }
         }
+        // the scores are in registers: the MMA warp may compute the next ones into S
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_s_free));
         const int kvj = n - 1 - j;  // the K/V tile of this step (diagonal first)
         if (p.causal && p.kv_tile0 + kvj == p.q_tile0 + qt) {
 #pragma unroll
@@ -774,8 +791,19 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
             rp[e & 3] = fadd2(rp[e & 3], a);
             pk[e] = pack_bf16(a.x, a.y);
           }
-          tmem_st32(tS + hh * 32, pk);
+          // P and O are free once the previous step's P.V product has completed
+          if (hh == 0 && g > 0) {
+            const bool pf =
+                bounded_wait(smem_u32(&bar_p_free), (g - 1) & 1, abort_ptr, p.status, kSitePFull);
+            if (!__all_sync(0xffffffffu, pf)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(tP + hh * 32, pk);
         }
+        if (!ok) break;
         const float2 r2 = fadd2(fadd2(rp[0], rp[1]), fadd2(rp[2], rp[3]));
         l = l * alpha + (r2.x + r2.y);
         if (j > 0 && __any_sync(0xffffffffu, grew)) {
@@ -796,14 +824,13 @@ __global__ void __launch_bounds__(PersistCfg::kThreads, 2)
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      const bool done = bounded_wait(smem_u32(&bar_o_done[s]), (k >> 1) & 1, abort_ptr, p.status,
-                                     kSiteODone);
+      const bool done = bounded_wait(smem_u32(&bar_o_done), k & 1, abort_ptr, p.status, kSiteODone);
       if (!__all_sync(0xffffffffu, done)) break;
       tc_fence_after();
       uint32_t o[2][32];
       tmem_ld32x2(tO, tO + 32, o[0], o[1]);
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_o_empty[s]));
+      mbar_arrive(smem_u32(&bar_o_empty));
       const float inv_l = 1.f / l;
       const uint32_t obuf = qbuf(k);  // the unit's Q tile: its last score product is done
 #pragma unroll
