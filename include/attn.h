@@ -282,7 +282,7 @@ const char* attn_version(void);
  * attn_fwd's pooled workspace and cached RoPE tables it uses one fixed array of
  * ATTN_FWD_NOALLOC_SCRATCH_BYTES in device memory that the CUDA runtime reserves on
  * every GPU where the library's code is loaded and keeps until the process exits.
- * Limit: 16*ceil64(S*D/2) + round256(2*B*Hq*S*D) + round256(2*B*Hkv*S*D) bytes
+ * Limit: 16*ceil64(S*D/2) + round256(2*B*Hq*S*D) + round256(2*B*Hkv*S*D) + 256 bytes
  * (ceil64: rounded up to a multiple of 64) must fit in that array (e.g. B=1, Hq=32,
  * Hkv=8, S=4096, D=128 needs 46 MB); larger problems return ATTN_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address (with that
