@@ -113,20 +113,23 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when
-    the record is for another workload or the kernel source changed since."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu records
+    (one record, or a list of them, per kernel), or None when there is no record for
+    that workload or the kernel source changed since it was taken."""
     import hashlib
 
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        h = hashlib.sha256()
-        for src in rec["sources"]:
-            with open(os.path.join(ROOT, src), "rb") as f:
-                h.update(f.read())
-        if rec["workload"] != workload or h.hexdigest()[:16] != rec["source_sha256_16"]:
-            return None
-        return float(rec["bytes"])
+            recs = json.load(f)[kernel]
+        for rec in recs if isinstance(recs, list) else [recs]:
+            if rec["workload"] != workload:
+                continue
+            h = hashlib.sha256()
+            for src in rec["sources"]:
+                with open(os.path.join(ROOT, src), "rb") as f:
+                    h.update(f.read())
+            return float(rec["bytes"]) if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+        return None
     except Exception:
         return None
 

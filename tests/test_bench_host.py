@@ -20,11 +20,13 @@ def test_traffic_records_match_their_sources():
     unchanged, and only for the workload it was captured on."""
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
-    for kernel, r in rec.items():
+    for kernel, recs in rec.items():
         if kernel.startswith("_"):
             continue
-        got = bench.ncu_traffic(kernel, r["workload"])
-        assert got == float(r["bytes"]), (kernel, "source hash no longer matches the record")
+        for r in recs if isinstance(recs, list) else [recs]:
+            got = bench.ncu_traffic(kernel, r["workload"])
+            assert got == float(r["bytes"]), (kernel, r["workload"],
+                                              "source hash no longer matches the record")
         assert bench.ncu_traffic(kernel, "tiny_mqa_fwd") is None
 
 
