@@ -55,3 +55,18 @@ def test_reference_arm_prints_one_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["config"]["workload"] == "palm_mqa_s2048"
+
+
+def test_launch_accounting():
+    """gpu_launches counts the library's kernels per step: RoPE pre-pass + forward, then
+    zeroing of the abs-max words, abs-max, row pass, main kernel and dq finalisation; the
+    exact delta pass by default above 8 query heads per K/V head; two dk / dv passes for
+    bf16 gradients or padded rows; the forward-only workload two."""
+    llama = by_name("llama3_8b_gqa_s4096")
+    assert bench.launches_per_step(llama) == 7
+    assert bench.launches_per_step(llama, "exact") == 8
+    assert bench.launches_per_step(llama, "auto", "bf16") == 9
+    assert bench.launches_per_step(by_name("tiny_mqa_fwd")) == 2
+    assert bench.bwd_launches(4096) == 5
+    assert bench.bwd_launches(1000) == 7
+    assert bench.bwd_launches(4096, "bf16", True) == 8
