@@ -51,6 +51,7 @@ def check_lse(got, want):
 FWD_CASES = [
     # (B, Hq, Hkv, Sq, Skv, D, q_pos0, kv_pos0, causal)
     (1, 4, 2, 256, 384, 128, 384, 0, True),    # keys all before the queries: no mask
+    (1, 4, 2, 256, 384, 64, 384, 0, True),     # the same at D = 64 (persistent forward)
     (1, 4, 1, 256, 256, 64, 256, 256, True),   # the diagonal block
     (1, 2, 2, 384, 256, 128, 0, 128, True),    # keys partly after: query tile 0 sees none
     (1, 2, 2, 384, 256, 64, 0, 128, True),     # the same at D = 64 (one query tile per CTA)
