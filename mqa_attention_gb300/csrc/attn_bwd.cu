@@ -41,7 +41,7 @@
 //   D = 128: dV [256,384) dK [384,512);
 //   D = 64:  dQ [256,320) dV [320,384) dK [384,448), K~ [448,480) V [480,512) (fp16
 //            pairs, copied from shared memory by the softmax warps at the start).
-// Q~/dO tiles (with lse2 and delta) arrive through a TMA ring of 3 stages (4 at D = 64).
+// Q~/dO tiles (with lse2 and delta) arrive through a TMA ring of 3 stages (5 at D = 64).
 // All products run in fp16 (kind::f16 with fp16 A and B): the operands q~, k~,
 // v, dO arrive from the pre-pass multiplied by exact powers of two (q~ and k~
 // hold their bf16-rounded values, so the recomputed scores equal the
@@ -84,9 +84,9 @@ struct BwdCfg {
   // that the score products Sᵀ = K~ Q~ᵀ and dPᵀ = V dOᵀ read their A operand from
   // there rather than from shared memory, whose bandwidth the N = 64 products
   // otherwise spend on re-reading K~ and V every step; the freed bandwidth also buys a
-  // fourth Q~/dO stage.
+  // fourth and a fifth Q~/dO stage.
   static constexpr bool kKvTmem = D == 64;
-  static constexpr int kStages = kKvTmem ? 4 : 3;
+  static constexpr int kStages = kKvTmem ? 5 : 3;
   static constexpr int kStageBytes = ((2 * kQTileBytes + 2 * BQ * 4) + 1023) / 1024 * 1024;
   static constexpr int kDsBufs = kDqPair ? 4 : 2;  // dSᵀ buffers (pairs stay adjacent)
   static constexpr int kDsBytes = 16384;           // dSᵀ: 128 key rows x 64 queries fp16
